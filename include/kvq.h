@@ -1,0 +1,211 @@
+/*
+ * kvq.h -- C ABI of the rotated 4-bit KV-cache decode path (GB300, sm_103a).
+ *
+ * Method: "Serving Kolibri-1 with a 4-bit KV cache" (sevren.ai), section "What we do":
+ * every key of a full-attention layer is rotated by a fixed randomized Hadamard matrix
+ * R = H diag(s)/sqrt(128) after its RMS norm, stored as 4-bit codes with one fp16 scale
+ * and one fp16 offset per token and head (4.25 bits per number); values are stored the
+ * same way without rotation; queries are rotated by the same R with both QK-norm gains
+ * folded in, and decode attention reads the 4-bit codes directly. The 40 sliding-window
+ * layers (window 513) keep a stock FP8 e4m3 cache, read by the same kernel family.
+ *
+ * Conventions for every entry point:
+ *  - All pointers are owned by the caller; the library allocates nothing. Pointers
+ *    documented as "device" must be device-accessible memory of the current device;
+ *    "host" pointers are ordinary CPU memory.
+ *  - Calls taking a stream are asynchronous on that stream and never synchronise.
+ *  - Host-side checks run first; on failure the call returns a non-zero kvq_status and
+ *    launches nothing.
+ *  - Problems only visible on the device (a block-table entry outside the page pool, a
+ *    position beyond capacity, a non-finite input, an fp16 scale or offset that had to
+ *    saturate, a bounded wait that gave up) are OR-ed into *dev_err as KVQ_DEVERR_* bits;
+ *    the affected token-heads or pages are skipped. Kernels never trap and never spin
+ *    without a time limit. The caller reads *dev_err after synchronising.
+ *  - Fixed geometry: head_dim 128, 64 tokens per page.
+ *  - Thread-safe: no mutable global state beyond per-device attribute caches.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer, workspace too small */
+  KVQ_ERR_UNSUPPORTED = 2, /* head_dim != 128, page_size != 64, S outside 1..8, too many rows */
+  KVQ_ERR_CUDA = 3         /* a CUDA runtime call or launch failed */
+} kvq_status;
+
+typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
+
+#define KVQ_HEAD_DIM 128
+#define KVQ_PAGE_SIZE 64
+#define KVQ_MAX_SEQS 1024
+
+/* bits of *dev_err */
+#define KVQ_DEVERR_PAGE 0x1      /* block-table entry outside [0, num_pages) */
+#define KVQ_DEVERR_POS 0x2       /* sequence id or position outside the cache */
+#define KVQ_DEVERR_NONFINITE 0x4 /* NaN/Inf in a key, value or query row (row skipped) */
+#define KVQ_DEVERR_RANGE 0x8     /* fp16 scale or offset saturated at +-65504 */
+#define KVQ_DEVERR_TIMEOUT 0x10  /* a bounded wait on a copy gave up (results invalid) */
+
+/*
+ * Paged int4 cache of one full-attention layer.
+ * Physical layout (all byte offsets from the given base pointers):
+ *   k_codes, v_codes: [num_pages][num_kv_heads][64 tokens][64 bytes]
+ *     record byte b holds code 2b in its low nibble and code 2b+1 in its high nibble.
+ *     k_codes records are stored as is. In v_codes the four 16-byte chunks of the record
+ *     of token slot t (0..63 within its page) are stored in XOR order: logical chunk c at
+ *     physical chunk c ^ ((t >> 1) & 3), so a transposing shared-memory read of eight
+ *     consecutive tokens touches eight distinct bank groups.
+ *   k_meta, v_meta:   [num_pages][num_kv_heads][64 tokens] uint32:
+ *     bits 0..15 the fp16 scale, bits 16..31 the fp16 offset; value = code*scale + offset.
+ *   block_table:      [num_seqs][max_pages_per_seq] int32 (device): physical page of
+ *     logical page p of sequence q; position `pos` lives in page pos/64, slot pos%64.
+ * All four data pointers must be 16-byte aligned (device).
+ */
+typedef struct kvq_int4_cache {
+  uint8_t* k_codes;
+  uint32_t* k_meta;
+  uint8_t* v_codes;
+  uint32_t* v_meta;
+  const int32_t* block_table;
+  int32_t num_seqs;
+  int32_t max_pages_per_seq;
+  int32_t num_pages;
+  int32_t num_kv_heads;
+  int32_t page_size; /* must be 64 */
+  int32_t head_dim;  /* must be 128 */
+} kvq_int4_cache;
+
+/*
+ * FP8 e4m3 ring cache of one sliding-window layer (stock format: one fp32 scale per
+ * tensor). Position `pos` of sequence q, head h lives in slot pos % capacity:
+ *   k, v: [num_seqs][num_kv_heads][capacity][128] bytes (device, 16-byte aligned),
+ *   the eight 16-byte chunks of the record in slot t stored at physical chunk c ^ (t & 7).
+ * capacity must be a multiple of 64 and at least window + S - 1 for the calls using it.
+ */
+typedef struct kvq_fp8_ring {
+  uint8_t* k;
+  uint8_t* v;
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t capacity;
+  int32_t head_dim; /* must be 128 */
+} kvq_fp8_ring;
+
+/* Human-readable name of a status code (static string). */
+const char* kvq_status_string(kvq_status status);
+
+/*
+ * kvq_build_rotation -- section "What we do": R = H diag(s)/sqrt(128), H the Sylvester
+ * Hadamard matrix, s a random sign per column: s[j] = +1 when the top bit of the j-th
+ * output of splitmix64 seeded with `seed` is 0, else -1. Entries computed in fp64 and
+ * rounded to fp32.
+ *   s_out: host int8[head_dim] (may be NULL); R_out: host float[head_dim*head_dim], row-major.
+ * Returns KVQ_ERR_UNSUPPORTED unless head_dim == 128, KVQ_ERR_INVALID_ARG if R_out is NULL.
+ */
+kvq_status kvq_build_rotation(uint64_t seed, int head_dim, int8_t* s_out, float* R_out);
+
+/*
+ * kvq_fold_qk -- section "What we do", QK-norm gain folding: scores depend only on q.k,
+ * so g_k moves to the query side and the cache holds R n(k):
+ *   M_q = R diag(g_q * g_k)  (each entry the fp64 product R[j][i]*(g_q[i]*g_k[i]) rounded
+ *   once to fp32),  M_k = R.
+ *   R, g_q, g_k: host inputs (row-major R); Mq_out, Mk_out: host float[128*128] outputs.
+ */
+kvq_status kvq_fold_qk(const float* R, const float* g_q, const float* g_k, int head_dim, float* Mq_out,
+                       float* Mk_out);
+
+/*
+ * kvq_rotate_quant_append -- section "What we do": keys rotated (with their RMS norm) by
+ * M_k and values unrotated, each quantised to 4-bit codes with fp16 scale/offset per
+ * token and head, written into the page slot of (seq_ids[t], positions[t]).
+ *   Mk:        device float[128*128] row-major (y = M_k n(k)).
+ *   k, v:      device [T][num_kv_heads][128] of `dtype` (pre-norm keys, raw values).
+ *   seq_ids, positions: device int32[T].
+ * Arithmetic (bit-exact specification, fp32, IEEE operations in this order):
+ *   lanes l=0..31 hold x[4l..4l+3]; t_l = fma(x3,x3,fma(x2,x2,fma(x1,x1,x0*x0)));
+ *   t_l <- t_l + t_(l^o) for o = 16,8,4,2,1; inv = 1/sqrt(t/128 + eps); n = x*inv;
+ *   y_j = fma chain over i=0..127 of M[j][i]*n_i;
+ *   o = fp16 toward -inf of min(y) (+0 for a zero); s = fp16 toward +inf of (max(y)-o)/15;
+ *   code_i = 0 if s == 0 else clamp(round_half_even((y_i - o)/s), 0, 15).
+ * Values use the same quantiser on the raw row. T == 0 is a no-op.
+ */
+kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk, const void* k, const void* v,
+                                   kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
+                                   float eps, int32_t* dev_err, kvq_stream_t stream);
+
+/*
+ * Bytes of device workspace needed by kvq_decode_attn_int4 / kvq_decode_attn_fp8_swa for
+ * B sequences, S query rows each, num_q_heads query heads over num_kv_heads KV heads.
+ * Returns 0 for arguments no call would accept.
+ */
+size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_heads);
+
+/*
+ * kvq_decode_attn_int4 -- split-K flash-decoding attention over the int4 cache (section
+ * "What we do": decode reads the 4-bit codes directly, nothing is rotated back).
+ *   Sequence b (0..B-1) uses block-table row b and has ctx_len[b] cached positions.
+ *   Query row r (0..S-1) sits at position ctx_len[b] + r and attends causally to
+ *   positions 0..ctx_len[b]+r (a speculative-decoding verify block when S > 1).
+ *   q:        device [B][S][num_q_heads][128] of `dtype`, pre-norm queries; the call applies
+ *             q~ = M_q n(q) with the prologue arithmetic above. Query head hq reads KV head
+ *             hq / (num_q_heads/num_kv_heads).
+ *   k_new, v_new: device [B][S][num_kv_heads][128] of `dtype`, or both NULL. When given, the
+ *             S rows are rotated, quantised and appended at positions ctx_len[b]+r first.
+ *   Mq, Mk:   device float[128*128] (Mk only read when k_new is given).
+ *   sm_scale: softmax scale applied to q~.k (1/sqrt(128) for the model).
+ *   out:      device float [B][S][num_q_heads][128], the normalised attention output.
+ *   workspace: device, >= kvq_decode_workspace_bytes(B, S, num_q_heads, num_kv_heads),
+ *             256-byte aligned; contents need no initialisation.
+ *   q_rot_out: optional device float [B][S][num_q_heads][128] copy of q~ (NULL to skip).
+ * Requires 1 <= B <= KVQ_MAX_SEQS, 1 <= S <= 8, S*(num_q_heads/num_kv_heads) <= 48.
+ */
+kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
+                                kvq_stream_t stream);
+
+/*
+ * kvq_fp8_append -- stock FP8 cache write of the sliding-window layers: code =
+ * e4m3(x / scale) with an IEEE fp32 division, round-to-nearest-even, saturating to +-448,
+ * into slot positions[t] % capacity of sequence seq_ids[t]. Rows with a non-finite entry
+ * are skipped (KVQ_DEVERR_NONFINITE).
+ *   k, v: device [T][num_kv_heads][128] of `dtype`; seq_ids, positions: device int32[T].
+ */
+kvq_status kvq_fp8_append(const kvq_fp8_ring* ring, const void* k, const void* v, kvq_dtype dtype, int T,
+                          const int32_t* seq_ids, const int32_t* positions, float k_scale, float v_scale,
+                          int32_t* dev_err, kvq_stream_t stream);
+
+/*
+ * kvq_decode_attn_fp8_swa -- sliding-window attention over the FP8 ring (the stock path of
+ * the 40 window-513 layers). Row r of sequence b sits at position pos0[b] + r and attends
+ * to positions max(0, pos0[b]+r-window+1) .. pos0[b]+r, dequantised as e4m3(c)*k_scale and
+ * e4m3(c)*v_scale. q is used as given (no prologue).
+ *   q: device [B][S][num_q_heads][128] of `dtype`; out: device float [B][S][num_q_heads][128].
+ *   k_new, v_new: device [B][S][num_kv_heads][128] of `dtype` or both NULL; when given they
+ *     are written (kvq_fp8_append arithmetic) at positions pos0[b]+r before attending.
+ *   workspace: as for kvq_decode_attn_int4.
+ * Requires 1 <= B <= KVQ_MAX_SEQS, 1 <= S <= 8, window >= 1, capacity >= window + S - 1.
+ */
+kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_dtype dtype, int B, int S,
+                                   int num_q_heads, const int32_t* pos0, int window, const void* k_new,
+                                   const void* v_new, float k_scale, float v_scale, float sm_scale, float* out,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                   kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,772 @@
+// Split-K flash-decoding attention over the rotated int4 cache and the FP8 ring.
+//
+// "Serving Kolibri-1 with a 4-bit KV cache", section "What we do": decode reads the 4-bit
+// codes directly and nothing is rotated back. The sliding-window layers read their stock
+// FP8 cache through the same kernel (FMT = 1).
+//
+// Work split (stream-K over pages): every (sequence b, KV head h) is a segment of np_b
+// pages; the segments are laid end to end and each CTA takes an equal contiguous range of
+// pages, so ragged contexts balance to within one page. A CTA emits one partial
+// (m, l, acc[128] per query row) for every segment it touches, into slot cta + segment;
+// combine_kernel merges a segment's partials with log-sum-exp weights.
+//
+// Inside a CTA: one producer warp streams page-head blocks (K codes, V codes, K/V meta)
+// into a ring of shared-memory stages with bulk asynchronous copies (TMA engine) signalled
+// on mbarriers; consumer warps are arranged as token groups x tile groups. A tile is 8
+// query rows (rows = S x G query heads of the KV head, row n = r*G + g). Per page a warp:
+//   QK^T on tensor cores: A = 16 tokens x 16 dims of centred codes (c - 8) in f16,
+//        B = 16 dims x 8 query rows of q~ in f16, fp32 accumulate (mma.m16n8k16);
+//   score = log2(e)*sm_scale*(s_K*dot + (o_K + 8 s_K)*sum(q~)) -- scale and offset per token;
+//   online softmax with warp-shuffle max, exp2;
+//   PV on tensor cores: A = 16 dims x 16 tokens of centred V codes (ldmatrix.trans),
+//        B = 16 tokens x 8 rows of p*s_V in f16 (movmatrix transposes the QK accumulator),
+//        plus sum_j p_j (o_V + 8 s_V) added per row.
+
+#include <algorithm>
+#include <cmath>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kStage4 = 2 * kPage * kRec4 + 2 * kPage * 4;  // 8704 bytes: K codes, V codes, K meta, V meta
+constexpr int kStage8 = 2 * kPage * kRec8;                  // 16384 bytes: K and V e4m3
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+  // int4 cache (fp8: kc/vc are the ring's K and V)
+  const uint8_t* kc;
+  const uint8_t* vc;
+  const uint32_t* km;
+  const uint32_t* vm;
+  const int32_t* block_table;
+  int max_pages;
+  int num_pages;
+  // fp8 ring
+  int cap;
+  int window;
+  float v_scale;
+  // shape
+  int B, S, Hq, Hkv, G, R;
+  const int32_t* ctx;
+  const float* q_rot;
+  const void* q;
+  int q_bf16;
+  float score_scale;
+  float* partials;
+  float* out;
+  int32_t* dev_err;
+  int ntg, nkg, nstages, rows_pad;
+  int n_cta;
+};
+
+__host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory layout, identical on host (sizing) and device.
+struct SmemLayout {
+  size_t stages, full, empty, valid, pre, flags, red, total;
+  __host__ __device__ SmemLayout(int fmt, int nstages, int B, int nkg, int rows_pad) {
+    const size_t stage = fmt == 0 ? kStage4 : kStage8;
+    stages = 0;
+    full = align_up(stages + nstages * stage, 16);
+    empty = full + 8 * nstages;
+    valid = empty + 8 * nstages;
+    pre = valid + 4 * nstages;
+    flags = pre + 4 * (B + 1);
+    red = align_up(flags + 16, 16);
+    total = red + (size_t)nkg * rows_pad * kPartialStride * 4;
+  }
+};
+
+// Context length of sequence b as used by every kernel of one call (clamped into the
+// cache; `bad` reports a clamp).
+__device__ __forceinline__ int eff_ctx(const AttnParams& p, int b, bool& bad, int fmt) {
+  int c = p.ctx[b];
+  if (fmt == 0) {
+    const int cap = p.max_pages * kPage - p.S;
+    if (c < 0 || c > cap) {
+      bad = true;
+      c = min(max(c, 0), cap);
+    }
+  } else if (c < 0) {
+    bad = true;
+    c = 0;
+  }
+  return c;
+}
+
+__device__ __forceinline__ int seg_pages(const AttnParams& p, int ctxb, int fmt) {
+  return fmt == 0 ? (ctxb + p.S + kPage - 1) / kPage : p.cap / kPage;
+}
+
+// Warp 0 builds pre[b] = sum_{b' < b} np_b' (pre[B] = total pages per KV head) and
+// flags[1] = any clamped context. Other warps return at once.
+__device__ void build_prefix(const AttnParams& p, int fmt, int* pre, volatile int* flags) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int carry = 0;
+  bool bad = false;
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    int np = 0;
+    if (b < p.B) np = seg_pages(p, eff_ctx(p, b, bad, fmt), fmt);
+    int incl = np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (b < p.B) pre[b] = carry + incl - np;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const bool any_bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    pre[p.B] = carry;
+    flags[0] = 0;
+    flags[1] = any_bad ? 1 : 0;
+  }
+}
+
+// Flattened page -> (sequence, head, local page, pages of the sequence).
+__device__ __forceinline__ void decode_page(const int* pre, int B, int Hkv, long long pg, int& b, int& h, int& lp,
+                                            int& np) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)Hkv * pre[mid] <= pg)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  b = lo;
+  np = pre[b + 1] - pre[b];
+  const long long rem = pg - (long long)Hkv * pre[b];
+  h = (int)(rem / np);
+  lp = (int)(rem - (long long)h * np);
+}
+
+// CTA whose page range [floor(i P / n), floor((i+1) P / n)) contains page pg (n <= P).
+__device__ __forceinline__ long long cta_of(long long pg, long long P, int n) { return ((pg + 1) * n - 1) / P; }
+
+__device__ __forceinline__ float warp_sum_g(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_g(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+  return v;
+}
+
+__device__ __forceinline__ float h2f_lo(uint32_t x) {
+  return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu)));
+}
+__device__ __forceinline__ float h2f_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+
+// Output dim of accumulator row `row` (0..15) of PV m-tile `mt` (0..7).
+template <int FMT>
+__device__ __forceinline__ int out_dim(int mt, int row) {
+  if (FMT == 0) return 32 * (mt >> 1) + 4 * (row & 7) + 2 * (mt & 1) + (row >> 3);
+  return 16 * mt + 2 * (row & 7) + (row >> 3);
+}
+
+template <int FMT, int NT>
+__global__ void __launch_bounds__(256) attn_kernel(const AttnParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kStage = FMT == 0 ? kStage4 : kStage8;
+  constexpr int MTU = NT == 1 ? 4 : 2;  // 16-token m-tiles per online-softmax update
+  const SmemLayout L(FMT, p.nstages, p.B, p.nkg, p.rows_pad);
+  uint8_t* stages = smem + L.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  volatile int* valid = reinterpret_cast<volatile int*>(smem + L.valid);
+  int* pre = reinterpret_cast<int*>(smem + L.pre);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwc = p.ntg * p.nkg;
+  const int nst = p.nstages;
+
+  build_prefix(p, FMT, pre, flags);
+  if (threadIdx.x < nst) {
+    mbar_init(&full[threadIdx.x], 1);
+    mbar_init(&empty[threadIdx.x], p.ntg);
+  }
+  fence_barrier_init();
+  __syncthreads();
+
+  if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
+  const long long P = (long long)p.Hkv * pre[p.B];
+  const int n_eff = (int)min((long long)p.n_cta, P);
+  if ((int)blockIdx.x >= n_eff) return;
+  const long long p0 = (long long)blockIdx.x * P / n_eff;
+  const long long p1 = (long long)(blockIdx.x + 1) * P / n_eff;
+
+  // ------------------------------------------------------------ producer warp
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      long long issued = 0;
+      for (long long pg = p0; pg < p1; ++pg) {
+        const long long k = pg - p0;
+        const int s = (int)(k % nst);
+        const int f = (int)(k / nst);
+        if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
+          set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+          flags[0] = 1;
+          break;
+        }
+        if (flags[0]) break;
+        int b, h, lp, np;
+        decode_page(pre, p.B, p.Hkv, pg, b, h, lp, np);
+        uint8_t* st = stages + (size_t)s * kStage;
+        if (FMT == 0) {
+          const int phys = p.block_table[(size_t)b * p.max_pages + lp];
+          if (phys < 0 || phys >= p.num_pages) {
+            set_err(p.dev_err, KVQ_DEVERR_PAGE);
+            valid[s] = 0;
+            mbar_arrive(&full[s]);
+            issued = k + 1;
+            continue;
+          }
+          valid[s] = 1;
+          const size_t ph = (size_t)phys * p.Hkv + h;
+          mbar_arrive_expect_tx(&full[s], kStage4);
+          bulk_g2s(st, p.kc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
+          bulk_g2s(st + kPage * kRec4, p.vc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
+          bulk_g2s(st + 2 * kPage * kRec4, p.km + ph * kPage, kPage * 4, &full[s], pol);
+          bulk_g2s(st + 2 * kPage * kRec4 + kPage * 4, p.vm + ph * kPage, kPage * 4, &full[s], pol);
+        } else {
+          const size_t base = (((size_t)b * p.Hkv + h) * p.cap + (size_t)lp * kPage) * kRec8;
+          valid[s] = 1;
+          mbar_arrive_expect_tx(&full[s], kStage8);
+          bulk_g2s(st, p.kc + base, kPage * kRec8, &full[s], pol);
+          bulk_g2s(st + kPage * kRec8, p.vc + base, kPage * kRec8, &full[s], pol);
+        }
+        issued = k + 1;
+      }
+      // Do not retire while copies into this CTA's shared memory may be in flight.
+      for (int s = 0; s < nst; ++s) {
+        if (issued <= s) break;
+        const long long last = s + ((issued - 1 - s) / nst) * nst;
+        const int f = (int)(last / nst);
+        if (!mbar_wait_bounded(&full[s], f & 1)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumer warps
+  const int kg = warp / p.ntg, tg = warp - (warp / p.ntg) * p.ntg;
+  const int g = lane >> 2, t = lane & 3;
+  const int R = p.R, G = p.G;
+
+  long long seg_start = p0;
+  while (seg_start < p1) {
+    int b, h, lp0, np;
+    decode_page(pre, p.B, p.Hkv, seg_start, b, h, lp0, np);
+    const long long seg_end = min(p1, seg_start + (np - lp0));
+    const int seg = b * p.Hkv + h;
+    bool dummy = false;
+    const int ctxb = eff_ctx(p, b, dummy, FMT);
+
+    // ---- segment setup: query fragments and per-row limits
+    uint32_t qf[NT][8][2];
+    float qs[NT][2];
+    int lim_lo[NT][2], lim_hi[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tile = tg * NT + nt;
+      const int nB = 8 * tile + g;
+      float qv[32];
+      if (nB < R) {
+        const size_t row = ((size_t)b * p.S + nB / G) * p.Hq + h * G + nB % G;
+        if (FMT == 0 || !p.q_bf16) {
+          const float* qbase = FMT == 0 ? p.q_rot : static_cast<const float*>(p.q);
+          const float4* src = reinterpret_cast<const float4*>(qbase + row * kD + 32 * t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = src[i];
+            qv[4 * i] = v.x;
+            qv[4 * i + 1] = v.y;
+            qv[4 * i + 2] = v.z;
+            qv[4 * i + 3] = v.w;
+          }
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + row * kD + 32 * t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = src[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              qv[8 * i + 2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
+              qv[8 * i + 2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+      }
+      float part = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) part += qv[i];
+      if (FMT == 0) {
+        // k-step 2wi+e, slots (2t,2t+1) <- dims (8wi+2e, +4), slots (2t+8,2t+9) <- (+1, +5)
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d0 = 8 * wi + 2 * e;
+            qf[nt][2 * wi + e][0] = pack_f16x2(qv[d0], qv[d0 + 4]);
+            qf[nt][2 * wi + e][1] = pack_f16x2(qv[d0 + 1], qv[d0 + 5]);
+          }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          qf[nt][ks][0] = pack_f16x2(qv[4 * ks], qv[4 * ks + 1]);
+          qf[nt][ks][1] = pack_f16x2(qv[4 * ks + 2], qv[4 * ks + 3]);
+        }
+      }
+      // full row sum (int4 offset term), then the sums of the rows of my accumulator columns
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float tot = __shfl_sync(0xffffffffu, part, (2 * t + j) * 4);
+        qs[nt][j] = tot * p.score_scale;
+        const int nC = 8 * tile + 2 * t + j;
+        const int r = nC < R ? nC / G : 0;
+        const int hi = ctxb + r;  // last visible position
+        lim_hi[nt][j] = hi;
+        lim_lo[nt][j] = FMT == 0 ? 0 : max(0, hi - p.window + 1);
+      }
+    }
+
+    float m[NT][2], l[NT][2], ov[NT][2], acc[NT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        m[nt][j] = -INFINITY;
+        l[nt][j] = 0.0f;
+        ov[nt][j] = 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[nt][i][c] = 0.0f;
+    }
+
+    // fp8 ring: the newest position written and its slot
+    const int p_last = ctxb + p.S - 1;
+    const int slot_last = FMT == 1 ? p_last % p.cap : 0;
+
+    const long long off = (seg_start - p0) % p.nkg;
+    for (long long pg = seg_start + ((kg - off + p.nkg) % p.nkg); pg < seg_end; pg += p.nkg) {
+      const long long k = pg - p0;
+      const int s = (int)(k % nst);
+      const int f = (int)(k / nst);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], f & 1));
+      if (!ok) {
+        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+        flags[0] = 1;
+      }
+      if (__any_sync(0xffffffffu, flags[0] != 0)) break;
+      const int lp = lp0 + (int)(pg - seg_start);
+      if (valid[s]) {
+        const uint8_t* st = stages + (size_t)s * kStage;
+        const bool need_mask = FMT == 1 || (lp + 1) * kPage > ctxb + 1;
+
+#pragma unroll
+        for (int mt0 = 0; mt0 < 4; mt0 += MTU) {
+          // ---- per-token scale/offset (int4) for the tokens of this thread's accumulator rows
+          float ka[MTU][2], kb[MTU][2], va[MTU][2], vb[MTU][2];
+          if (FMT == 0) {
+            const uint32_t* Km = reinterpret_cast<const uint32_t*>(st + 2 * kPage * kRec4);
+            const uint32_t* Vm = Km + kPage;
+#pragma unroll
+            for (int u = 0; u < MTU; ++u)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int tok = 16 * (mt0 + u) + g + 8 * hh;
+                const uint32_t mk = Km[tok], mv = Vm[tok];
+                const float sk = h2f_lo(mk), ok_ = h2f_hi(mk), sv = h2f_lo(mv), ovv = h2f_hi(mv);
+                ka[u][hh] = sk * p.score_scale;
+                kb[u][hh] = fmaf(8.0f, sk, ok_);
+                va[u][hh] = sv;
+                vb[u][hh] = fmaf(8.0f, sv, ovv);
+              }
+          }
+
+          // ---- scores
+          float sc[NT][MTU][4];
+#pragma unroll
+          for (int u = 0; u < MTU; ++u) {
+            const int mt = mt0 + u;
+            float d[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
+            if (FMT == 0) {
+              const uint8_t* Ks = st;
+              const uint4 wa = *reinterpret_cast<const uint4*>(Ks + (16 * mt + g) * kRec4 + 16 * t);
+              const uint4 wb = *reinterpret_cast<const uint4*>(Ks + (16 * mt + g + 8) * kRec4 + 16 * t);
+              const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+              const uint32_t Bw[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+              for (int wi = 0; wi < 4; ++wi) {
+                uint32_t ha[4], hb[4];
+                unpack8_centred(A[wi], ha);
+                unpack8_centred(Bw[wi], hb);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  mma_16816(d[nt], ha[0], hb[0], ha[1], hb[1], qf[nt][2 * wi][0], qf[nt][2 * wi][1]);
+                  mma_16816(d[nt], ha[2], hb[2], ha[3], hb[3], qf[nt][2 * wi + 1][0], qf[nt][2 * wi + 1][1]);
+                }
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  sc[nt][u][c] = fmaf(d[nt][c], ka[u][c >> 1], kb[u][c >> 1] * qs[nt][c & 1]);
+            } else {
+              const uint8_t* Ks = st;
+              const int ta = 16 * mt + g, tb = ta + 8;  // slot & 7 == g for both tokens
+              const uint4 a0 = *reinterpret_cast<const uint4*>(Ks + ta * kRec8 + 16 * ((2 * t) ^ g));
+              const uint4 a1 = *reinterpret_cast<const uint4*>(Ks + ta * kRec8 + 16 * ((2 * t + 1) ^ g));
+              const uint4 b0 = *reinterpret_cast<const uint4*>(Ks + tb * kRec8 + 16 * ((2 * t) ^ g));
+              const uint4 b1 = *reinterpret_cast<const uint4*>(Ks + tb * kRec8 + 16 * ((2 * t + 1) ^ g));
+              const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const uint32_t Bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t x0 = e4m3x2_to_f16x2(A[ks] & 0xFFFFu), x2 = e4m3x2_to_f16x2(A[ks] >> 16);
+                const uint32_t x1 = e4m3x2_to_f16x2(Bw[ks] & 0xFFFFu), x3 = e4m3x2_to_f16x2(Bw[ks] >> 16);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt], x0, x1, x2, x3, qf[nt][ks][0], qf[nt][ks][1]);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[nt][u][c] = d[nt][c] * p.score_scale;
+            }
+            if (need_mask) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int tok = 16 * mt + g + 8 * hh;
+                int pos;
+                if (FMT == 0) {
+                  pos = lp * kPage + tok;
+                } else {
+                  const int slot = lp * kPage + tok;
+                  int back = slot_last - slot;
+                  if (back < 0) back += p.cap;
+                  pos = p_last - back;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                  for (int j = 0; j < 2; ++j)
+                    if (pos < lim_lo[nt][j] || pos > lim_hi[nt][j]) sc[nt][u][2 * hh + j] = -INFINITY;
+              }
+            }
+          }
+
+          // ---- online softmax update
+          float muse[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              float mx = -INFINITY;
+#pragma unroll
+              for (int u = 0; u < MTU; ++u) mx = fmaxf(mx, fmaxf(sc[nt][u][j], sc[nt][u][2 + j]));
+              mx = warp_max_g(mx);
+              const float mnew = fmaxf(m[nt][j], mx);
+              muse[nt][j] = mnew == -INFINITY ? 0.0f : mnew;
+              const float alpha = fast_exp2(m[nt][j] - muse[nt][j]);
+              m[nt][j] = mnew;
+              if (alpha != 1.0f) {
+                l[nt][j] *= alpha;
+                ov[nt][j] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  acc[nt][i][j] *= alpha;
+                  acc[nt][i][2 + j] *= alpha;
+                }
+              }
+            }
+
+          // ---- P and PV
+#pragma unroll
+          for (int u = 0; u < MTU; ++u) {
+            const int mt = mt0 + u;
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              float pr[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[nt][u][c] - muse[nt][c & 1]);
+              l[nt][0] += pr[0] + pr[2];
+              l[nt][1] += pr[1] + pr[3];
+              if (FMT == 0) {
+                ov[nt][0] = fmaf(pr[0], vb[u][0], fmaf(pr[2], vb[u][1], ov[nt][0]));
+                ov[nt][1] = fmaf(pr[1], vb[u][0], fmaf(pr[3], vb[u][1], ov[nt][1]));
+                pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0] * va[u][0], pr[1] * va[u][0]));
+                pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2] * va[u][1], pr[3] * va[u][1]));
+              } else {
+                pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
+                pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
+              }
+            }
+            const uint8_t* Vs = st + kPage * (FMT == 0 ? kRec4 : kRec8);
+            const int qi = lane >> 3, r8 = lane & 7;
+            if (FMT == 0) {
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int cprime = 2 * cc + (qi >> 1), th = qi & 1;
+                const int tok = 16 * mt + 8 * th + r8;
+                uint32_t rr[4];
+                ldsm_x4_trans(rr, smem_addr(Vs + tok * kRec4 + 16 * (cprime ^ (r8 >> 1))));
+#pragma unroll
+                for (int ci = 0; ci < 2; ++ci) {
+                  uint32_t h0[4], h1[4];
+                  unpack8_centred(rr[2 * ci], h0);
+                  unpack8_centred(rr[2 * ci + 1], h1);
+#pragma unroll
+                  for (int e1 = 0; e1 < 2; ++e1) {
+                    const int mtd = 2 * (2 * cc + ci) + e1;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                      mma_16816(acc[nt][mtd], h0[2 * e1], h0[2 * e1 + 1], h1[2 * e1], h1[2 * e1 + 1], pb[nt][0],
+                                pb[nt][1]);
+                  }
+                }
+              }
+            } else {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const int cprime = 2 * cc + (qi >> 1), th = qi & 1;
+                const int tok = 16 * mt + 8 * th + r8;
+                uint32_t rr[4];
+                ldsm_x4_trans(rr, smem_addr(Vs + tok * kRec8 + 16 * (cprime ^ r8)));
+#pragma unroll
+                for (int ci = 0; ci < 2; ++ci) {
+                  const uint32_t y0 = prmt(rr[2 * ci], 0u, 0x3120u);
+                  const uint32_t y1 = prmt(rr[2 * ci + 1], 0u, 0x3120u);
+                  const uint32_t a0 = e4m3x2_to_f16x2(y0 & 0xFFFFu), a1 = e4m3x2_to_f16x2(y0 >> 16);
+                  const uint32_t a2 = e4m3x2_to_f16x2(y1 & 0xFFFFu), a3 = e4m3x2_to_f16x2(y1 >> 16);
+                  const int mtd = 2 * cc + ci;
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt][mtd], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                }
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- segment end: reduce this warp's partial, merge token groups, write the CTA partial
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tile = tg * NT + nt;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float lt = warp_sum_g(l[nt][j]);
+        const float ot = warp_sum_g(ov[nt][j]);
+        const int row = 8 * tile + 2 * t + j;
+        float* dst = red + ((size_t)kg * p.rows_pad + row) * kPartialStride;
+        if (g == 0) {
+          dst[0] = m[nt][j];
+          dst[1] = lt;
+        }
+        const float vs = FMT == 0 ? 1.0f : p.v_scale;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int dlo = out_dim<FMT>(i, g), dhi = out_dim<FMT>(i, g + 8);
+          dst[2 + dlo] = (acc[nt][i][j] + ot) * vs;
+          dst[2 + dhi] = (acc[nt][i][2 + j] + ot) * vs;
+        }
+      }
+    }
+    named_barrier(1, nwc * 32);
+    {
+      float* dstp = p.partials + ((size_t)(blockIdx.x + seg) * R) * kPartialStride;
+      for (int e = threadIdx.x; e < R * kPartialStride; e += nwc * 32) {
+        const int row = e / kPartialStride, c = e - row * kPartialStride;
+        float M = -INFINITY;
+        for (int kk = 0; kk < p.nkg; ++kk) M = fmaxf(M, red[((size_t)kk * p.rows_pad + row) * kPartialStride]);
+        float v;
+        if (c == 0) {
+          v = M;
+        } else {
+          const float Mu = M == -INFINITY ? 0.0f : M;
+          v = 0.0f;
+          for (int kk = 0; kk < p.nkg; ++kk) {
+            const float* src = red + ((size_t)kk * p.rows_pad + row) * kPartialStride;
+            v += fast_exp2(src[0] - Mu) * src[c];
+          }
+        }
+        dstp[e] = v;
+      }
+    }
+    named_barrier(1, nwc * 32);
+    seg_start = seg_end;
+  }
+}
+
+// One block per (segment, query row): merges the segment's CTA partials and normalises.
+template <int FMT>
+__global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
+  extern __shared__ __align__(16) int cpre[];
+  volatile int* flags = cpre + p.B + 1;
+  build_prefix(p, FMT, cpre, flags);
+  __syncthreads();
+  const int R = p.R;
+  const int seg = blockIdx.x / R, row = blockIdx.x - (blockIdx.x / R) * R;
+  const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+  const long long P = (long long)p.Hkv * cpre[p.B];
+  const int n_eff = (int)min((long long)p.n_cta, P);
+  const int np = cpre[b + 1] - cpre[b];
+  const long long first_pg = (long long)p.Hkv * cpre[b] + (long long)h * np;
+  const int c0 = (int)cta_of(first_pg, P, n_eff), c1 = (int)cta_of(first_pg + np - 1, P, n_eff);
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.partials[((size_t)(c + seg) * R + row) * kPartialStride]);
+  const float Mu = M == -INFINITY ? 0.0f : M;
+  float lsum = 0.0f, a = 0.0f;
+  for (int c = c0; c <= c1; ++c) {
+    const float* src = p.partials + ((size_t)(c + seg) * R + row) * kPartialStride;
+    const float w = fast_exp2(src[0] - Mu);
+    lsum += w * src[1];
+    a += w * src[2 + d];
+  }
+  const int r = row / p.G, gi = row - (row / p.G) * p.G;
+  p.out[(((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + d] = a / lsum;
+}
+
+struct DevCache {
+  int sm = 0;
+  bool attr[2][4] = {{false}};
+};
+DevCache g_dev[64];
+
+template <int FMT, int NT>
+cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_max, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+  if (dc.sm == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    dc.sm = n > 0 ? n : 1;
+  }
+  if (!dc.attr[FMT][NT]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_kernel<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    dc.attr[FMT][NT] = true;
+  }
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<FMT, NT>, threads, smem);
+  if (e != cudaSuccess) return e;
+  occ = std::max(occ, 1);
+  long long grid = std::min<long long>((long long)dc.sm * occ, kMaxCtas);
+  grid = std::max<long long>(1, std::min(grid, p_max));
+  p.n_cta = (int)grid;
+  attn_kernel<FMT, NT><<<(unsigned)grid, threads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t csmem = (p.B + 1 + 4) * sizeof(int);
+  combine_kernel<FMT><<<(unsigned)(p.B * p.Hkv * p.R), 128, csmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t workspace_qrot_bytes(int B, int S, int Hq) { return align_up((size_t)B * S * Hq * kD * 4, 256); }
+
+size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv) {
+  const int G = Hq / Hkv;
+  return align_up(((size_t)kMaxCtas + (size_t)B * Hkv) * S * G * kPartialStride * 4, 256);
+}
+
+cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
+  AttnParams p{};
+  p.B = job.B;
+  p.S = job.S;
+  p.Hq = job.Hq;
+  p.Hkv = job.Hkv;
+  p.G = job.Hq / job.Hkv;
+  p.R = p.S * p.G;
+  p.ctx = job.ctx;
+  p.out = job.out;
+  p.partials = job.partials;
+  p.dev_err = job.dev_err;
+  long long p_max;
+  if (job.fmt == 0) {
+    p.kc = job.cache.k_codes;
+    p.vc = job.cache.v_codes;
+    p.km = job.cache.k_meta;
+    p.vm = job.cache.v_meta;
+    p.block_table = job.cache.block_table;
+    p.max_pages = job.cache.max_pages_per_seq;
+    p.num_pages = job.cache.num_pages;
+    p.q_rot = job.q_rot;
+    p.score_scale = job.sm_scale * kLog2e;
+    p_max = (long long)p.Hkv * p.B * p.max_pages;
+  } else {
+    p.kc = job.ring.k;
+    p.vc = job.ring.v;
+    p.cap = job.ring.capacity;
+    p.window = job.window;
+    p.v_scale = job.v_scale;
+    p.q = job.q;
+    p.q_bf16 = job.q_bf16;
+    p.score_scale = job.sm_scale * kLog2e * job.k_scale;
+    p_max = (long long)p.Hkv * p.B * (p.cap / kPage);
+  }
+  const int ntiles = (p.R + 7) / 8;
+  int NT;
+  if (ntiles <= 3) {
+    NT = ntiles;
+    p.ntg = 1;
+    p.nkg = 4;
+  } else {
+    NT = (ntiles + 1) / 2;
+    p.ntg = 2;
+    p.nkg = 2;
+  }
+  p.nstages = job.fmt == 0 ? 2 * p.nkg : 4;
+  p.rows_pad = p.ntg * NT * 8;
+  const int threads = (p.ntg * p.nkg + 1) * 32;
+  const SmemLayout L(job.fmt, p.nstages, p.B, p.nkg, p.rows_pad);
+  const size_t smem = L.total;
+  if (job.fmt == 0) {
+    switch (NT) {
+      case 1: return launch_attn_t<0, 1>(p, smem, threads, p_max, stream);
+      case 2: return launch_attn_t<0, 2>(p, smem, threads, p_max, stream);
+      default: return launch_attn_t<0, 3>(p, smem, threads, p_max, stream);
+    }
+  }
+  switch (NT) {
+    case 1: return launch_attn_t<1, 1>(p, smem, threads, p_max, stream);
+    case 2: return launch_attn_t<1, 2>(p, smem, threads, p_max, stream);
+    default: return launch_attn_t<1, 3>(p, smem, threads, p_max, stream);
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,207 @@
+// Device helpers for the kvq kernels (sm_103a): inline PTX wrappers for mbarriers,
+// bulk asynchronous copies, warp-level tensor-core MMA, ldmatrix/movmatrix, and the
+// 4-bit / e4m3 -> fp16 register conversions.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kD = 128;          // head dim
+constexpr int kPage = 64;        // tokens per page
+constexpr int kRec4 = 64;        // bytes per int4 token-head record
+constexpr int kRec8 = 128;       // bytes per fp8 token-head record
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after 2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the phase with the given parity has completed. Gives up after
+// kWaitLimitNs (or 2^30 polls) and returns false; the caller records
+// KVQ_DEVERR_TIMEOUT and abandons its work.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
+// ------------------------------------------------------------------ bulk copies
+
+// One-dimensional bulk copy global -> shared through the TMA engine, completion counted
+// on `bar` in bytes. Both addresses 16-byte aligned and bytes a multiple of 16 (page-head
+// blocks of 4096/256/8192 bytes at 16-byte aligned bases, checked by the host).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for streamed KV pages: read once per decode step, so evict first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Named barrier among the first `nthreads` threads (consumer warps only).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------ tensor cores (warp MMA)
+
+// D += A(16x16, f16, row) * B(16x8, f16, col), fp32 accumulate.
+// Fragments (g = lane/4, t = lane%4): a0 (row g, k 2t..2t+1), a1 (row g+8, k 2t..),
+// a2 (row g, k 2t+8..), a3 (row g+8, k 2t+8..); b0 (k 2t..2t+1, n g), b1 (k 2t+8.., n g);
+// d0,d1 (row g, n 2t, 2t+1), d2,d3 (row g+8, n 2t, 2t+1).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices, transposed on load. Lane i gives the row address of row i%8 of
+// matrix i/8; register k of thread (g = lane/4, t = lane%4) receives element [2t][g] in
+// its low half and [2t+1][g] in its high half of matrix k.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// Transpose of an 8x8 b16 matrix held in the standard fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ conversions
+
+template <uint32_t LUT>
+__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, %4;" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(LUT));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Eight 4-bit codes n0..n7 (n_k in bits 4k..4k+3) -> four f16x2 holding the centred
+// values (n-8): h[0] = (n0,n4), h[1] = (n1,n5), h[2] = (n2,n6), h[3] = (n3,n7), low half
+// first. The exponent trick 0x6400|n = 1024+n is exact; the low nibbles then take an exact
+// f16 subtract of 1032, the high nibbles (read in place as 1024+16n) an exact f16 fma by
+// 1/16 and -72. Centring keeps the tensor-core sums free of a large common term.
+__device__ __forceinline__ void unpack8_centred(uint32_t x, uint32_t (&h)[4]) {
+  constexpr uint32_t kMagic = 0x64006400u;      // (1024, 1024)
+  constexpr uint32_t kBias = 0x64086408u;       // (1032, 1032)
+  constexpr uint32_t kSixteenth = 0x2C002C00u;  // (1/16, 1/16)
+  constexpr uint32_t kNeg72 = 0xD480D480u;      // (-72, -72)
+  const uint32_t x8 = x >> 8;
+  h[0] = hsub2_u(lop3<0xEA>(x, 0x000F000Fu, kMagic), kBias);
+  h[1] = hfma2_u(lop3<0xEA>(x, 0x00F000F0u, kMagic), kSixteenth, kNeg72);
+  h[2] = hsub2_u(lop3<0xEA>(x8, 0x000F000Fu, kMagic), kBias);
+  h[3] = hfma2_u(lop3<0xEA>(x8, 0x00F000F0u, kMagic), kSixteenth, kNeg72);
+}
+
+// Two e4m3 bytes (low byte first) -> f16x2 (exact: e4m3 is a subset of f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(two_bytes));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// (lo, hi) fp32 -> f16x2, round to nearest even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// (lo, hi) fp32 -> two e4m3 bytes (lo in the low byte), nearest even, saturating finite.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void set_err(int32_t* dev_err, int bits) {
+  if (dev_err) atomicOr(dev_err, bits);
+}
+
+}  // namespace kvq

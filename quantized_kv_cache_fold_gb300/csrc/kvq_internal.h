@@ -1,0 +1,83 @@
+// Internal launch interface between the C-ABI layer (kvq_api.cpp) and the kernel
+// translation units. Host-side only; all arguments have been validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kMaxCtas = 1024;       // cap on attention CTAs (sizes the partial-result workspace)
+constexpr int kMaxRows = 48;         // S * (num_q_heads / num_kv_heads) rows per KV head and sequence
+constexpr int kPartialStride = 130;  // floats per partial row: m, l, acc[128]
+
+// Job description for the prologue/quantise kernel.
+struct PrepJobs {
+  // int4 append (keys rotated, values raw)
+  kvq_int4_cache cache;
+  const float* Mk;
+  const void* k;
+  const void* v;
+  int kv_bf16;
+  int T;                   // tokens to append (each has num_kv_heads heads)
+  const int32_t* seq_ids;  // explicit mode (or null)
+  const int32_t* positions;
+  const int32_t* ctx_len;  // derived mode: seq = t / S, pos = ctx_len[seq] + t % S
+  int S;
+  // query prologue
+  const float* Mq;
+  const void* q;
+  int q_bf16;
+  int nq_rows;
+  float* q_rot;      // workspace destination [nq_rows][128]
+  float* q_rot_out;  // optional copy
+  float eps;
+  int32_t* dev_err;
+};
+
+cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream);
+
+struct Fp8AppendJob {
+  kvq_fp8_ring ring;
+  const void* k;
+  const void* v;
+  int bf16;
+  int T;
+  const int32_t* seq_ids;  // explicit mode (or null)
+  const int32_t* positions;
+  const int32_t* pos0;     // derived mode: seq = t / S, pos = pos0[seq] + t % S
+  int S;
+  float k_scale, v_scale;
+  int32_t* dev_err;
+};
+
+cudaError_t launch_fp8_append(const Fp8AppendJob& job, cudaStream_t stream);
+
+// Attention over either cache format.
+struct AttnJob {
+  int fmt;  // 0 = int4 paged, 1 = fp8 ring
+  kvq_int4_cache cache;
+  kvq_fp8_ring ring;
+  int window;
+  float k_scale, v_scale;
+  int B, S, Hq, Hkv;
+  const int32_t* ctx;  // int4: ctx_len[b]; fp8: pos0[b]
+  const float* q_rot;  // int4: rotated queries [B][S][Hq][128] fp32 (workspace)
+  const void* q;       // fp8: queries as given
+  int q_bf16;
+  float sm_scale;
+  float* out;
+  float* partials;  // workspace
+  int32_t* dev_err;
+};
+
+cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream);
+
+// Workspace layout shared by the API and the launchers.
+size_t workspace_qrot_bytes(int B, int S, int Hq);
+size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv);
+
+}  // namespace kvq

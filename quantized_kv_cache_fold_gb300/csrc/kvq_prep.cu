@@ -1,0 +1,303 @@
+// Append-time kernels of the rotated 4-bit KV cache and of the FP8 sliding-window cache.
+//
+// prep_kernel: "Serving Kolibri-1 with a 4-bit KV cache", section "What we do". One warp
+// per key/value token-head: RMS norm and the fixed 128x128 matrix M_k = R on the key
+// (the fused Q/K prologue), then 4-bit codes with an fp16 scale and offset for the key
+// and for the unrotated value, written into the page slot. The same kernel applies the
+// query prologue q~ = M_q n(q) (M_q = R diag(g_q g_k)) for the attention that follows.
+// Blocks with blockIdx.x < kv_blocks do key/value work with M_k in shared memory; the
+// rest do query rows with M_q.
+//
+// Every floating-point step uses explicit IEEE round-to-nearest intrinsics in the order
+// fixed by the specification in kvq.h, so the codes are bit-identical to a plain CPU
+// evaluation of the same formula.
+
+#include <algorithm>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kPrepWarps = 8;
+constexpr int kPrepThreads = kPrepWarps * 32;
+constexpr int kMStride = 129;  // padded row stride of the matrix in shared memory (conflict-free)
+constexpr int kPrepSmem = (128 * kMStride + kPrepWarps * 128) * 4;
+
+struct PrepParams {
+  PrepJobs j;
+  int kv_blocks;
+  int kv_jobs;
+  int q_jobs;
+};
+
+__device__ __forceinline__ void load_row(const void* base, int bf16, size_t row, int lane, float (&x)[4]) {
+  if (bf16) {
+    const uint2 u = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row * kD)[lane];
+    x[0] = bf16_bits_to_f32(u.x & 0xFFFFu);
+    x[1] = bf16_bits_to_f32(u.x >> 16);
+    x[2] = bf16_bits_to_f32(u.y & 0xFFFFu);
+    x[3] = bf16_bits_to_f32(u.y >> 16);
+  } else {
+    const float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kD)[lane];
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+  }
+}
+
+__device__ __forceinline__ bool warp_all_finite(const float (&x)[4]) {
+  const bool ok = isfinite(x[0]) && isfinite(x[1]) && isfinite(x[2]) && isfinite(x[3]);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// y = M n(x). Lane l holds x[4l..4l+3] and returns y[l + 32u], u = 0..3.
+// Ms: shared [128][kMStride] (Ms[j*kMStride + i] = M[j][i]); nbuf: shared float[128] of this warp.
+__device__ __forceinline__ void prologue(const float* __restrict__ Ms, float* nbuf, const float (&x)[4], float eps,
+                                         int lane, float (&y)[4]) {
+  float t = __fmul_rn(x[0], x[0]);
+  t = __fmaf_rn(x[1], x[1], t);
+  t = __fmaf_rn(x[2], x[2], t);
+  t = __fmaf_rn(x[3], x[3], t);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, 128.0f), eps)));
+  reinterpret_cast<float4*>(nbuf)[lane] =
+      make_float4(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv), __fmul_rn(x[2], inv), __fmul_rn(x[3], inv));
+  __syncwarp();
+  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+  const float* m0 = Ms + lane * kMStride;
+#pragma unroll 2
+  for (int i = 0; i < kD; i += 4) {
+    const float4 n4 = reinterpret_cast<const float4*>(nbuf)[i >> 2];
+    const float nv[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a0 = __fmaf_rn(m0[i + u], nv[u], a0);
+      a1 = __fmaf_rn(m0[32 * kMStride + i + u], nv[u], a1);
+      a2 = __fmaf_rn(m0[64 * kMStride + i + u], nv[u], a2);
+      a3 = __fmaf_rn(m0[96 * kMStride + i + u], nv[u], a3);
+    }
+  }
+  __syncwarp();
+  y[0] = a0;
+  y[1] = a1;
+  y[2] = a2;
+  y[3] = a3;
+}
+
+struct Quant4 {
+  uint32_t c[4];  // codes of this lane's four elements
+  uint32_t meta;  // fp16 scale | fp16 offset << 16
+  int flags;
+};
+
+// int4 quantiser of one 128-vector spread over the warp (4 elements per lane).
+__device__ __forceinline__ Quant4 quantize(const float (&y)[4]) {
+  float mn = fminf(fminf(y[0], y[1]), fminf(y[2], y[3]));
+  float mx = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  Quant4 r;
+  r.flags = 0;
+  unsigned short ob = __half_as_ushort(__float2half_rd(mn));
+  if ((ob & 0x7FFFu) == 0x7C00u) {  // below -65504: saturate
+    ob = 0xFBFFu;
+    r.flags |= KVQ_DEVERR_RANGE;
+  }
+  if (ob == 0x8000u) ob = 0;  // canonical +0
+  const float o = __half2float(__ushort_as_half(ob));
+  const float span = __fdiv_rn(__fsub_rn(mx, o), 15.0f);
+  unsigned short sb = __half_as_ushort(__float2half_ru(span));
+  if (sb == 0x7C00u) {
+    sb = 0x7BFFu;
+    r.flags |= KVQ_DEVERR_RANGE;
+  }
+  const float s = __half2float(__ushort_as_half(sb));
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    int c = 0;
+    if (s != 0.0f) c = __float2int_rn(__fdiv_rn(__fsub_rn(y[u], o), s));
+    r.c[u] = (uint32_t)min(max(c, 0), 15);
+  }
+  r.meta = (uint32_t)sb | ((uint32_t)ob << 16);
+  return r;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
+  extern __shared__ __align__(16) float smem_f[];
+  float* Ms = smem_f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* nbuf = smem_f + 128 * kMStride + warp * 128;
+  const PrepJobs& j = p.j;
+  const bool kv_role = (int)blockIdx.x < p.kv_blocks;
+  const float* M = kv_role ? j.Mk : j.Mq;
+  for (int e = threadIdx.x; e < kD * kD; e += kPrepThreads) Ms[(e >> 7) * kMStride + (e & 127)] = M[e];
+  __syncthreads();
+
+  const int Hkv = j.cache.num_kv_heads;
+  if (kv_role) {
+    for (int job = blockIdx.x * kPrepWarps + warp; job < p.kv_jobs; job += p.kv_blocks * kPrepWarps) {
+      const int tok = job / Hkv, h = job - (job / Hkv) * Hkv;
+      int seq, pos;
+      if (j.seq_ids) {
+        seq = j.seq_ids[tok];
+        pos = j.positions[tok];
+      } else {
+        seq = tok / j.S;
+        pos = j.ctx_len[seq] + (tok - seq * j.S);
+      }
+      if (seq < 0 || seq >= j.cache.num_seqs || pos < 0 || pos >= j.cache.max_pages_per_seq * kPage) {
+        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_POS);
+        continue;
+      }
+      const int page = j.cache.block_table[(size_t)seq * j.cache.max_pages_per_seq + pos / kPage];
+      if (page < 0 || page >= j.cache.num_pages) {
+        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_PAGE);
+        continue;
+      }
+      const int slot = pos & (kPage - 1);
+      const size_t rec = ((size_t)page * Hkv + h) * kPage + slot;
+      const size_t row = (size_t)tok * Hkv + h;
+
+      float x[4];
+      load_row(j.k, j.kv_bf16, row, lane, x);
+      if (!warp_all_finite(x)) {
+        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+      } else {
+        float y[4];
+        prologue(Ms, nbuf, x, j.eps, lane, y);  // lane holds y[lane + 32u]
+        const Quant4 q = quantize(y);
+        uint8_t* dst = j.cache.k_codes + rec * kRec4;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t hi = __shfl_down_sync(0xffffffffu, q.c[u], 1);
+          if ((lane & 1) == 0) dst[(lane + 32 * u) >> 1] = (uint8_t)(q.c[u] | (hi << 4));
+        }
+        if (lane == 0) {
+          j.cache.k_meta[rec] = q.meta;
+          if (q.flags) set_err(j.dev_err, q.flags);
+        }
+      }
+
+      load_row(j.v, j.kv_bf16, row, lane, x);
+      if (!warp_all_finite(x)) {
+        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+      } else {
+        const Quant4 q = quantize(x);  // lane holds elements 4l..4l+3
+        const uint32_t two = (q.c[0] | (q.c[1] << 4)) | ((q.c[2] | (q.c[3] << 4)) << 8);
+        const int chunk = (lane >> 3) ^ ((slot >> 1) & 3);
+        *reinterpret_cast<uint16_t*>(j.cache.v_codes + rec * kRec4 + chunk * 16 + ((2 * lane) & 15)) =
+            (uint16_t)two;
+        if (lane == 0) {
+          j.cache.v_meta[rec] = q.meta;
+          if (q.flags) set_err(j.dev_err, q.flags);
+        }
+      }
+    }
+  } else {
+    const int qb = blockIdx.x - p.kv_blocks, nqb = gridDim.x - p.kv_blocks;
+    for (int row = qb * kPrepWarps + warp; row < p.q_jobs; row += nqb * kPrepWarps) {
+      float x[4];
+      load_row(j.q, j.q_bf16, (size_t)row, lane, x);
+      if (!warp_all_finite(x) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+      float y[4];
+      prologue(Ms, nbuf, x, j.eps, lane, y);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        j.q_rot[(size_t)row * kD + lane + 32 * u] = y[u];
+        if (j.q_rot_out) j.q_rot_out[(size_t)row * kD + lane + 32 * u] = y[u];
+      }
+    }
+  }
+}
+
+// Stock FP8 cache write: one warp per token-head, lane l converts elements 4l..4l+3.
+__global__ void fp8_append_kernel(const Fp8AppendJob j) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int Hkv = j.ring.num_kv_heads;
+  for (int job = warp; job < j.T * Hkv; job += nwarps) {
+    const int tok = job / Hkv, h = job - (job / Hkv) * Hkv;
+    int seq, pos;
+    if (j.seq_ids) {
+      seq = j.seq_ids[tok];
+      pos = j.positions[tok];
+    } else {
+      seq = tok / j.S;
+      pos = j.pos0[seq] + (tok - seq * j.S);
+    }
+    if (seq < 0 || seq >= j.ring.num_seqs || pos < 0) {
+      if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_POS);
+      continue;
+    }
+    const int slot = pos % j.ring.capacity;
+    const size_t rec = ((size_t)seq * Hkv + h) * j.ring.capacity + slot;
+    const int off = ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
+    for (int which = 0; which < 2; ++which) {
+      float x[4];
+      load_row(which ? j.v : j.k, j.bf16, (size_t)tok * Hkv + h, lane, x);
+      if (!warp_all_finite(x)) {
+        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+        continue;
+      }
+      const float sc = which ? j.v_scale : j.k_scale;
+      const uint32_t lo = pack_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
+      const uint32_t hi = pack_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc));
+      uint8_t* base = which ? j.ring.v : j.ring.k;
+      *reinterpret_cast<uint32_t*>(base + rec * kRec8 + off) = lo | (hi << 16);
+    }
+  }
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
+  PrepParams p;
+  p.j = jobs;
+  p.kv_jobs = jobs.k ? jobs.T * jobs.cache.num_kv_heads : 0;
+  p.q_jobs = jobs.q ? jobs.nq_rows : 0;
+  if (p.kv_jobs == 0 && p.q_jobs == 0) return cudaSuccess;
+  const int cap = 2 * sm_count();
+  p.kv_blocks = std::min((p.kv_jobs + kPrepWarps - 1) / kPrepWarps, cap);
+  const int q_blocks = std::min((p.q_jobs + kPrepWarps - 1) / kPrepWarps, cap);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  prep_kernel<<<p.kv_blocks + q_blocks, kPrepThreads, kPrepSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_append(const Fp8AppendJob& job, cudaStream_t stream) {
+  const int jobs = job.T * job.ring.num_kv_heads;
+  if (jobs == 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = std::min((jobs * 32 + threads - 1) / threads, 4 * sm_count());
+  fp8_append_kernel<<<blocks, threads, 0, stream>>>(job);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq
