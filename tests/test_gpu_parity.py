@@ -1,0 +1,225 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Codes, fp16 scales/offsets and rotated queries must be bit-exact; attention outputs within
+max-abs 2e-3 and relative L2 1e-3 of the oracle's fp64 attention on its own (identical)
+dequantised cache. Inputs come from the synth generator on both sides.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import (assert_close, device_kv, device_new_kv, device_q, oracle_int4_seq, oracle_layer_params,
+                      oracle_swa_seq, unpack_fp8, unpack_int4)
+from quantized_kv_cache_fold_gb300 import DEVERR_NONFINITE, DEVERR_PAGE, KvqError
+from quantized_kv_cache_fold_gb300.runner import DecodeStack
+from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, Workload, config
+
+pytestmark = pytest.mark.gpu
+
+
+def build_int4(w, layer, S, page_perm=True):
+    max_pages = w.max_pages()
+    perm = None
+    if page_perm and w.page_order == "random":
+        perm = lambda l, n: synth.page_permutation(w.seed, layer, n)  # noqa: E731
+    st = DecodeStack(w.B, w.Hq, w.Hkv, S, max_pages, 1, 1, page_perm=perm)
+    gq, gk = synth.gains(w.seed, layer)
+    st.set_int4_params(0, synth.rotation_seed(w.seed, layer), gq, gk)
+
+    def fill(b, p0, T, kb, vb):
+        device_kv(w, layer, b, p0, T, "k", kb[:T])
+        device_kv(w, layer, b, p0, T, "v", vb[:T])
+
+    st.prefill_int4(0, w.ctx, fill, bf16=w.bf16)
+    return st
+
+
+def run_int4_step(st, w, layer, S):
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    q = device_q(w, layer, S, w.ctx)
+    k_new = device_new_kv(w, layer, S, w.ctx, "k")
+    v_new = device_new_kv(w, layer, S, w.ctx, "v")
+    out = torch.empty((w.B, S, w.Hq, 128), dtype=torch.float32, device="cuda")
+    qrot = torch.empty_like(out)
+    st.decode_layer(0, q, ctx, out, k_new=k_new, v_new=v_new, q_rot_out=qrot)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), qrot.cpu().numpy()
+
+
+def check_int4(orc, w, layer, S, seqs, heads=None, st=None):
+    st = st or build_int4(w, layer, S)
+    out, qrot = run_int4_step(st, w, layer, S)
+    assert st.read_error() == 0, f"device error word {st.read_error():#x}"
+    params = oracle_layer_params(orc, w, layer)
+    errs = []
+    for b in seqs:
+        cb = int(w.ctx[b])
+        for h in (heads if heads is not None else range(w.Hkv)):
+            codes, qt, ref = oracle_int4_seq(orc, w, layer, b, h, S, cb, params)
+            got = unpack_int4(st.layers[0].tensors, b, h, cb + S)
+            for key in ("kc", "ks", "ko", "vc", "vs", "vo"):
+                if not np.array_equal(got[key], codes[key]):
+                    bad = np.argwhere(got[key] != codes[key])[:3]
+                    raise AssertionError(f"{key} differs for seq {b} head {h} at {bad.tolist()}")
+            g = w.G
+            assert np.array_equal(qrot[b, :, h * g:(h + 1) * g], qt), f"q~ differs seq {b} head {h}"
+            errs.append(assert_close(out[b, :, h * g:(h + 1) * g], ref, f"seq {b} head {h}"))
+    return st, out, errs
+
+
+def test_generator_device_matches_host():
+    for bf16 in (False, True):
+        mult = synth.key_multiplier(5, 3)
+        k = synth.key(5, synth.S_KEYS)
+        for start, n in ((0, 1000), (123456789, 4099), (2**40 + 7, 777)):
+            host = synth.normals(k, start, n, mult, bf16)
+            dev = torch.empty(n, dtype=torch.int16 if bf16 else torch.float32, device="cuda")
+            synth.normals_device(k, start, n, dev.data_ptr(), mult, bf16, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            assert dev.cpu().numpy().tobytes() == host.tobytes()
+
+
+def test_config1_tiny(orc):
+    w = config(1)
+    check_int4(orc, w, 0, 1, [0])
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 8])
+def test_ragged_page_edges(orc, S):
+    """Contexts around page boundaries (0, 1, 63, 64, 65, 127, 200), fp32 inputs, random pages."""
+    ctx = np.array([0, 1, 63, 64, 65, 127, 200], np.int64)
+    w = Workload("edges", 11, len(ctx), 20, 4, S, ctx, False)
+    check_int4(orc, w, 2, S, range(len(ctx)))
+
+
+def test_gqa_group_sizes(orc):
+    """Other head groupings: G = 8 (S=6 -> 48 rows) and G = 1."""
+    w = Workload("g8", 12, 3, 16, 2, 6, np.array([300, 77, 1000]), True)
+    check_int4(orc, w, 1, 6, range(3))
+    w = Workload("g1", 13, 2, 4, 4, 1, np.array([500, 129]), True)
+    check_int4(orc, w, 1, 1, range(2))
+
+
+def test_config2_all(orc):
+    w = config(2)
+    _, _, errs = check_int4(orc, w, 0, 1, range(w.B))
+    print("config2 worst max-abs %.2e rel-L2 %.2e" % (max(e[0] for e in errs), max(e[1] for e in errs)))
+
+
+def test_verify_rows_match_single_row(orc):
+    """Row r of an S-block equals the single-row decode at context L + r over the same cache."""
+    w = Workload("verify", 14, 4, 20, 4, 4, np.array([1000, 1023, 64, 4000]), True)
+    st, out_blk, _ = check_int4(orc, w, 3, 4, range(4))
+    ctx0 = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    for r in range(4):
+        q = device_q(w, 3, 4, w.ctx)[:, r:r + 1].contiguous()
+        out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device="cuda")
+        st.decode_layer(0, q, ctx0 + r, out)  # cache already holds the block rows
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy()[:, 0], out_blk[:, r], f"row {r}")
+
+
+def test_deterministic(orc):
+    w = Workload("det", 15, 3, 20, 4, 2, np.array([5000, 70, 900]), True)
+    st = build_int4(w, 0, 2)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    q = device_q(w, 0, 2, w.ctx)
+    outs = []
+    for _ in range(2):
+        out = torch.empty((w.B, 2, w.Hq, 128), dtype=torch.float32, device="cuda")
+        st.decode_layer(0, q, ctx, out)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_bad_page_and_nonfinite_flagged():
+    w = Workload("err", 16, 2, 20, 4, 1, np.array([100, 100]), True)
+    st = build_int4(w, 0, 1)
+    L = st.layers[0]
+    # a block-table entry outside the pool: flagged, skipped, no fault
+    saved = int(L.tensors["block_table"][1, 0])
+    L.tensors["block_table"][1, 0] = L.cache.num_pages + 5
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    q = device_q(w, 0, 1, w.ctx)
+    out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device="cuda")
+    st.decode_layer(0, q, ctx, out)
+    torch.cuda.synchronize()
+    assert st.read_error() & DEVERR_PAGE
+    # a NaN in an appended key: flagged, row skipped
+    st.dev_err.zero_()
+    L.tensors["block_table"][1, 0] = saved
+    k_new = device_new_kv(w, 0, 1, w.ctx, "k")
+    k_new[0, 0, 2, 5] = float("nan")
+    v_new = device_new_kv(w, 0, 1, w.ctx, "v")
+    st.decode_layer(0, q, ctx, out, k_new=k_new, v_new=v_new)
+    torch.cuda.synchronize()
+    assert st.read_error() & DEVERR_NONFINITE
+    # the context stays usable
+    st.dev_err.zero_()
+    st.decode_layer(0, q, ctx, out)
+    torch.cuda.synchronize()
+    assert st.read_error() == 0 and np.isfinite(out.cpu().numpy()).all()
+
+
+def test_host_errors_raise():
+    w = Workload("err", 17, 2, 20, 4, 1, np.array([10, 10]), True)
+    st = build_int4(w, 0, 1)
+    q = device_q(w, 0, 1, w.ctx)
+    out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(KvqError):
+        st.decode_layer(0, q[:, :, :19].contiguous(), torch.zeros(2, dtype=torch.int32, device="cuda"), out)
+
+
+# ---------------------------------------------------------------- FP8 sliding window
+
+def build_swa(w, layer, S, cap=576, window=513):
+    st = DecodeStack(w.B, w.Hq, w.Hkv, S, 1, 1, 2, ring_capacity=cap, window=window, swa_k_scale=SWA_K_SCALE,
+                     swa_v_scale=SWA_V_SCALE)
+    L = st.layers[0]
+    from quantized_kv_cache_fold_gb300 import kvq_fp8_append
+    for b in range(w.B):
+        P = int(w.ctx[b])
+        lo = max(0, P - cap)
+        if P - lo <= 0:
+            continue
+        k = device_kv(w, layer, b, lo, P - lo, "swa_k")
+        v = device_kv(w, layer, b, lo, P - lo, "swa_v")
+        seq = torch.full((P - lo,), b, dtype=torch.int32, device="cuda")
+        pos = torch.arange(lo, P, dtype=torch.int32, device="cuda")
+        kvq_fp8_append(L.ring, k, v, seq, pos, SWA_K_SCALE, SWA_V_SCALE, st.dev_err)
+    return st
+
+
+def check_swa(orc, w, layer, S, window=513, cap=576):
+    st = build_swa(w, layer, S, cap, window)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    q = device_q(w, layer, S, w.ctx, swa=True)
+    k_new = device_new_kv(w, layer, S, w.ctx, "swa_k")
+    v_new = device_new_kv(w, layer, S, w.ctx, "swa_v")
+    out = torch.empty((w.B, S, w.Hq, 128), dtype=torch.float32, device="cuda")
+    st.decode_layer(0, q, ctx, out, k_new=k_new, v_new=v_new)
+    torch.cuda.synchronize()
+    assert st.read_error() == 0, f"device error word {st.read_error():#x}"
+    out = out.cpu().numpy()
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            kc, vc, positions, ref = oracle_swa_seq(orc, w, layer, b, h, S, int(w.ctx[b]), window)
+            gk, gv = unpack_fp8(st.layers[0].tensors, b, h, positions)
+            assert np.array_equal(gk, kc) and np.array_equal(gv, vc), f"e4m3 codes differ seq {b} head {h}"
+            assert_close(out[b, :, h * w.G:(h + 1) * w.G], ref, f"swa seq {b} head {h}")
+
+
+@pytest.mark.parametrize("S", [1, 4, 8])
+def test_swa_window_wrap(orc, S):
+    """Early rings (position < window), exact window, and wrap-around of the 576-slot ring."""
+    ctx = np.array([0, 5, 300, 512, 513, 600, 1151, 5000], np.int64)
+    w = Workload("swa", 21, len(ctx), 20, 4, S, ctx, True)
+    check_swa(orc, w, 0, S)
+
+
+def test_swa_small_window(orc):
+    w = Workload("swa16", 22, 3, 20, 4, 2, np.array([10, 100, 1000]), False)
+    check_swa(orc, w, 1, 2, window=16, cap=64)
