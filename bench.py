@@ -1,0 +1,476 @@
+"""Benchmark of the rotated 4-bit KV-cache decode path on GB300.
+
+Workload (default): full decode step at 256k context -- 8 sequences at 262,144 cached
+positions over a 50-layer stack (every fifth layer full attention with the rotated int4
+cache, the other 40 sliding-window layers with window 513 and an FP8 e4m3 cache), 20
+query / 4 KV heads of 128, bf16 inputs, one query row per sequence, timed over K
+consecutive decode steps (each step appends one token per sequence and layer). Inputs
+are seeded synthetic data (synth) already resident in HBM; the int4 cache alone is
+11.4 GB, far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line: session-steps/s (value), the HBM roofline of the int4 attention
+call, the 64k point (32 ragged sequences, one int4 layer), an end-to-end figure with
+host<->device copies, and the CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "int4 decode-attn HBM GB/s & % of peak; session-steps/s at 64k and 256k context"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("KVQ_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device="cpu"):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- the workload on the GPU
+
+class Stack256k:
+    """The 50-layer decode stack with synthetic caches and per-step inputs resident on the device."""
+
+    def __init__(self, steps_total, device):
+        import torch
+
+        import synth
+        from quantized_kv_cache_fold_gb300.runner import DecodeStack
+        from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, config
+
+        w = config(5)
+        self.w = w
+        self.device = device
+        B, S = w.B, 1
+        max_pages = w.max_pages(extra_steps=steps_total)
+        perm = lambda l, n: synth.page_permutation(w.seed, l, n)  # noqa: E731
+        self.st = DecodeStack(B, w.Hq, w.Hkv, S, max_pages, n_layers=w.int4_layers + w.swa_layers, full_every=5,
+                              ring_capacity=w.ring_capacity, window=w.window, swa_k_scale=SWA_K_SCALE,
+                              swa_v_scale=SWA_V_SCALE, page_perm=perm, device=device)
+        st = self.st
+        stream = torch.cuda.current_stream().cuda_stream
+        from quantized_kv_cache_fold_gb300 import kvq_fp8_append
+        for l in st.int4_layers():
+            gq, gk = synth.gains(w.seed, l)
+            st.set_int4_params(l, synth.rotation_seed(w.seed, l), gq, gk)
+
+            def fill(b, p0, T, kb, vb, l=l):
+                synth.kv_rows_device(w.seed, l, b, p0, T, w.Hkv, "k", True, kb.data_ptr(), stream)
+                synth.kv_rows_device(w.seed, l, b, p0, T, w.Hkv, "v", True, vb.data_ptr(), stream)
+
+            st.prefill_int4(l, w.ctx, fill, chunk_tokens=32768)
+        for l in st.swa_layers():
+            L = st.layers[l]
+            cap = w.ring_capacity
+            for b in range(B):
+                P = int(w.ctx[b])
+                k = torch.empty((cap, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+                v = torch.empty_like(k)
+                synth.kv_rows_device(w.seed, l, b, P - cap, cap, w.Hkv, "swa_k", True, k.data_ptr(), stream)
+                synth.kv_rows_device(w.seed, l, b, P - cap, cap, w.Hkv, "swa_v", True, v.data_ptr(), stream)
+                seq = torch.full((cap,), b, dtype=torch.int32, device=device)
+                pos = torch.arange(P - cap, P, dtype=torch.int32, device=device)
+                kvq_fp8_append(L.ring, k, v, seq, pos, SWA_K_SCALE, SWA_V_SCALE, st.dev_err)
+        # per-step inputs: queries and the appended key/value row of every layer
+        nL = len(st.layers)
+        self.q = torch.empty((steps_total, nL, B, S, w.Hq, 128), dtype=torch.bfloat16, device=device)
+        self.kn = torch.empty((steps_total, nL, B, S, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+        self.vn = torch.empty_like(self.kn)
+        for idx, (buf, sid) in enumerate(((self.q, synth.S_QUERIES), (self.kn, synth.S_KEYS),
+                                         (self.vn, synth.S_VALUES))):
+            k = synth.key(w.seed + 1000, sid)
+            synth.normals_device(k, 0, buf.numel(), buf.data_ptr(), None, True, stream)
+        self.ctx = (torch.from_numpy(w.ctx.astype(np.int32)).to(device)[None, :] +
+                    torch.arange(steps_total, dtype=torch.int32, device=device)[:, None]).contiguous()
+        self.out = torch.empty((nL, B, S, w.Hq, 128), dtype=torch.float32, device=device)
+        torch.cuda.synchronize()
+        assert st.read_error() == 0, f"device error during set-up: {st.read_error():#x}"
+        self.int4 = set(st.int4_layers())
+        self.nL = nL
+
+    def step(self, t, ev_pairs=None):
+        st = self.st
+        for l in range(self.nL):
+            if ev_pairs is not None and l in self.int4:
+                ev_pairs[0].record()
+            st.decode_layer(l, self.q[t, l], self.ctx[t], self.out[l], k_new=self.kn[t, l], v_new=self.vn[t, l])
+            if ev_pairs is not None and l in self.int4:
+                ev_pairs[1].record()
+                ev_pairs = None if len(ev_pairs) == 2 else ev_pairs[2:]
+
+    def int4_call_bytes(self, t):
+        """Algorithmic bytes of one int4 layer call at step t: 136 B per token-head over
+        ctx + 1 positions of every sequence (K+V codes 128 B, fp16 scale/offset 8 B)."""
+        ctx = self.w.ctx + t
+        return int((ctx + 1).sum()) * self.w.Hkv * 136
+
+    def launches_per_step(self):
+        return 3 * self.nL  # prologue/append, split-K attention, combine per layer
+
+
+def run_64k(device, steps=30, warmup=3):
+    """The 64k point: 32 sequences, context U[32768, 65536], one int4 layer, random page order."""
+    import torch
+
+    import synth
+    from quantized_kv_cache_fold_gb300.runner import DecodeStack
+    from synth.workloads import config
+
+    w = config(3)
+    perm = lambda l, n: synth.page_permutation(w.seed, l, n)  # noqa: E731
+    st = DecodeStack(w.B, w.Hq, w.Hkv, 1, w.max_pages(), 1, 1, page_perm=perm, device=device)
+    gq, gk = synth.gains(w.seed, 0)
+    st.set_int4_params(0, synth.rotation_seed(w.seed, 0), gq, gk)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def fill(b, p0, T, kb, vb):
+        synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "k", True, kb.data_ptr(), stream)
+        synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "v", True, vb.data_ptr(), stream)
+
+    st.prefill_int4(0, w.ctx, fill, chunk_tokens=32768)
+    q = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.bfloat16, device=device)
+    synth.normals_device(synth.key(w.seed + 1000, synth.S_QUERIES), 0, q.numel(), q.data_ptr(), None, True, stream)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).to(device)
+    out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device=device)
+    for _ in range(warmup):
+        st.decode_layer(0, q, ctx, out)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        e0.record()
+        st.decode_layer(0, q, ctx, out)
+        e1.record()
+    torch.cuda.synchronize()
+    assert st.read_error() == 0
+    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    t = statistics.median(ms) * 1e-3
+    by = int((w.ctx + 1).sum()) * w.Hkv * 136
+    del st
+    torch.cuda.empty_cache()
+    return {"workload": "32 sequences, context U[32768,65536] (mean %d), one int4 layer, random page order" %
+                        int(w.ctx.mean()),
+            "int4_call_us": round(t * 1e6, 1), "hbm_gbs": round(by / t / 1e9, 1),
+            "session_layer_steps_per_s": round(w.B / t, 1), "algorithmic_bytes": by}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(seconds_budget=20.0):
+    """Oracle (CPU, fp64) on a bounded sample of the 256k step: the attention of one KV head (5
+    query rows) of one int4 layer over 262,145 positions, and one window layer of one sequence
+    (4 KV heads), on a cache of seeded random codes. Scaled to session-steps/s."""
+    import oracle
+    import synth
+    from synth.workloads import config
+
+    w = config(5)
+    O = oracle.Oracle()
+    L = int(w.ctx[0]) + 1
+    k = synth.key(99, 1)
+    d = synth.draws(k, 0, L * 128 // 8 * 2 + 4 * L)
+    raw = d.view(np.uint8)
+    kc = (raw[: L * 128] & 15).reshape(L, 128)
+    vc = (raw[L * 128: 2 * L * 128] >> 4).reshape(L, 128)
+    ks = np.full(L, 0x2E66, np.uint16)
+    ko = np.full(L, 0xC1A0, np.uint16)
+    q = synth.normals(synth.key(99, 2), 0, w.G * 128).reshape(w.G, 128)
+    vis = np.full(w.G, L)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        O.attention_int4(q, vis, kc, ks, ko, vc, ks, ko, 128 ** -0.5)
+        reps += 1
+        if time.perf_counter() - t0 > seconds_budget / 2 or reps >= 4:
+            break
+    t_head = (time.perf_counter() - t0) / reps
+    W = w.window
+    k8 = (raw[: W * 128].reshape(W, 128) & 0x77)
+    q8 = synth.normals(synth.key(99, 3), 0, w.Hq * 128).reshape(w.Hq, 128)
+    lo = np.zeros(w.Hq, np.int64)
+    hi = np.full(w.Hq, W - 1, np.int64)
+    t1 = time.perf_counter()
+    O.attention_fp8(q8, lo, hi, k8, k8, 0.01, 0.01, 128 ** -0.5)
+    t_swa = time.perf_counter() - t1
+    per_step = w.int4_layers * w.Hkv * t_head + w.swa_layers * t_swa
+    return {"value": round(1.0 / per_step, 4), "unit": "session-steps/s", "cores": O.threads, "kind": "oracle",
+            "sample": ("fp64 oracle attention of 1 KV head (5 query rows) of 1 int4 layer at 262,145 positions "
+                       f"({reps}x, {t_head:.3f} s each) scaled x{w.int4_layers * w.Hkv} (10 layers x 4 heads), "
+                       f"plus 1 window-513 layer of 1 sequence ({t_swa:.4f} s) scaled x{w.swa_layers}"),
+            "seconds_per_session_step": per_step}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_kvq(args, rank, world, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    K, W = args.steps, args.warmup
+    total = K + W + 2 * min(K, 64)  # timed, warm-up and end-to-end steps each append one position
+    bench = Stack256k(total, device)
+    peak, peak_kind = measured_peak()
+
+    # ---- device-resident timed region
+    for t in range(W):
+        bench.step(t)
+    torch.cuda.synchronize()
+    n_int4 = len(bench.int4)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_int4 * K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    torch.cuda.nvtx.range_push("timed")
+    start.record()
+    for i in range(K):
+        bench.step(W + i, evs[2 * n_int4 * i: 2 * n_int4 * (i + 1)])
+    end.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms_local = start.elapsed_time(end)
+    err = bench.st.read_error()
+    assert err == 0, f"device error word {err:#x}"
+    ms = max_over_ranks(ms_local, world, device)
+    t = ms * 1e-3
+    value = world * bench.w.B * K / t
+    call_ms = [evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(n_int4 * K)]
+    call_bytes = [bench.int4_call_bytes(W + j // n_int4) for j in range(n_int4 * K)]
+    achieved = sum(call_bytes) / (sum(call_ms) * 1e-3) / 1e9
+
+    # ---- end to end: inputs copied from pinned host memory, outputs read back, every step
+    Ke = min(K, 64)
+    nL = bench.nL
+    pool = 4
+    hq = torch.empty((pool,) + tuple(bench.q.shape[1:]), dtype=torch.bfloat16).pin_memory()
+    hk = torch.empty((pool,) + tuple(bench.kn.shape[1:]), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    for i in range(pool):
+        hq[i].copy_(bench.q[i])
+        hk[i].copy_(bench.kn[i])
+        hv[i].copy_(bench.vn[i])
+    hout = torch.empty(tuple(bench.out.shape), dtype=torch.float32).pin_memory()
+    h2d = hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2
+    d2h = hout.numel() * 4
+    base = W + K
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(Ke):
+        t_ = base + i
+        bench.q[t_].copy_(hq[i % pool], non_blocking=True)
+        bench.kn[t_].copy_(hk[i % pool], non_blocking=True)
+        bench.vn[t_].copy_(hv[i % pool], non_blocking=True)
+        bench.step(t_)
+        hout.copy_(bench.out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    te = max_over_ranks(e0.elapsed_time(e1), world, device) * 1e-3
+    e2e_value = world * bench.w.B * Ke / te
+    del bench
+    torch.cuda.empty_cache()
+
+    sec = run_64k(device) if rank == 0 else None
+    cpu = oracle_sample() if rank == 0 else None
+
+    if rank == 0:
+        frac = achieved / peak
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "session-steps/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u4", "data": "synthetic",
+            "config": {"workload": "decode step at 256k: 8 sequences x 262,144 context, 50 layers "
+                                   "(10 rotated int4 + 40 FP8 window 513), 20/4 heads x 128, bf16 inputs, 1 query row",
+                       "global_batch": 8 * world, "seq_len": int(bench_ctx0()), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (11.4 GB of int4 cache read per step)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(frac, 4), "traffic": None, "peak_kind": peak_kind,
+                         "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
+                         "kernel": "kvq_decode_attn_int4 call (query prologue + split-K attention + combine)",
+                         "bytes_per_call": int(np.mean(call_bytes)), "avg_call_us": round(1e3 * np.mean(call_ms), 2)},
+            "at_64k": sec,
+            "e2e": {"value": round(e2e_value, 2), "unit": "session-steps/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "steps": Ke},
+            "cpu_baseline": {k: v for k, v in cpu.items() if k != "seconds_per_session_step"},
+            "gpu_launches": 150 * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def bench_ctx0():
+    from synth.workloads import config
+    return config(5).ctx[0]
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the machine's host cores: each step is a bounded sample of the
+    256k decode step (one KV head of one int4 layer); rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    from synth.workloads import config
+
+    w = config(5)
+    O = oracle.Oracle()
+    L = int(w.ctx[0]) + 1
+    raw = synth.draws(synth.key(99, 1), 0, L * 128 // 4).view(np.uint8)
+    kc = (raw[: L * 128] & 15).reshape(L, 128)
+    vc = (raw[: L * 128] >> 4).reshape(L, 128)
+    ks = np.full(L, 0x2E66, np.uint16)
+    ko = np.full(L, 0xC1A0, np.uint16)
+    q = synth.normals(synth.key(99, 2), 0, w.G * 128).reshape(w.G, 128)
+    vis = np.full(w.G, L)
+    for _ in range(args.warmup):
+        O.attention_int4(q, vis, kc, ks, ko, vc, ks, ko, 128 ** -0.5)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.attention_int4(q, vis, kc, ks, ko, vc, ks, ko, 128 ** -0.5)
+    t = time.perf_counter() - t0
+    per_sample = t / args.steps
+    frac = 1.0 / (w.int4_layers * w.Hkv)      # one KV head of one int4 layer of one sequence
+    value = frac / per_sample
+    sample = (f"each step: fp64 oracle attention of 1 KV head (5 query rows) of 1 int4 layer at {L} positions "
+              f"= 1/{w.int4_layers * w.Hkv} of one sequence's int4 work per decode step (window layers excluded)")
+    line = {"metric": METRIC, "value": round(value, 5), "unit": "session-steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_sample * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "decode step at 256k (oracle sample)", "global_batch": 8, "seq_len": L - 1},
+            "cpu_baseline": {"value": round(value, 5), "unit": "session-steps/s", "cores": O.threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "session-steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--only", default=None, choices=["64k"],
+                    help="run only the 64k single-layer point (a small case for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.only == "64k":
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_64k(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+    elif args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_kvq(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
