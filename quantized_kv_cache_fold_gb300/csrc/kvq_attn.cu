@@ -31,6 +31,19 @@
 namespace kvq {
 namespace {
 
+// Tuning of the attention CTA when one warp covers every query row of a KV head (S*G <= 24):
+// consumer token groups, shared-memory pipeline stages (a multiple of the token groups) and
+// the minimum resident CTAs per SM requested from the register allocator.
+#ifndef KVQ_TOKEN_GROUPS
+#define KVQ_TOKEN_GROUPS 4
+#endif
+#ifndef KVQ_STAGES_INT4
+#define KVQ_STAGES_INT4 8
+#endif
+#ifndef KVQ_MIN_CTAS
+#define KVQ_MIN_CTAS 1
+#endif
+
 constexpr int kStage4 = 2 * kPage * kRec4 + 2 * kPage * 4;  // 8704 bytes: K codes, V codes, K meta, V meta
 constexpr int kStage8 = 2 * kPage * kRec8;                  // 16384 bytes: K and V e4m3
 constexpr float kLog2e = 1.4426950408889634f;
@@ -177,7 +190,8 @@ __device__ __forceinline__ int out_dim(int mt, int row) {
 }
 
 template <int FMT, int NT>
-__global__ void __launch_bounds__(256) attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, NT == 1 ? KVQ_MIN_CTAS : 1)
+    attn_kernel(const AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kStage = FMT == 0 ? kStage4 : kStage8;
   constexpr int MTU = NT == 1 ? 4 : 2;  // 16-token m-tiles per online-softmax update
@@ -409,37 +423,64 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnParams p) {
 
           // ---- scores
           float sc[NT][MTU][4];
+          if (FMT == 0) {
+            // Load every m-tile's K words first, then interleave the m-tiles' MMA chains so
+            // independent accumulators hide the tensor-core latency.
+            const uint8_t* Ks = st;
+            uint32_t A[MTU][4], Bw[MTU][4];
 #pragma unroll
-          for (int u = 0; u < MTU; ++u) {
-            const int mt = mt0 + u;
-            float d[NT][4];
+            for (int u = 0; u < MTU; ++u) {
+              const uint4 wa = *reinterpret_cast<const uint4*>(Ks + (16 * (mt0 + u) + g) * kRec4 + 16 * t);
+              const uint4 wb = *reinterpret_cast<const uint4*>(Ks + (16 * (mt0 + u) + g + 8) * kRec4 + 16 * t);
+              A[u][0] = wa.x;
+              A[u][1] = wa.y;
+              A[u][2] = wa.z;
+              A[u][3] = wa.w;
+              Bw[u][0] = wb.x;
+              Bw[u][1] = wb.y;
+              Bw[u][2] = wb.z;
+              Bw[u][3] = wb.w;
+            }
+            float d[NT][MTU][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
-            if (FMT == 0) {
-              const uint8_t* Ks = st;
-              const uint4 wa = *reinterpret_cast<const uint4*>(Ks + (16 * mt + g) * kRec4 + 16 * t);
-              const uint4 wb = *reinterpret_cast<const uint4*>(Ks + (16 * mt + g + 8) * kRec4 + 16 * t);
-              const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
-              const uint32_t Bw[4] = {wb.x, wb.y, wb.z, wb.w};
+              for (int u = 0; u < MTU; ++u)
 #pragma unroll
-              for (int wi = 0; wi < 4; ++wi) {
-                uint32_t ha[4], hb[4];
-                unpack8_centred(A[wi], ha);
-                unpack8_centred(Bw[wi], hb);
+                for (int c = 0; c < 4; ++c) d[nt][u][c] = 0.0f;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  mma_16816(d[nt], ha[0], hb[0], ha[1], hb[1], qf[nt][2 * wi][0], qf[nt][2 * wi][1]);
-                  mma_16816(d[nt], ha[2], hb[2], ha[3], hb[3], qf[nt][2 * wi + 1][0], qf[nt][2 * wi + 1][1]);
-                }
+            for (int wi = 0; wi < 4; ++wi) {
+              uint32_t ha[MTU][4], hb[MTU][4];
+#pragma unroll
+              for (int u = 0; u < MTU; ++u) {
+                unpack8_centred(A[u][wi], ha[u]);
+                unpack8_centred(Bw[u][wi], hb[u]);
               }
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int u = 0; u < MTU; ++u)
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt)
+                    mma_16816(d[nt][u], ha[u][2 * e], hb[u][2 * e], ha[u][2 * e + 1], hb[u][2 * e + 1],
+                              qf[nt][2 * wi + e][0], qf[nt][2 * wi + e][1]);
+            }
+#pragma unroll
+            for (int u = 0; u < MTU; ++u)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                  sc[nt][u][c] = fmaf(d[nt][c], ka[u][c >> 1], kb[u][c >> 1] * qs[nt][c & 1]);
-            } else {
+                  sc[nt][u][c] = fmaf(d[nt][u][c], ka[u][c >> 1], kb[u][c >> 1] * qs[nt][c & 1]);
+          } else {
+#pragma unroll
+            for (int u = 0; u < MTU; ++u) {
+              const int mt = mt0 + u;
+              float d[NT][4];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
               const uint8_t* Ks = st;
               const int ta = 16 * mt + g, tb = ta + 8;  // slot & 7 == g for both tokens
               const uint4 a0 = *reinterpret_cast<const uint4*>(Ks + ta * kRec8 + 16 * ((2 * t) ^ g));
@@ -460,10 +501,13 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnParams p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) sc[nt][u][c] = d[nt][c] * p.score_scale;
             }
-            if (need_mask) {
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int u = 0; u < MTU; ++u)
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
-                const int tok = 16 * mt + g + 8 * hh;
+                const int tok = 16 * (mt0 + u) + g + 8 * hh;
                 int pos;
                 if (FMT == 0) {
                   pos = lp * kPage + tok;
@@ -479,7 +523,6 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnParams p) {
                   for (int j = 0; j < 2; ++j)
                     if (pos < lim_lo[nt][j] || pos > lim_hi[nt][j]) sc[nt][u][2 * hh + j] = -INFINITY;
               }
-            }
           }
 
           // ---- online softmax update
@@ -741,16 +784,22 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
   }
   const int ntiles = (p.R + 7) / 8;
   int NT;
-  if (ntiles <= 3) {
+  if (ntiles == 1) {
+    NT = 1;
+    p.ntg = 1;
+    p.nkg = KVQ_TOKEN_GROUPS;
+    p.nstages = job.fmt == 0 ? KVQ_STAGES_INT4 : KVQ_TOKEN_GROUPS;
+  } else if (ntiles <= 3) {
     NT = ntiles;
     p.ntg = 1;
     p.nkg = 4;
+    p.nstages = job.fmt == 0 ? 8 : 4;
   } else {
     NT = (ntiles + 1) / 2;
     p.ntg = 2;
     p.nkg = 2;
+    p.nstages = 4;
   }
-  p.nstages = job.fmt == 0 ? 2 * p.nkg : 4;
   p.rows_pad = p.ntg * NT * 8;
   const int threads = (p.ntg * p.nkg + 1) * 32;
   const SmemLayout L(job.fmt, p.nstages, p.B, p.nkg, p.rows_pad);
