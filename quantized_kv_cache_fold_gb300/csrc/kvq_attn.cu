@@ -224,49 +224,72 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, N
   const long long p1 = (long long)(blockIdx.x + 1) * P / n_eff;
 
   // ------------------------------------------------------------ producer warp
+  // The 32 lanes resolve the source blocks of 32 consecutive pages at once (block-table
+  // loads in parallel); lane 0 then issues the bulk copies in order as stages free up.
   if (warp == nwc) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      long long issued = 0;
-      for (long long pg = p0; pg < p1; ++pg) {
-        const long long k = pg - p0;
-        const int s = (int)(k % nst);
-        const int f = (int)(k / nst);
-        if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
-          set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-          flags[0] = 1;
-          break;
-        }
-        if (flags[0]) break;
+    const uint64_t pol = policy_evict_first();
+    long long issued = 0;
+    bool stop = false;
+    for (long long base = p0; base < p1 && !stop; base += 32) {
+      const long long mine = base + lane;
+      long long src = -1;  // page-head block index (int4) or byte offset (fp8); -1 = invalid page
+      if (mine < p1) {
         int b, h, lp, np;
-        decode_page(pre, p.B, p.Hkv, pg, b, h, lp, np);
-        uint8_t* st = stages + (size_t)s * kStage;
+        decode_page(pre, p.B, p.Hkv, mine, b, h, lp, np);
         if (FMT == 0) {
           const int phys = p.block_table[(size_t)b * p.max_pages + lp];
-          if (phys < 0 || phys >= p.num_pages) {
+          if (phys >= 0 && phys < p.num_pages)
+            src = (long long)phys * p.Hkv + h;
+          else
             set_err(p.dev_err, KVQ_DEVERR_PAGE);
-            valid[s] = 0;
-            mbar_arrive(&full[s]);
-            issued = k + 1;
-            continue;
-          }
-          valid[s] = 1;
-          const size_t ph = (size_t)phys * p.Hkv + h;
-          mbar_arrive_expect_tx(&full[s], kStage4);
-          bulk_g2s(st, p.kc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
-          bulk_g2s(st + kPage * kRec4, p.vc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
-          bulk_g2s(st + 2 * kPage * kRec4, p.km + ph * kPage, kPage * 4, &full[s], pol);
-          bulk_g2s(st + 2 * kPage * kRec4 + kPage * 4, p.vm + ph * kPage, kPage * 4, &full[s], pol);
         } else {
-          const size_t base = (((size_t)b * p.Hkv + h) * p.cap + (size_t)lp * kPage) * kRec8;
-          valid[s] = 1;
-          mbar_arrive_expect_tx(&full[s], kStage8);
-          bulk_g2s(st, p.kc + base, kPage * kRec8, &full[s], pol);
-          bulk_g2s(st + kPage * kRec8, p.vc + base, kPage * kRec8, &full[s], pol);
+          src = (((long long)b * p.Hkv + h) * p.cap + (long long)lp * kPage) * kRec8;
         }
-        issued = k + 1;
       }
-      // Do not retire while copies into this CTA's shared memory may be in flight.
+      const int n = (int)min(32LL, p1 - base);
+      for (int j = 0; j < n; ++j) {
+        const long long sj = __shfl_sync(0xffffffffu, src, j);
+        int halt = 0;
+        if (lane == 0) {
+          const long long k = base + j - p0;
+          const int s = (int)(k % nst);
+          const int f = (int)(k / nst);
+          if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
+            set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+            flags[0] = 1;
+          }
+          if (flags[0]) {
+            halt = 1;
+          } else {
+            uint8_t* st = stages + (size_t)s * kStage;
+            if (sj < 0) {
+              valid[s] = 0;
+              mbar_arrive(&full[s]);
+            } else if (FMT == 0) {
+              const size_t ph = (size_t)sj;
+              valid[s] = 1;
+              mbar_arrive_expect_tx(&full[s], kStage4);
+              bulk_g2s(st, p.kc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
+              bulk_g2s(st + kPage * kRec4, p.vc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
+              bulk_g2s(st + 2 * kPage * kRec4, p.km + ph * kPage, kPage * 4, &full[s], pol);
+              bulk_g2s(st + 2 * kPage * kRec4 + kPage * 4, p.vm + ph * kPage, kPage * 4, &full[s], pol);
+            } else {
+              valid[s] = 1;
+              mbar_arrive_expect_tx(&full[s], kStage8);
+              bulk_g2s(st, p.kc + sj, kPage * kRec8, &full[s], pol);
+              bulk_g2s(st + kPage * kRec8, p.vc + sj, kPage * kRec8, &full[s], pol);
+            }
+            issued = k + 1;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, halt, 0)) {
+          stop = true;
+          break;
+        }
+      }
+    }
+    // Do not retire while copies into this CTA's shared memory may be in flight.
+    if (lane == 0) {
       for (int s = 0; s < nst; ++s) {
         if (issued <= s) break;
         const long long last = s + ((issued - 1 - s) / nst) * nst;
