@@ -59,24 +59,25 @@ typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
 
 /*
  * Paged int4 cache of one full-attention layer.
- * Physical layout (all byte offsets from the given base pointers):
- *   k_codes, v_codes: [num_pages][num_kv_heads][64 tokens][64 bytes]
- *     record byte b holds code 2b in its low nibble and code 2b+1 in its high nibble.
- *     k_codes records are stored as is. In v_codes the four 16-byte chunks of the record
- *     of token slot t (0..63 within its page) are stored in XOR order: logical chunk c at
- *     physical chunk c ^ ((t >> 1) & 3), so a transposing shared-memory read of eight
- *     consecutive tokens touches eight distinct bank groups.
- *   k_meta, v_meta:   [num_pages][num_kv_heads][64 tokens] uint32:
- *     bits 0..15 the fp16 scale, bits 16..31 the fp16 offset; value = code*scale + offset.
- *   block_table:      [num_seqs][max_pages_per_seq] int32 (device): physical page of
- *     logical page p of sequence q; position `pos` lives in page pos/64, slot pos%64.
- * All four data pointers must be 16-byte aligned (device).
+ * Physical layout: one contiguous 8704-byte block per (page, KV head), so that one bulk copy
+ * moves a page of one head into shared memory:
+ *   pages: [num_pages][num_kv_heads][8704] bytes (device, 16-byte aligned); within a block
+ *     bytes    0..4095  K codes [64 tokens][64 bytes]
+ *     bytes 4096..8191  V codes [64 tokens][64 bytes]
+ *     bytes 8192..8447  K meta  [64 tokens] uint32
+ *     bytes 8448..8703  V meta  [64 tokens] uint32
+ *   A code record: byte b holds code 2b in its low nibble and code 2b+1 in its high nibble.
+ *   K records are stored as is. In V records the four 16-byte chunks of token slot t (0..63)
+ *   are stored in XOR order: logical chunk c at physical chunk c ^ ((t >> 1) & 3), so a
+ *   transposing shared-memory read of eight consecutive tokens touches eight bank groups.
+ *   A meta word: bits 0..15 the fp16 scale, bits 16..31 the fp16 offset; value = code*scale + offset.
+ *   block_table: [num_seqs][max_pages_per_seq] int32 (device): physical page of logical
+ *     page p of sequence q; position `pos` lives in page pos/64, slot pos%64.
  */
+#define KVQ_INT4_BLOCK_BYTES 8704
+
 typedef struct kvq_int4_cache {
-  uint8_t* k_codes;
-  uint32_t* k_meta;
-  uint8_t* v_codes;
-  uint32_t* v_meta;
+  uint8_t* pages;
   const int32_t* block_table;
   int32_t num_seqs;
   int32_t max_pages_per_seq;
@@ -88,14 +89,15 @@ typedef struct kvq_int4_cache {
 
 /*
  * FP8 e4m3 ring cache of one sliding-window layer (stock format: one fp32 scale per
- * tensor). Position `pos` of sequence q, head h lives in slot pos % capacity:
- *   k, v: [num_seqs][num_kv_heads][capacity][128] bytes (device, 16-byte aligned),
- *   the eight 16-byte chunks of the record in slot t stored at physical chunk c ^ (t & 7).
+ * tensor). Position `pos` of sequence q, head h lives in slot pos % capacity. The ring is
+ * stored in blocks of 64 slots, keys then values, one contiguous 16384-byte block each:
+ *   data: [num_seqs][num_kv_heads][capacity/64][2 (K, V)][64 slots][128] bytes (device,
+ *   16-byte aligned); the eight 16-byte chunks of the record in slot t are stored at
+ *   physical chunk c ^ (t & 7).
  * capacity must be a multiple of 64 and at least window + S - 1 for the calls using it.
  */
 typedef struct kvq_fp8_ring {
-  uint8_t* k;
-  uint8_t* v;
+  uint8_t* data;
   int32_t num_seqs;
   int32_t num_kv_heads;
   int32_t capacity;

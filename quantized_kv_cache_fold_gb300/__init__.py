@@ -29,16 +29,19 @@ class KvqError(RuntimeError):
         self.status = status
 
 
+INT4_BLOCK_BYTES = 8704  # one (page, KV head): K codes 4096, V codes 4096, K meta 256, V meta 256
+FP8_BLOCK_BYTES = 16384  # 64 ring slots of one head: K 8192, V 8192
+
+
 class Int4Cache(ctypes.Structure):
-    _fields_ = [("k_codes", ctypes.c_void_p), ("k_meta", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("v_meta", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
+    _fields_ = [("pages", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
 class Fp8Ring(ctypes.Structure):
-    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
-                ("num_kv_heads", ctypes.c_int32), ("capacity", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+    _fields_ = [("data", ctypes.c_void_p), ("num_seqs", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
 def _load():
@@ -133,35 +136,37 @@ def kvq_fold_qk(R, g_q, g_k):
 
 # ---------------------------------------------------------------- cache descriptors
 
-def int4_cache(k_codes, k_meta, v_codes, v_meta, block_table, num_kv_heads: int) -> Int4Cache:
-    """Descriptor over caller-owned device tensors (see kvq.h for the layout)."""
+def int4_cache(pages, block_table) -> Int4Cache:
+    """Descriptor over caller-owned device tensors: pages uint8 [num_pages, num_kv_heads, 8704]
+    and block_table int32 [num_seqs, max_pages_per_seq] (see kvq.h for the block layout)."""
     num_seqs, max_pages = block_table.shape
-    return Int4Cache(_ptr(k_codes), _ptr(k_meta), _ptr(v_codes), _ptr(v_meta), _ptr(block_table), num_seqs,
-                     max_pages, k_meta.shape[0], num_kv_heads, PAGE_SIZE, HEAD_DIM)
+    num_pages, num_kv_heads, nbytes = pages.shape
+    assert nbytes == INT4_BLOCK_BYTES
+    return Int4Cache(_ptr(pages), _ptr(block_table), num_seqs, max_pages, num_pages, num_kv_heads, PAGE_SIZE,
+                     HEAD_DIM)
 
 
-def fp8_ring(k, v) -> Fp8Ring:
-    num_seqs, num_kv, cap, hd = k.shape
-    return Fp8Ring(_ptr(k), _ptr(v), num_seqs, num_kv, cap, hd)
+def fp8_ring(data) -> Fp8Ring:
+    """data uint8 [num_seqs, num_kv_heads, capacity/64, 16384]."""
+    num_seqs, num_kv, nblk, nbytes = data.shape
+    assert nbytes == FP8_BLOCK_BYTES
+    return Fp8Ring(_ptr(data), num_seqs, num_kv, nblk * PAGE_SIZE, HEAD_DIM)
 
 
 def alloc_int4_cache(num_pages: int, num_kv_heads: int, block_table, device="cuda"):
     """Device tensors for an int4 cache (plumbing only: torch allocates, kernels fill)."""
     import torch
-    k_codes = torch.zeros((num_pages, num_kv_heads, PAGE_SIZE, 64), dtype=torch.uint8, device=device)
-    v_codes = torch.zeros_like(k_codes)
-    k_meta = torch.zeros((num_pages, num_kv_heads, PAGE_SIZE), dtype=torch.int32, device=device)
-    v_meta = torch.zeros_like(k_meta)
+    pages = torch.zeros((num_pages, num_kv_heads, INT4_BLOCK_BYTES), dtype=torch.uint8, device=device)
     bt = block_table.to(device=device, dtype=torch.int32).contiguous()
-    tensors = {"k_codes": k_codes, "k_meta": k_meta, "v_codes": v_codes, "v_meta": v_meta, "block_table": bt}
-    return tensors, int4_cache(k_codes, k_meta, v_codes, v_meta, bt, num_kv_heads)
+    return {"pages": pages, "block_table": bt}, int4_cache(pages, bt)
 
 
 def alloc_fp8_ring(num_seqs: int, num_kv_heads: int, capacity: int, device="cuda"):
     import torch
-    k = torch.zeros((num_seqs, num_kv_heads, capacity, HEAD_DIM), dtype=torch.uint8, device=device)
-    v = torch.zeros_like(k)
-    return {"k": k, "v": v}, fp8_ring(k, v)
+    assert capacity % PAGE_SIZE == 0
+    data = torch.zeros((num_seqs, num_kv_heads, capacity // PAGE_SIZE, FP8_BLOCK_BYTES), dtype=torch.uint8,
+                       device=device)
+    return {"data": data}, fp8_ring(data)
 
 
 # ---------------------------------------------------------------- device calls

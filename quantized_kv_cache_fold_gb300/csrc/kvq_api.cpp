@@ -32,9 +32,7 @@ int popcount32(uint32_t x) {
 kvq_status check_int4_cache(const kvq_int4_cache* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;
   if (c->head_dim != KVQ_HEAD_DIM || c->page_size != KVQ_PAGE_SIZE) return KVQ_ERR_UNSUPPORTED;
-  if (!c->k_codes || !c->k_meta || !c->v_codes || !c->v_meta || !c->block_table) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(c->k_codes, 16) || !aligned(c->k_meta, 16) || !aligned(c->v_codes, 16) || !aligned(c->v_meta, 16))
-    return KVQ_ERR_INVALID_ARG;
+  if (!c->pages || !c->block_table || !aligned(c->pages, 16)) return KVQ_ERR_INVALID_ARG;
   if (c->num_seqs < 1 || c->max_pages_per_seq < 1 || c->num_pages < 1 || c->num_kv_heads < 1)
     return KVQ_ERR_INVALID_ARG;
   if ((long long)c->max_pages_per_seq * KVQ_PAGE_SIZE > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
@@ -44,7 +42,7 @@ kvq_status check_int4_cache(const kvq_int4_cache* c) {
 kvq_status check_ring(const kvq_fp8_ring* r) {
   if (!r) return KVQ_ERR_INVALID_ARG;
   if (r->head_dim != KVQ_HEAD_DIM) return KVQ_ERR_UNSUPPORTED;
-  if (!r->k || !r->v || !aligned(r->k, 16) || !aligned(r->v, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!r->data || !aligned(r->data, 16)) return KVQ_ERR_INVALID_ARG;
   if (r->num_seqs < 1 || r->num_kv_heads < 1 || r->capacity < KVQ_PAGE_SIZE || r->capacity % KVQ_PAGE_SIZE)
     return KVQ_ERR_INVALID_ARG;
   return KVQ_OK;

@@ -49,11 +49,8 @@ constexpr int kStage8 = 2 * kPage * kRec8;                  // 16384 bytes: K an
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
-  // int4 cache (fp8: kc/vc are the ring's K and V)
-  const uint8_t* kc;
-  const uint8_t* vc;
-  const uint32_t* km;
-  const uint32_t* vm;
+  // int4: page-head blocks [num_pages][Hkv][8704]; fp8: ring blocks [B][Hkv][cap/64][16384]
+  const uint8_t* blocks;
   const int32_t* block_table;
   int max_pages;
   int num_pages;
@@ -225,76 +222,61 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, N
 
   // ------------------------------------------------------------ producer warp
   // The 32 lanes resolve the source blocks of 32 consecutive pages at once (block-table
-  // loads in parallel); lane 0 then issues the bulk copies in order as stages free up.
+  // loads in parallel); lane 0 then issues one bulk copy per page, in order, as stages free.
   if (warp == nwc) {
     const uint64_t pol = policy_evict_first();
-    long long issued = 0;
-    bool stop = false;
-    for (long long base = p0; base < p1 && !stop; base += 32) {
-      const long long mine = base + lane;
-      long long src = -1;  // page-head block index (int4) or byte offset (fp8); -1 = invalid page
-      if (mine < p1) {
+    const int npages = (int)(p1 - p0);
+    int issued = 0;
+    int s = 0, f = 0;  // stage and fill round of the next page
+    for (int base = 0; base < npages; base += 32) {
+      const int mine = base + lane;
+      long long src = -1;  // byte offset of the page's block; -1 = invalid page
+      if (mine < npages) {
         int b, h, lp, np;
-        decode_page(pre, p.B, p.Hkv, mine, b, h, lp, np);
+        decode_page(pre, p.B, p.Hkv, p0 + mine, b, h, lp, np);
         if (FMT == 0) {
           const int phys = p.block_table[(size_t)b * p.max_pages + lp];
           if (phys >= 0 && phys < p.num_pages)
-            src = (long long)phys * p.Hkv + h;
+            src = ((long long)phys * p.Hkv + h) * kStage4;
           else
             set_err(p.dev_err, KVQ_DEVERR_PAGE);
         } else {
-          src = (((long long)b * p.Hkv + h) * p.cap + (long long)lp * kPage) * kRec8;
+          src = (((long long)b * p.Hkv + h) * (p.cap / kPage) + lp) * kStage8;
         }
       }
-      const int n = (int)min(32LL, p1 - base);
+      const int n = min(32, npages - base);
+      int halt = 0;
       for (int j = 0; j < n; ++j) {
         const long long sj = __shfl_sync(0xffffffffu, src, j);
-        int halt = 0;
-        if (lane == 0) {
-          const long long k = base + j - p0;
-          const int s = (int)(k % nst);
-          const int f = (int)(k / nst);
+        if (lane == 0 && !halt) {
           if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
             set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
             flags[0] = 1;
-          }
-          if (flags[0]) {
             halt = 1;
           } else {
-            uint8_t* st = stages + (size_t)s * kStage;
             if (sj < 0) {
               valid[s] = 0;
               mbar_arrive(&full[s]);
-            } else if (FMT == 0) {
-              const size_t ph = (size_t)sj;
-              valid[s] = 1;
-              mbar_arrive_expect_tx(&full[s], kStage4);
-              bulk_g2s(st, p.kc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
-              bulk_g2s(st + kPage * kRec4, p.vc + ph * (kPage * kRec4), kPage * kRec4, &full[s], pol);
-              bulk_g2s(st + 2 * kPage * kRec4, p.km + ph * kPage, kPage * 4, &full[s], pol);
-              bulk_g2s(st + 2 * kPage * kRec4 + kPage * 4, p.vm + ph * kPage, kPage * 4, &full[s], pol);
             } else {
               valid[s] = 1;
-              mbar_arrive_expect_tx(&full[s], kStage8);
-              bulk_g2s(st, p.kc + sj, kPage * kRec8, &full[s], pol);
-              bulk_g2s(st + kPage * kRec8, p.vc + sj, kPage * kRec8, &full[s], pol);
+              mbar_arrive_expect_tx(&full[s], kStage);
+              bulk_g2s(stages + (size_t)s * kStage, p.blocks + sj, kStage, &full[s], pol);
             }
-            issued = k + 1;
+            ++issued;
+            if (++s == nst) {
+              s = 0;
+              ++f;
+            }
           }
         }
-        if (__shfl_sync(0xffffffffu, halt, 0)) {
-          stop = true;
-          break;
-        }
       }
+      if (__shfl_sync(0xffffffffu, halt | flags[0], 0)) break;
     }
     // Do not retire while copies into this CTA's shared memory may be in flight.
     if (lane == 0) {
-      for (int s = 0; s < nst; ++s) {
-        if (issued <= s) break;
-        const long long last = s + ((issued - 1 - s) / nst) * nst;
-        const int f = (int)(last / nst);
-        if (!mbar_wait_bounded(&full[s], f & 1)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+      for (int st = 0; st < nst && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / nst) * nst;
+        if (!mbar_wait_bounded(&full[st], (last / nst) & 1)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
       }
     }
     return;
@@ -407,11 +389,11 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, N
     const int p_last = ctxb + p.S - 1;
     const int slot_last = FMT == 1 ? p_last % p.cap : 0;
 
-    const long long off = (seg_start - p0) % p.nkg;
-    for (long long pg = seg_start + ((kg - off + p.nkg) % p.nkg); pg < seg_end; pg += p.nkg) {
-      const long long k = pg - p0;
-      const int s = (int)(k % nst);
-      const int f = (int)(k / nst);
+    const int k_beg = (int)(seg_start - p0), k_end = (int)(seg_end - p0);
+    for (int k = k_beg + ((kg - k_beg % p.nkg + p.nkg) % p.nkg); k < k_end; k += p.nkg) {
+      const long long pg = p0 + k;
+      const int s = k % nst;
+      const int f = k / nst;
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], f & 1));
       if (!ok) {
         if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
@@ -784,10 +766,7 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
   p.dev_err = job.dev_err;
   long long p_max;
   if (job.fmt == 0) {
-    p.kc = job.cache.k_codes;
-    p.vc = job.cache.v_codes;
-    p.km = job.cache.k_meta;
-    p.vm = job.cache.v_meta;
+    p.blocks = job.cache.pages;
     p.block_table = job.cache.block_table;
     p.max_pages = job.cache.max_pages_per_seq;
     p.num_pages = job.cache.num_pages;
@@ -795,8 +774,7 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p.score_scale = job.sm_scale * kLog2e;
     p_max = (long long)p.Hkv * p.B * p.max_pages;
   } else {
-    p.kc = job.ring.k;
-    p.vc = job.ring.v;
+    p.blocks = job.ring.data;
     p.cap = job.ring.capacity;
     p.window = job.window;
     p.v_scale = job.v_scale;

@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         continue;
       }
       const int slot = pos & (kPage - 1);
-      const size_t rec = ((size_t)page * Hkv + h) * kPage + slot;
+      uint8_t* blk = j.cache.pages + ((size_t)page * Hkv + h) * KVQ_INT4_BLOCK_BYTES;
+      uint32_t* meta = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kRec4);
       const size_t row = (size_t)tok * Hkv + h;
 
       float x[4];
@@ -173,14 +174,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         float y[4];
         prologue(Ms, nbuf, x, j.eps, lane, y);  // lane holds y[lane + 32u]
         const Quant4 q = quantize(y);
-        uint8_t* dst = j.cache.k_codes + rec * kRec4;
+        uint8_t* dst = blk + slot * kRec4;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t hi = __shfl_down_sync(0xffffffffu, q.c[u], 1);
           if ((lane & 1) == 0) dst[(lane + 32 * u) >> 1] = (uint8_t)(q.c[u] | (hi << 4));
         }
         if (lane == 0) {
-          j.cache.k_meta[rec] = q.meta;
+          meta[slot] = q.meta;
           if (q.flags) set_err(j.dev_err, q.flags);
         }
       }
@@ -192,10 +193,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         const Quant4 q = quantize(x);  // lane holds elements 4l..4l+3
         const uint32_t two = (q.c[0] | (q.c[1] << 4)) | ((q.c[2] | (q.c[3] << 4)) << 8);
         const int chunk = (lane >> 3) ^ ((slot >> 1) & 3);
-        *reinterpret_cast<uint16_t*>(j.cache.v_codes + rec * kRec4 + chunk * 16 + ((2 * lane) & 15)) =
+        *reinterpret_cast<uint16_t*>(blk + kPage * kRec4 + slot * kRec4 + chunk * 16 + ((2 * lane) & 15)) =
             (uint16_t)two;
         if (lane == 0) {
-          j.cache.v_meta[rec] = q.meta;
+          meta[kPage + slot] = q.meta;
           if (q.flags) set_err(j.dev_err, q.flags);
         }
       }
@@ -237,8 +238,10 @@ __global__ void fp8_append_kernel(const Fp8AppendJob j) {
       continue;
     }
     const int slot = pos % j.ring.capacity;
-    const size_t rec = ((size_t)seq * Hkv + h) * j.ring.capacity + slot;
-    const int off = ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
+    // block of 64 slots: K records then V records
+    uint8_t* blk = j.ring.data + (((size_t)seq * Hkv + h) * (j.ring.capacity / kPage) + slot / kPage) *
+                                     (2 * kPage * kRec8);
+    const int off = (slot % kPage) * kRec8 + ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
     for (int which = 0; which < 2; ++which) {
       float x[4];
       load_row(which ? j.v : j.k, j.bf16, (size_t)tok * Hkv + h, lane, x);
@@ -249,8 +252,7 @@ __global__ void fp8_append_kernel(const Fp8AppendJob j) {
       const float sc = which ? j.v_scale : j.k_scale;
       const uint32_t lo = pack_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
       const uint32_t hi = pack_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc));
-      uint8_t* base = which ? j.ring.v : j.ring.k;
-      *reinterpret_cast<uint32_t*>(base + rec * kRec8 + off) = lo | (hi << 16);
+      *reinterpret_cast<uint32_t*>(blk + which * kPage * kRec8 + off) = lo | (hi << 16);
     }
   }
 }

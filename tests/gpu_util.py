@@ -50,18 +50,21 @@ def unpack_int4(tensors, b, h, L):
     """Logical K/V codes and fp16 scale/offset bits of positions 0..L-1 of sequence b, head h."""
     bt = tensors["block_table"][b].cpu().numpy()
     pos = np.arange(L)
-    pages = torch.from_numpy(bt[pos // 64].astype(np.int64)).to(tensors["k_codes"].device)
-    slots = torch.from_numpy((pos % 64).astype(np.int64)).to(tensors["k_codes"].device)
-    kc = tensors["k_codes"][pages, h, slots].cpu().numpy()
-    vc = tensors["v_codes"][pages, h, slots].cpu().numpy()
-    km = tensors["k_meta"][pages, h, slots].cpu().numpy().view(np.uint32)
-    vm = tensors["v_meta"][pages, h, slots].cpu().numpy().view(np.uint32)
+    dev = tensors["pages"].device
+    pages = torch.from_numpy(bt[pos // 64].astype(np.int64)).to(dev)
+    blk = tensors["pages"][pages, h].cpu().numpy()          # [L, 8704]: each position's page-head block
+    slot = pos % 64
+    rows = np.arange(L)
+    kc = blk[rows[:, None], slot[:, None] * 64 + np.arange(64)[None, :]]
+    vc = blk[rows[:, None], 4096 + slot[:, None] * 64 + np.arange(64)[None, :]]
+    meta = blk[:, 8192:8704].copy().view(np.uint32)          # [L, 128]: K meta 0..63, V meta 64..127
+    km = meta[rows, slot]
+    vm = meta[rows, 64 + slot]
     # undo the V chunk swizzle: logical chunk c sits at physical chunk c ^ ((slot >> 1) & 3)
-    sw = (pos % 64 >> 1) & 3
+    sw = (slot >> 1) & 3
     vlog = np.empty_like(vc)
     for c in range(4):
-        pc = c ^ sw
-        idx = (pc[:, None] * 16 + np.arange(16)[None, :])
+        idx = ((c ^ sw)[:, None] * 16 + np.arange(16)[None, :])
         vlog[:, c * 16:(c + 1) * 16] = np.take_along_axis(vc, idx, axis=1)
     return {
         "kc": _nibbles(kc), "ks": (km & 0xFFFF).astype(np.uint16), "ko": (km >> 16).astype(np.uint16),
@@ -71,10 +74,14 @@ def unpack_int4(tensors, b, h, L):
 
 def unpack_fp8(tensors, b, h, positions):
     """Logical e4m3 K/V bytes [n, 128] of the given positions of sequence b, head h."""
-    cap = tensors["k"].shape[2]
+    data = tensors["data"][b, h].cpu().numpy()              # [cap/64, 16384]
+    cap = data.shape[0] * 64
     slots = np.asarray(positions) % cap
-    k = tensors["k"][b, h].cpu().numpy()[slots]
-    v = tensors["v"][b, h].cpu().numpy()[slots]
+    blk = data[slots // 64]
+    within = slots % 64
+    rows = np.arange(len(slots))
+    k = blk[rows[:, None], within[:, None] * 128 + np.arange(128)[None, :]]
+    v = blk[rows[:, None], 8192 + within[:, None] * 128 + np.arange(128)[None, :]]
     sw = slots & 7
     out = []
     for x in (k, v):

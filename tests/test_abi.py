@@ -59,8 +59,8 @@ def test_workspace_bytes():
 
 
 def _fake_cache(**over):
-    d = dict(k_codes=0x10000, k_meta=0x20000, v_codes=0x30000, v_meta=0x40000, block_table=0x50000, num_seqs=4,
-             max_pages_per_seq=8, num_pages=32, num_kv_heads=4, page_size=64, head_dim=128)
+    d = dict(pages=0x10000, block_table=0x50000, num_seqs=4, max_pages_per_seq=8, num_pages=32, num_kv_heads=4,
+             page_size=64, head_dim=128)
     d.update(over)
     return kvq.Int4Cache(**d)
 
@@ -87,12 +87,12 @@ def test_host_validation_rejects_before_launch():
     assert _attn(c, q=0) == 1
     assert _attn(c, err=0) == 1
     assert _attn(c, sm=float("nan")) == 1
-    assert _attn(_fake_cache(k_codes=0x10008)) == 1  # cache array not 16-byte aligned
-    ring = kvq.Fp8Ring(0x10000, 0x20000, 4, 4, 576, 128)
+    assert _attn(_fake_cache(pages=0x10008)) == 1  # cache array not 16-byte aligned
+    ring = kvq.Fp8Ring(0x10000, 4, 4, 576, 128)
     f = kvq.lib.kvq_decode_attn_fp8_swa
     assert f(ctypes.byref(ring), 0x80000, 1, 2, 1, 20, 0x90000, 600, None, None, 0.01, 0.01, 0.088, 0xA0000,
              0xB0000, 1 << 30, 0xC0000, None) == 1  # window larger than the ring
-    bad_ring = kvq.Fp8Ring(0x10000, 0x20000, 4, 4, 500, 128)
+    bad_ring = kvq.Fp8Ring(0x10000, 4, 4, 500, 128)
     assert f(ctypes.byref(bad_ring), 0x80000, 1, 2, 1, 20, 0x90000, 400, None, None, 0.01, 0.01, 0.088, 0xA0000,
              0xB0000, 1 << 30, 0xC0000, None) == 1  # capacity not a multiple of 64
     assert kvq.lib.kvq_build_rotation(1, 64, None, 0x1000) == 2
