@@ -233,7 +233,10 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
   if (workspace_bytes < kvq_decode_workspace_bytes(B, S, num_q_heads, ring->num_kv_heads))
     return KVQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (k_new) {
+  // The attention kernel appends the new rows itself when one CTA owns each (sequence, KV
+  // head); beyond that many segments the rows are appended by a separate launch first.
+  const bool fused_append = (long long)B * ring->num_kv_heads <= kvq::kMaxCtas;
+  if (k_new && !fused_append) {
     kvq::Fp8AppendJob j{};
     j.ring = *ring;
     j.k = k_new;
@@ -261,6 +264,8 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
   a.ctx = pos0;
   a.q = q;
   a.q_bf16 = dtype == KVQ_BF16;
+  a.k_new = fused_append ? k_new : nullptr;
+  a.v_new = fused_append ? v_new : nullptr;
   a.sm_scale = sm_scale;
   a.out = out;
   a.partials = reinterpret_cast<float*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads));

@@ -70,6 +70,13 @@ struct AttnParams {
   int32_t* dev_err;
   int ntg, nkg, nstages, rows_pad;
   int n_cta;
+  // direct: every CTA covers whole segments and writes the normalised output itself
+  int direct;
+  // fp8 only: rows to append before attending ([B][S][Hkv][128] or null), their dtype and scale
+  const void* k_new;
+  const void* v_new;
+  int kv_bf16;
+  float k_scale;
 };
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -186,8 +193,12 @@ __device__ __forceinline__ int out_dim(int mt, int row) {
   return 16 * mt + 2 * (row & 7) + (row >> 3);
 }
 
+// FP8 window layers: one CTA per (sequence, KV head), up to 8 consumer warps.
+constexpr int kFp8Groups = 8;
+
 template <int FMT, int NT>
-__global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, NT == 1 ? KVQ_MIN_CTAS : 1)
+__global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_TOKEN_GROUPS) + 1) : 160,
+                                  (FMT == 0 && NT == 1) ? KVQ_MIN_CTAS : 1)
     attn_kernel(const AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kStage = FMT == 0 ? kStage4 : kStage8;
@@ -224,6 +235,31 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, N
   // The 32 lanes resolve the source blocks of 32 consecutive pages at once (block-table
   // loads in parallel); lane 0 then issues one bulk copy per page, in order, as stages free.
   if (warp == nwc) {
+    if (FMT == 1 && p.k_new != nullptr) {
+      // Append this segment's new rows into the ring first (one CTA per segment in this mode),
+      // then order those generic writes before the bulk copies that read them back.
+      int b, h, lp, np;
+      decode_page(pre, p.B, p.Hkv, p0, b, h, lp, np);
+      bool dummy = false;
+      const int c0 = eff_ctx(p, b, dummy, FMT);
+      for (int r = 0; r < p.S; ++r) {
+        const int slot = (c0 + r) % p.cap;
+        uint8_t* blk = const_cast<uint8_t*>(p.blocks) +
+                       (((size_t)b * p.Hkv + h) * (p.cap / kPage) + slot / kPage) * kStage8;
+        const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
+        for (int which = 0; which < 2; ++which) {
+          float x[4];
+          load_row4(which ? p.v_new : p.k_new, p.kv_bf16, row, lane, x);
+          if (!warp_all_finite(x)) {
+            if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
+            continue;
+          }
+          fp8_store_row(blk + which * kPage * kRec8, slot, x, which ? p.v_scale : p.k_scale, lane);
+        }
+      }
+      fence_proxy_async_global();
+      __syncwarp();
+    }
     const uint64_t pol = policy_evict_first();
     const int npages = (int)(p1 - p0);
     int issued = 0;
@@ -651,7 +687,24 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (KVQ_TOKEN_GROUPS + 1) : 160, N
       }
     }
     named_barrier(1, nwc * 32);
-    {
+    if (p.direct) {
+      // whole segment in this CTA: merge the token groups and write the normalised output
+      for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
+        const int row = e / kD, d = e - row * kD;
+        float M = -INFINITY;
+        for (int kk = 0; kk < p.nkg; ++kk) M = fmaxf(M, red[((size_t)kk * p.rows_pad + row) * kPartialStride]);
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        float lsum = 0.0f, a = 0.0f;
+        for (int kk = 0; kk < p.nkg; ++kk) {
+          const float* src = red + ((size_t)kk * p.rows_pad + row) * kPartialStride;
+          const float w = fast_exp2(src[0] - Mu);
+          lsum += w * src[1];
+          a += w * src[2 + d];
+        }
+        const int r = row / G, gi = row - (row / G) * G;
+        p.out[(((size_t)b * p.S + r) * p.Hq + h * G + gi) * kD + d] = a / lsum;
+      }
+    } else {
       float* dstp = p.partials + ((size_t)(blockIdx.x + seg) * R) * kPartialStride;
       for (int e = threadIdx.x; e < R * kPartialStride; e += nwc * 32) {
         const int row = e / kPartialStride, c = e - row * kPartialStride;
@@ -734,10 +787,11 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   occ = std::max(occ, 1);
   long long grid = std::min<long long>((long long)dc.sm * occ, kMaxCtas);
   grid = std::max<long long>(1, std::min(grid, p_max));
+  if (p.direct) grid = std::min<long long>((long long)p.B * p.Hkv, kMaxCtas);
   p.n_cta = (int)grid;
   attn_kernel<FMT, NT><<<(unsigned)grid, threads, smem, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.direct) return e;
   const size_t csmem = (p.B + 1 + 4) * sizeof(int);
   combine_kernel<FMT><<<(unsigned)(p.B * p.Hkv * p.R), 128, csmem, stream>>>(p);
   return cudaGetLastError();
@@ -785,21 +839,28 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
   }
   const int ntiles = (p.R + 7) / 8;
   int NT;
-  if (ntiles == 1) {
-    NT = 1;
-    p.ntg = 1;
-    p.nkg = KVQ_TOKEN_GROUPS;
-    p.nstages = job.fmt == 0 ? KVQ_STAGES_INT4 : KVQ_TOKEN_GROUPS;
-  } else if (ntiles <= 3) {
+  if (ntiles <= 3) {
     NT = ntiles;
     p.ntg = 1;
-    p.nkg = 4;
-    p.nstages = job.fmt == 0 ? 8 : 4;
+    p.nkg = NT == 1 ? KVQ_TOKEN_GROUPS : 4;
+    p.nstages = NT == 1 ? KVQ_STAGES_INT4 : 8;
   } else {
     NT = (ntiles + 1) / 2;
     p.ntg = 2;
     p.nkg = 2;
     p.nstages = 4;
+  }
+  if (job.fmt == 1) {
+    // window layers: one CTA per (sequence, KV head) over the whole ring, output written directly;
+    // all of a segment's blocks in flight at once (up to 9 stages of 16 KB)
+    const int nblk = p.cap / kPage;
+    p.direct = (long long)p.B * p.Hkv <= kMaxCtas ? 1 : 0;
+    p.nkg = std::min(NT == 1 ? kFp8Groups : 2, nblk);
+    p.nstages = std::min(nblk, 9);
+    p.k_new = job.k_new;
+    p.v_new = job.v_new;
+    p.kv_bf16 = job.q_bf16;
+    p.k_scale = job.k_scale;
   }
   p.rows_pad = p.ntg * NT * 8;
   const int threads = (p.ntg * p.nkg + 1) * 32;

@@ -204,4 +204,42 @@ __device__ __forceinline__ void set_err(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }
 
+// One 128-element row (lane l holds x[4l..4l+3]) as e4m3(x / scale): IEEE division, nearest
+// even, saturating; stored into the record of `slot` of a 64-slot ring block half (K or V),
+// with the record's 16-byte chunks in XOR order (chunk c at c ^ (slot & 7)).
+__device__ __forceinline__ void fp8_store_row(uint8_t* block_half, int slot, const float (&x)[4], float scale,
+                                              int lane) {
+  const uint32_t lo = pack_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
+  const uint32_t hi = pack_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
+  const int off = (slot % kPage) * kRec8 + ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
+  *reinterpret_cast<uint32_t*>(block_half + off) = lo | (hi << 16);
+}
+
+// Lane l's four elements of row `row` of a [rows][128] tensor of fp32 or bf16.
+__device__ __forceinline__ void load_row4(const void* base, int bf16, size_t row, int lane, float (&x)[4]) {
+  if (bf16) {
+    const uint2 u = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row * kD)[lane];
+    x[0] = bf16_bits_to_f32(u.x & 0xFFFFu);
+    x[1] = bf16_bits_to_f32(u.x >> 16);
+    x[2] = bf16_bits_to_f32(u.y & 0xFFFFu);
+    x[3] = bf16_bits_to_f32(u.y >> 16);
+  } else {
+    const float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kD)[lane];
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+  }
+}
+
+__device__ __forceinline__ bool warp_all_finite(const float (&x)[4]) {
+  const bool ok = isfinite(x[0]) && isfinite(x[1]) && isfinite(x[2]) && isfinite(x[3]);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Orders this thread's generic-proxy global writes before later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 }  // namespace kvq

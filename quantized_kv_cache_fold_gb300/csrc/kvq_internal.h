@@ -68,6 +68,8 @@ struct AttnJob {
   const float* q_rot;  // int4: rotated queries [B][S][Hq][128] fp32 (workspace)
   const void* q;       // fp8: queries as given
   int q_bf16;
+  const void* k_new;   // fp8: rows appended inside the attention kernel (null: none)
+  const void* v_new;
   float sm_scale;
   float* out;
   float* partials;  // workspace

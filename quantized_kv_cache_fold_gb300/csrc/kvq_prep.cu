@@ -32,27 +32,6 @@ struct PrepParams {
   int q_jobs;
 };
 
-__device__ __forceinline__ void load_row(const void* base, int bf16, size_t row, int lane, float (&x)[4]) {
-  if (bf16) {
-    const uint2 u = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row * kD)[lane];
-    x[0] = bf16_bits_to_f32(u.x & 0xFFFFu);
-    x[1] = bf16_bits_to_f32(u.x >> 16);
-    x[2] = bf16_bits_to_f32(u.y & 0xFFFFu);
-    x[3] = bf16_bits_to_f32(u.y >> 16);
-  } else {
-    const float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * kD)[lane];
-    x[0] = f.x;
-    x[1] = f.y;
-    x[2] = f.z;
-    x[3] = f.w;
-  }
-}
-
-__device__ __forceinline__ bool warp_all_finite(const float (&x)[4]) {
-  const bool ok = isfinite(x[0]) && isfinite(x[1]) && isfinite(x[2]) && isfinite(x[3]);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // y = M n(x). Lane l holds x[4l..4l+3] and returns y[l + 32u], u = 0..3.
 // Ms: shared [128][kMStride] (Ms[j*kMStride + i] = M[j][i]); nbuf: shared float[128] of this warp.
 __device__ __forceinline__ void prologue(const float* __restrict__ Ms, float* nbuf, const float (&x)[4], float eps,
@@ -137,7 +116,22 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   const PrepJobs& j = p.j;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
-  for (int e = threadIdx.x; e < kD * kD; e += kPrepThreads) Ms[(e >> 7) * kMStride + (e & 127)] = M[e];
+  {
+    // 16 independent 16-byte loads per thread, then the padded (conflict-free) shared stores
+    constexpr int kPer = kD * kD / 4 / kPrepThreads;
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) v[u] = reinterpret_cast<const float4*>(M)[threadIdx.x + u * kPrepThreads];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = 4 * (threadIdx.x + u * kPrepThreads);
+      float* d = Ms + (e >> 7) * kMStride + (e & 127);
+      d[0] = v[u].x;
+      d[1] = v[u].y;
+      d[2] = v[u].z;
+      d[3] = v[u].w;
+    }
+  }
   __syncthreads();
 
   const int Hkv = j.cache.num_kv_heads;
@@ -167,7 +161,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       const size_t row = (size_t)tok * Hkv + h;
 
       float x[4];
-      load_row(j.k, j.kv_bf16, row, lane, x);
+      load_row4(j.k, j.kv_bf16, row, lane, x);
       if (!warp_all_finite(x)) {
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       } else {
@@ -186,7 +180,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         }
       }
 
-      load_row(j.v, j.kv_bf16, row, lane, x);
+      load_row4(j.v, j.kv_bf16, row, lane, x);
       if (!warp_all_finite(x)) {
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       } else {
@@ -205,7 +199,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
     const int qb = blockIdx.x - p.kv_blocks, nqb = gridDim.x - p.kv_blocks;
     for (int row = qb * kPrepWarps + warp; row < p.q_jobs; row += nqb * kPrepWarps) {
       float x[4];
-      load_row(j.q, j.q_bf16, (size_t)row, lane, x);
+      load_row4(j.q, j.q_bf16, (size_t)row, lane, x);
       if (!warp_all_finite(x) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       float y[4];
       prologue(Ms, nbuf, x, j.eps, lane, y);
@@ -241,18 +235,14 @@ __global__ void fp8_append_kernel(const Fp8AppendJob j) {
     // block of 64 slots: K records then V records
     uint8_t* blk = j.ring.data + (((size_t)seq * Hkv + h) * (j.ring.capacity / kPage) + slot / kPage) *
                                      (2 * kPage * kRec8);
-    const int off = (slot % kPage) * kRec8 + ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
     for (int which = 0; which < 2; ++which) {
       float x[4];
-      load_row(which ? j.v : j.k, j.bf16, (size_t)tok * Hkv + h, lane, x);
+      load_row4(which ? j.v : j.k, j.bf16, (size_t)tok * Hkv + h, lane, x);
       if (!warp_all_finite(x)) {
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
         continue;
       }
-      const float sc = which ? j.v_scale : j.k_scale;
-      const uint32_t lo = pack_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
-      const uint32_t hi = pack_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc));
-      *reinterpret_cast<uint32_t*>(blk + which * kPage * kRec8 + off) = lo | (hi << 16);
+      fp8_store_row(blk + which * kPage * kRec8, slot, x, which ? j.v_scale : j.k_scale, lane);
     }
   }
 }
