@@ -762,6 +762,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
 struct DevCache {
   int sm = 0;
   bool attr[2][4] = {{false}};
+  size_t occ_smem[2][4] = {{0}};  // occupancy cache: last (smem, threads) queried per instantiation
+  int occ_threads[2][4] = {{0}};
+  int occ[2][4] = {{0}};
 };
 DevCache g_dev[64];
 
@@ -781,10 +784,16 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
     if (e != cudaSuccess) return e;
     dc.attr[FMT][NT] = true;
   }
-  int occ = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<FMT, NT>, threads, smem);
-  if (e != cudaSuccess) return e;
-  occ = std::max(occ, 1);
+  cudaError_t e = cudaSuccess;
+  if (dc.occ_smem[FMT][NT] != smem || dc.occ_threads[FMT][NT] != threads) {
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<FMT, NT>, threads, smem);
+    if (e != cudaSuccess) return e;
+    dc.occ[FMT][NT] = std::max(o, 1);
+    dc.occ_smem[FMT][NT] = smem;
+    dc.occ_threads[FMT][NT] = threads;
+  }
+  const int occ = dc.occ[FMT][NT];
   long long grid = std::min<long long>((long long)dc.sm * occ, kMaxCtas);
   grid = std::max<long long>(1, std::min(grid, p_max));
   if (p.direct) grid = std::min<long long>((long long)p.B * p.Hkv, kMaxCtas);
