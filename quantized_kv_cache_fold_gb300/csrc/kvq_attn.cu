@@ -77,6 +77,9 @@ struct AttnParams {
   const void* v_new;
   int kv_bf16;
   float k_scale;
+  // int4: per-segment arrival counters (zeroed by the prologue kernel); the last CTA to finish
+  // a segment merges its partials and writes the output. Null: separate combine pass.
+  int* counters;
 };
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -92,7 +95,7 @@ struct SmemLayout {
     valid = empty + 8 * nstages;
     pre = valid + 4 * nstages;
     flags = pre + 4 * (B + 1);
-    red = align_up(flags + 16, 16);
+    red = align_up(flags + 32, 16);
     total = red + (size_t)nkg * rows_pad * kPartialStride * 4;
   }
 };
@@ -193,8 +196,9 @@ __device__ __forceinline__ int out_dim(int mt, int row) {
   return 16 * mt + 2 * (row & 7) + (row >> 3);
 }
 
-// FP8 window layers: one CTA per (sequence, KV head), up to 8 consumer warps.
-constexpr int kFp8Groups = 8;
+// FP8 window layers: one CTA per (sequence, KV head) when the ring has at most kFp8Groups
+// 64-slot blocks; one consumer warp and one stage per block, output written directly.
+constexpr int kFp8Groups = kFp8DirectBlocks;
 
 template <int FMT, int NT>
 __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_TOKEN_GROUPS) + 1) : 160,
@@ -235,30 +239,58 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_T
   // The 32 lanes resolve the source blocks of 32 consecutive pages at once (block-table
   // loads in parallel); lane 0 then issues one bulk copy per page, in order, as stages free.
   if (warp == nwc) {
-    if (FMT == 1 && p.k_new != nullptr) {
-      // Append this segment's new rows into the ring first (one CTA per segment in this mode),
-      // then order those generic writes before the bulk copies that read them back.
+    if (FMT == 1 && p.direct) {
+      // Whole ring of one (sequence, KV head); one stage per block. Blocks without a new row
+      // are requested first; the new rows are then written into the ring, ordered before the
+      // bulk copies that read them back (proxy fence), and their blocks requested last.
+      const uint64_t pol = policy_evict_first();
       int b, h, lp, np;
       decode_page(pre, p.B, p.Hkv, p0, b, h, lp, np);
       bool dummy = false;
       const int c0 = eff_ctx(p, b, dummy, FMT);
-      for (int r = 0; r < p.S; ++r) {
-        const int slot = (c0 + r) % p.cap;
-        uint8_t* blk = const_cast<uint8_t*>(p.blocks) +
-                       (((size_t)b * p.Hkv + h) * (p.cap / kPage) + slot / kPage) * kStage8;
-        const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
-        for (int which = 0; which < 2; ++which) {
-          float x[4];
-          load_row4(which ? p.v_new : p.k_new, p.kv_bf16, row, lane, x);
-          if (!warp_all_finite(x)) {
-            if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
-            continue;
-          }
-          fp8_store_row(blk + which * kPage * kRec8, slot, x, which ? p.v_scale : p.k_scale, lane);
+      const int nblk = p.cap / kPage;
+      uint32_t newmask = 0;
+      if (p.k_new != nullptr)
+        for (int r = 0; r < p.S; ++r) newmask |= 1u << (((c0 + r) % p.cap) / kPage);
+      const uint8_t* seg_base = p.blocks + ((size_t)b * p.Hkv + h) * nblk * (size_t)kStage8;
+      if (lane == 0) {
+        for (int j = 0; j < nblk; ++j) {
+          if (newmask >> j & 1u) continue;
+          valid[j] = 1;
+          mbar_arrive_expect_tx(&full[j], kStage8);
+          bulk_g2s(stages + (size_t)j * kStage, seg_base + (size_t)j * kStage8, kStage8, &full[j], pol);
         }
       }
-      fence_proxy_async_global();
-      __syncwarp();
+      if (newmask) {
+        for (int r = 0; r < p.S; ++r) {
+          const int slot = (c0 + r) % p.cap;
+          uint8_t* blk = const_cast<uint8_t*>(seg_base) + (size_t)(slot / kPage) * kStage8;
+          const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
+          for (int which = 0; which < 2; ++which) {
+            float x[4];
+            load_row4(which ? p.v_new : p.k_new, p.kv_bf16, row, lane, x);
+            if (!warp_all_finite(x)) {
+              if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
+              continue;
+            }
+            fp8_store_row(blk + which * kPage * kRec8, slot, x, which ? p.v_scale : p.k_scale, lane);
+          }
+        }
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) {
+          for (int j = 0; j < nblk; ++j) {
+            if (!(newmask >> j & 1u)) continue;
+            valid[j] = 1;
+            mbar_arrive_expect_tx(&full[j], kStage8);
+            bulk_g2s(stages + (size_t)j * kStage, seg_base + (size_t)j * kStage8, kStage8, &full[j], pol);
+          }
+        }
+      }
+      if (lane == 0)
+        for (int j = 0; j < nblk; ++j)
+          if (!mbar_wait_bounded(&full[j], 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+      return;
     }
     const uint64_t pol = policy_evict_first();
     const int npages = (int)(p1 - p0);
@@ -687,7 +719,10 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_T
       }
     }
     named_barrier(1, nwc * 32);
-    if (p.direct) {
+    // CTAs covering this segment (its pages are split over c_first..c_last)
+    const long long first_pg = (long long)p.Hkv * pre[b] + (long long)h * np;
+    const int c_first = (int)cta_of(first_pg, P, n_eff), c_last = (int)cta_of(first_pg + np - 1, P, n_eff);
+    if (p.direct || (p.counters != nullptr && c_first == c_last)) {
       // whole segment in this CTA: merge the token groups and write the normalised output
       for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
         const int row = e / kD, d = e - row * kD;
@@ -722,6 +757,32 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_T
           }
         }
         dstp[e] = v;
+      }
+      if (p.counters != nullptr) {
+        // publish the partial; the last of the segment's CTAs merges all of them (no waiting)
+        __threadfence();
+        named_barrier(1, nwc * 32);
+        if (threadIdx.x == 0) flags[2] = atomicAdd(&p.counters[seg], 1) == c_last - c_first ? 1 : 0;
+        named_barrier(1, nwc * 32);
+        if (flags[2]) {
+          __threadfence();
+          for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
+            const int row = e / kD, d = e - row * kD;
+            float M = -INFINITY;
+            for (int c = c_first; c <= c_last; ++c)
+              M = fmaxf(M, __ldcg(p.partials + ((size_t)(c + seg) * R + row) * kPartialStride));
+            const float Mu = M == -INFINITY ? 0.0f : M;
+            float lsum = 0.0f, a = 0.0f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const float* src = p.partials + ((size_t)(c + seg) * R + row) * kPartialStride;
+              const float w = fast_exp2(__ldcg(src) - Mu);
+              lsum += w * __ldcg(src + 1);
+              a += w * __ldcg(src + 2 + d);
+            }
+            const int r = row / G, gi = row - (row / G) * G;
+            p.out[(((size_t)b * p.S + r) * p.Hq + h * G + gi) * kD + d] = a / lsum;
+          }
+        }
       }
     }
     named_barrier(1, nwc * 32);
@@ -800,7 +861,7 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   p.n_cta = (int)grid;
   attn_kernel<FMT, NT><<<(unsigned)grid, threads, smem, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess || p.direct) return e;
+  if (e != cudaSuccess || p.direct || p.counters != nullptr) return e;
   const size_t csmem = (p.B + 1 + 4) * sizeof(int);
   combine_kernel<FMT><<<(unsigned)(p.B * p.Hkv * p.R), 128, csmem, stream>>>(p);
   return cudaGetLastError();
@@ -809,6 +870,8 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
 }  // namespace
 
 size_t workspace_qrot_bytes(int B, int S, int Hq) { return align_up((size_t)B * S * Hq * kD * 4, 256); }
+
+size_t workspace_counters_bytes(int B, int Hkv) { return align_up((size_t)B * Hkv * 4, 256); }
 
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv) {
   const int G = Hq / Hkv;
@@ -834,6 +897,7 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p.max_pages = job.cache.max_pages_per_seq;
     p.num_pages = job.cache.num_pages;
     p.q_rot = job.q_rot;
+    p.counters = job.counters;
     p.score_scale = job.sm_scale * kLog2e;
     p_max = (long long)p.Hkv * p.B * p.max_pages;
   } else {
@@ -860,12 +924,18 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p.nstages = 4;
   }
   if (job.fmt == 1) {
-    // window layers: one CTA per (sequence, KV head) over the whole ring, output written directly;
-    // all of a segment's blocks in flight at once (up to 9 stages of 16 KB)
+    // window layers: when the ring has at most kFp8Groups blocks, one CTA per (sequence, KV head)
+    // with one stage (and, for one query tile, one consumer warp) per block, output written
+    // directly; otherwise the general split with a combine pass
     const int nblk = p.cap / kPage;
-    p.direct = (long long)p.B * p.Hkv <= kMaxCtas ? 1 : 0;
-    p.nkg = std::min(NT == 1 ? kFp8Groups : 2, nblk);
-    p.nstages = std::min(nblk, 9);
+    p.direct = ((long long)p.B * p.Hkv <= kMaxCtas && nblk <= kFp8Groups) ? 1 : 0;
+    if (p.direct) {
+      p.nkg = NT == 1 ? nblk : std::min(2, nblk);
+      p.nstages = nblk;
+    } else {
+      p.nkg = NT == 1 ? 4 : 2;
+      p.nstages = 4;
+    }
     p.k_new = job.k_new;
     p.v_new = job.v_new;
     p.kv_bf16 = job.q_bf16;

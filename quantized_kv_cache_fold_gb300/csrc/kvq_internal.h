@@ -13,6 +13,7 @@ namespace kvq {
 constexpr int kMaxCtas = 1024;       // cap on attention CTAs (sizes the partial-result workspace)
 constexpr int kMaxRows = 48;         // S * (num_q_heads / num_kv_heads) rows per KV head and sequence
 constexpr int kPartialStride = 130;  // floats per partial row: m, l, acc[128]
+constexpr int kFp8DirectBlocks = 10; // window rings up to this many 64-slot blocks take the one-CTA path
 
 // Job description for the prologue/quantise kernel.
 struct PrepJobs {
@@ -34,6 +35,8 @@ struct PrepJobs {
   int nq_rows;
   float* q_rot;      // workspace destination [nq_rows][128]
   float* q_rot_out;  // optional copy
+  int* zero_ints;    // workspace counters to clear (or null)
+  int n_zero;
   float eps;
   int32_t* dev_err;
 };
@@ -73,6 +76,7 @@ struct AttnJob {
   float sm_scale;
   float* out;
   float* partials;  // workspace
+  int* counters;    // int4: per-segment arrival counters, zeroed by the prologue kernel
   int32_t* dev_err;
 };
 
@@ -81,5 +85,6 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream);
 // Workspace layout shared by the API and the launchers.
 size_t workspace_qrot_bytes(int B, int S, int Hq);
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv);
+size_t workspace_counters_bytes(int B, int Hkv);
 
 }  // namespace kvq

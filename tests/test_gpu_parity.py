@@ -223,3 +223,16 @@ def test_swa_window_wrap(orc, S):
 def test_swa_small_window(orc):
     w = Workload("swa16", 22, 3, 20, 4, 2, np.array([10, 100, 1000]), False)
     check_swa(orc, w, 1, 2, window=16, cap=64)
+
+
+def test_swa_large_ring_general_path(orc):
+    """A 1024-slot ring (16 blocks) takes the split path with a separate append and a combine pass."""
+    w = Workload("swa-ring1024", 23, 3, 20, 4, 2, np.array([40, 700, 3000]), True)
+    check_swa(orc, w, 2, 2, window=513, cap=1024)
+
+
+def test_int4_many_segments_single_cta(orc):
+    """More (sequence, KV head) segments than CTAs: short contexts, every segment in one CTA."""
+    ctx = (np.arange(300) * 7 % 180).astype(np.int64)
+    w = Workload("many", 24, len(ctx), 8, 4, 1, ctx, True)
+    check_int4(orc, w, 1, 1, [0, 1, 57, 299])
