@@ -41,7 +41,7 @@ namespace {
 #define KVQ_STAGES_INT4 8
 #endif
 #ifndef KVQ_MIN_CTAS
-#define KVQ_MIN_CTAS 1
+#define KVQ_MIN_CTAS 2
 #endif
 
 constexpr int kStage4 = 2 * kPage * kRec4 + 2 * kPage * 4;  // 8704 bytes: K codes, V codes, K meta, V meta
