@@ -146,6 +146,7 @@ __device__ void build_prefix(const AttnParams& p, int fmt, int* pre, volatile in
     pre[p.B] = carry;
     flags[0] = 0;
     flags[1] = any_bad ? 1 : 0;
+    flags[3] = 0;
   }
 }
 
@@ -758,35 +759,53 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_T
         }
         dstp[e] = v;
       }
-      if (p.counters != nullptr) {
-        // publish the partial; the last of the segment's CTAs merges all of them (no waiting)
-        __threadfence();
-        named_barrier(1, nwc * 32);
-        if (threadIdx.x == 0) flags[2] = atomicAdd(&p.counters[seg], 1) == c_last - c_first ? 1 : 0;
-        named_barrier(1, nwc * 32);
-        if (flags[2]) {
-          __threadfence();
-          for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
-            const int row = e / kD, d = e - row * kD;
-            float M = -INFINITY;
-            for (int c = c_first; c <= c_last; ++c)
-              M = fmaxf(M, __ldcg(p.partials + ((size_t)(c + seg) * R + row) * kPartialStride));
-            const float Mu = M == -INFINITY ? 0.0f : M;
-            float lsum = 0.0f, a = 0.0f;
-            for (int c = c_first; c <= c_last; ++c) {
-              const float* src = p.partials + ((size_t)(c + seg) * R + row) * kPartialStride;
-              const float w = fast_exp2(__ldcg(src) - Mu);
-              lsum += w * __ldcg(src + 1);
-              a += w * __ldcg(src + 2 + d);
-            }
-            const int r = row / G, gi = row - (row / G) * G;
-            p.out[(((size_t)b * p.S + r) * p.Hq + h * G + gi) * kD + d] = a / lsum;
-          }
-        }
+      if (p.counters != nullptr && threadIdx.x == 0) {
+        // a segment shared with other CTAs: merged after this CTA's last segment (see below)
+        const int k = flags[3]++;
+        flags[4 + 2 * k] = seg;
+        flags[5 + 2 * k] = (c_first << 16) | c_last;
       }
     }
     named_barrier(1, nwc * 32);
     seg_start = seg_end;
+  }
+
+  // Shared segments (at most this CTA's first and last): publish the partials, take a ticket;
+  // the CTA that arrives last for a segment merges every partial of it. Nothing waits.
+  if (p.counters != nullptr && flags[3] > 0) {
+    __threadfence();
+    named_barrier(1, nwc * 32);
+    if (threadIdx.x == 0)
+      for (int k = 0; k < flags[3]; ++k) {
+        const int c_first = flags[5 + 2 * k] >> 16, c_last = flags[5 + 2 * k] & 0xFFFF;
+        const bool last = atomicAdd(&p.counters[flags[4 + 2 * k]], 1) == c_last - c_first;
+        flags[5 + 2 * k] |= last ? (1 << 31) : 0;
+      }
+    named_barrier(1, nwc * 32);
+    for (int k = 0; k < flags[3]; ++k) {
+      const int word = flags[5 + 2 * k];
+      if (word >= 0) continue;  // not the last arrival
+      __threadfence();
+      const int seg = flags[4 + 2 * k];
+      const int c_first = (word >> 16) & 0x7FFF, c_last = word & 0xFFFF;
+      const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+      for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
+        const int row = e / kD, d = e - row * kD;
+        float M = -INFINITY;
+        for (int c = c_first; c <= c_last; ++c)
+          M = fmaxf(M, __ldcg(p.partials + ((size_t)(c + seg) * R + row) * kPartialStride));
+        const float Mu = M == -INFINITY ? 0.0f : M;
+        float lsum = 0.0f, a = 0.0f;
+        for (int c = c_first; c <= c_last; ++c) {
+          const float* src = p.partials + ((size_t)(c + seg) * R + row) * kPartialStride;
+          const float w = fast_exp2(__ldcg(src) - Mu);
+          lsum += w * __ldcg(src + 1);
+          a += w * __ldcg(src + 2 + d);
+        }
+        const int r = row / G, gi = row - (row / G) * G;
+        p.out[(((size_t)b * p.S + r) * p.Hq + h * G + gi) * kD + d] = a / lsum;
+      }
+    }
   }
 }
 
