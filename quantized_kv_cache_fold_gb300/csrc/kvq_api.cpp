@@ -122,7 +122,7 @@ kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk,
 
 size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_heads) {
   if (B < 1 || B > KVQ_MAX_SEQS || S < 1 || S > 8 || !heads_ok(num_q_heads, num_kv_heads, S)) return 0;
-  return kvq::workspace_qrot_bytes(B, S, num_q_heads) + kvq::workspace_counters_bytes(B, num_kv_heads) +
+  return kvq::workspace_qrot_bytes(B, S, num_q_heads) +
          kvq::workspace_partials_bytes(B, S, num_q_heads, num_kv_heads);
 }
 
@@ -147,9 +147,7 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* q_rot = reinterpret_cast<float*>(ws);
-  int* counters = reinterpret_cast<int*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads));
-  float* partials = reinterpret_cast<float*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads) +
-                                             kvq::workspace_counters_bytes(B, cache->num_kv_heads));
+  float* partials = reinterpret_cast<float*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads));
   cudaStream_t s = (cudaStream_t)stream;
 
   kvq::PrepJobs j{};
@@ -167,8 +165,6 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
   j.nq_rows = B * S * num_q_heads;
   j.q_rot = q_rot;
   j.q_rot_out = q_rot_out;
-  j.zero_ints = counters;
-  j.n_zero = B * cache->num_kv_heads;
   j.eps = eps;
   j.dev_err = dev_err;
   cudaError_t e = kvq::launch_prep(j, s);
@@ -186,7 +182,6 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
   a.sm_scale = sm_scale;
   a.out = out;
   a.partials = partials;
-  a.counters = counters;
   a.dev_err = dev_err;
   return from_cuda(kvq::launch_attention(a, s));
 }
@@ -274,8 +269,7 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
   a.v_new = fused_append ? v_new : nullptr;
   a.sm_scale = sm_scale;
   a.out = out;
-  a.partials = reinterpret_cast<float*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads) +
-                                        kvq::workspace_counters_bytes(B, ring->num_kv_heads));
+  a.partials = reinterpret_cast<float*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads));
   a.dev_err = dev_err;
   return from_cuda(kvq::launch_attention(a, s));
 }

@@ -31,17 +31,16 @@
 namespace kvq {
 namespace {
 
-// Tuning of the attention CTA when one warp covers every query row of a KV head (S*G <= 24):
-// consumer token groups, shared-memory pipeline stages (a multiple of the token groups) and
-// the minimum resident CTAs per SM requested from the register allocator.
+// Tuning of the attention CTA when one warp covers every query row of a KV head (S*G <= 8):
+// consumer token groups, shared-memory pipeline stages and the register cap per thread.
 #ifndef KVQ_TOKEN_GROUPS
 #define KVQ_TOKEN_GROUPS 4
 #endif
 #ifndef KVQ_STAGES_INT4
 #define KVQ_STAGES_INT4 8
 #endif
-#ifndef KVQ_MIN_CTAS
-#define KVQ_MIN_CTAS 2
+#ifndef KVQ_INT4_MAXREG
+#define KVQ_INT4_MAXREG 168
 #endif
 
 constexpr int kStage4 = 2 * kPage * kRec4 + 2 * kPage * 4;  // 8704 bytes: K codes, V codes, K meta, V meta
@@ -77,9 +76,6 @@ struct AttnParams {
   const void* v_new;
   int kv_bf16;
   float k_scale;
-  // int4: per-segment arrival counters (zeroed by the prologue kernel); the last CTA to finish
-  // a segment merges its partials and writes the output. Null: separate combine pass.
-  int* counters;
 };
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -95,7 +91,7 @@ struct SmemLayout {
     valid = empty + 8 * nstages;
     pre = valid + 4 * nstages;
     flags = pre + 4 * (B + 1);
-    red = align_up(flags + 32, 16);
+    red = align_up(flags + 16, 16);
     total = red + (size_t)nkg * rows_pad * kPartialStride * 4;
   }
 };
@@ -146,7 +142,6 @@ __device__ void build_prefix(const AttnParams& p, int fmt, int* pre, volatile in
     pre[p.B] = carry;
     flags[0] = 0;
     flags[1] = any_bad ? 1 : 0;
-    flags[3] = 0;
   }
 }
 
@@ -201,9 +196,10 @@ __device__ __forceinline__ int out_dim(int mt, int row) {
 // 64-slot blocks; one consumer warp and one stage per block, output written directly.
 constexpr int kFp8Groups = kFp8DirectBlocks;
 
+// Register caps: the int4 single-tile CTA (5 warps) must fit twice per SM, i.e. 3 warps per
+// SM sub-partition -> at most 170 registers; the window CTA has up to 11 warps (<= 186).
 template <int FMT, int NT>
-__global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_TOKEN_GROUPS) + 1) : 160,
-                                  (FMT == 0 && NT == 1) ? KVQ_MIN_CTAS : 1)
+__global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
     attn_kernel(const AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kStage = FMT == 0 ? kStage4 : kStage8;
@@ -720,10 +716,7 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_T
       }
     }
     named_barrier(1, nwc * 32);
-    // CTAs covering this segment (its pages are split over c_first..c_last)
-    const long long first_pg = (long long)p.Hkv * pre[b] + (long long)h * np;
-    const int c_first = (int)cta_of(first_pg, P, n_eff), c_last = (int)cta_of(first_pg + np - 1, P, n_eff);
-    if (p.direct || (p.counters != nullptr && c_first == c_last)) {
+    if (p.direct) {
       // whole segment in this CTA: merge the token groups and write the normalised output
       for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
         const int row = e / kD, d = e - row * kD;
@@ -759,54 +752,11 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * ((FMT == 1 ? kFp8Groups : KVQ_T
         }
         dstp[e] = v;
       }
-      if (p.counters != nullptr && threadIdx.x == 0) {
-        // a segment shared with other CTAs: merged after this CTA's last segment (see below)
-        const int k = flags[3]++;
-        flags[4 + 2 * k] = seg;
-        flags[5 + 2 * k] = (c_first << 16) | c_last;
-      }
     }
     named_barrier(1, nwc * 32);
     seg_start = seg_end;
   }
 
-  // Shared segments (at most this CTA's first and last): publish the partials, take a ticket;
-  // the CTA that arrives last for a segment merges every partial of it. Nothing waits.
-  if (p.counters != nullptr && flags[3] > 0) {
-    __threadfence();
-    named_barrier(1, nwc * 32);
-    if (threadIdx.x == 0)
-      for (int k = 0; k < flags[3]; ++k) {
-        const int c_first = flags[5 + 2 * k] >> 16, c_last = flags[5 + 2 * k] & 0xFFFF;
-        const bool last = atomicAdd(&p.counters[flags[4 + 2 * k]], 1) == c_last - c_first;
-        flags[5 + 2 * k] |= last ? (1 << 31) : 0;
-      }
-    named_barrier(1, nwc * 32);
-    for (int k = 0; k < flags[3]; ++k) {
-      const int word = flags[5 + 2 * k];
-      if (word >= 0) continue;  // not the last arrival
-      __threadfence();
-      const int seg = flags[4 + 2 * k];
-      const int c_first = (word >> 16) & 0x7FFF, c_last = word & 0xFFFF;
-      const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
-      for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
-        const int row = e / kD, d = e - row * kD;
-        float M = -INFINITY;
-        for (int c = c_first; c <= c_last; ++c)
-          M = fmaxf(M, __ldcg(p.partials + ((size_t)(c + seg) * R + row) * kPartialStride));
-        const float Mu = M == -INFINITY ? 0.0f : M;
-        float lsum = 0.0f, a = 0.0f;
-        for (int c = c_first; c <= c_last; ++c) {
-          const float* src = p.partials + ((size_t)(c + seg) * R + row) * kPartialStride;
-          const float w = fast_exp2(__ldcg(src) - Mu);
-          lsum += w * __ldcg(src + 1);
-          a += w * __ldcg(src + 2 + d);
-        }
-        const int r = row / G, gi = row - (row / G) * G;
-        p.out[(((size_t)b * p.S + r) * p.Hq + h * G + gi) * kD + d] = a / lsum;
-      }
-    }
-  }
 }
 
 // One block per (segment, query row): merges the segment's CTA partials and normalises.
@@ -880,7 +830,7 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   p.n_cta = (int)grid;
   attn_kernel<FMT, NT><<<(unsigned)grid, threads, smem, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess || p.direct || p.counters != nullptr) return e;
+  if (e != cudaSuccess || p.direct) return e;
   const size_t csmem = (p.B + 1 + 4) * sizeof(int);
   combine_kernel<FMT><<<(unsigned)(p.B * p.Hkv * p.R), 128, csmem, stream>>>(p);
   return cudaGetLastError();
@@ -889,8 +839,6 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
 }  // namespace
 
 size_t workspace_qrot_bytes(int B, int S, int Hq) { return align_up((size_t)B * S * Hq * kD * 4, 256); }
-
-size_t workspace_counters_bytes(int B, int Hkv) { return align_up((size_t)B * Hkv * 4, 256); }
 
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv) {
   const int G = Hq / Hkv;
@@ -916,7 +864,6 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p.max_pages = job.cache.max_pages_per_seq;
     p.num_pages = job.cache.num_pages;
     p.q_rot = job.q_rot;
-    p.counters = job.counters;
     p.score_scale = job.sm_scale * kLog2e;
     p_max = (long long)p.Hkv * p.B * p.max_pages;
   } else {

@@ -35,8 +35,6 @@ struct PrepJobs {
   int nq_rows;
   float* q_rot;      // workspace destination [nq_rows][128]
   float* q_rot_out;  // optional copy
-  int* zero_ints;    // workspace counters to clear (or null)
-  int n_zero;
   float eps;
   int32_t* dev_err;
 };
@@ -76,7 +74,6 @@ struct AttnJob {
   float sm_scale;
   float* out;
   float* partials;  // workspace
-  int* counters;    // int4: per-segment arrival counters, zeroed by the prologue kernel
   int32_t* dev_err;
 };
 
@@ -85,6 +82,5 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream);
 // Workspace layout shared by the API and the launchers.
 size_t workspace_qrot_bytes(int B, int S, int Hq);
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv);
-size_t workspace_counters_bytes(int B, int Hkv);
 
 }  // namespace kvq

@@ -114,8 +114,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* nbuf = smem_f + 128 * kMStride + warp * 128;
   const PrepJobs& j = p.j;
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < j.n_zero; i += kPrepThreads) j.zero_ints[i] = 0;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
   {
@@ -269,11 +267,10 @@ cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
   p.j = jobs;
   p.kv_jobs = jobs.k ? jobs.T * jobs.cache.num_kv_heads : 0;
   p.q_jobs = jobs.q ? jobs.nq_rows : 0;
-  if (p.kv_jobs == 0 && p.q_jobs == 0 && jobs.n_zero == 0) return cudaSuccess;
+  if (p.kv_jobs == 0 && p.q_jobs == 0) return cudaSuccess;
   const int cap = 2 * sm_count();
   p.kv_blocks = std::min((p.kv_jobs + kPrepWarps - 1) / kPrepWarps, cap);
-  int q_blocks = std::min((p.q_jobs + kPrepWarps - 1) / kPrepWarps, cap);
-  if (p.kv_blocks + q_blocks == 0) q_blocks = 1;  // counters to clear only
+  const int q_blocks = std::min((p.q_jobs + kPrepWarps - 1) / kPrepWarps, cap);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
