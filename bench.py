@@ -201,9 +201,9 @@ class Stack256k:
         return int((ctx + 1).sum()) * self.w.Hkv * 136
 
     def launches_per_step(self):
-        # int4 layer: prologue/append kernel + split-K attention (merge in the last CTA of a
-        # segment); window layer: one kernel (append, attention, merge)
-        return 2 * len(self.int4) + (self.nL - len(self.int4))
+        # int4 layer: prologue/append kernel, split-K attention kernel, combine kernel;
+        # window layer: one kernel (append, attention, in-CTA merge)
+        return 3 * len(self.int4) + (self.nL - len(self.int4))
 
 
 def run_64k(device, steps=30, warmup=3):
@@ -428,7 +428,7 @@ def run_kvq(args, rank, world, local):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(frac, 4), "traffic": None, "peak_kind": peak_kind,
                          "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
-                         "kernel": "kvq_decode_attn_int4 call (query prologue/append kernel + split-K attention kernel)",
+                         "kernel": "kvq_decode_attn_int4 call (query prologue/append + split-K attention + combine kernels)",
                          "bytes_per_call": int(np.mean(call_bytes)), "avg_call_us": round(1e3 * np.mean(call_ms), 2)},
             "at_64k": sec,
             "e2e": {"value": round(e2e_value, 2), "unit": "session-steps/s", "h2d_bytes_per_step": int(h2d),
