@@ -41,7 +41,8 @@ typedef enum kvq_status {
   KVQ_OK = 0,
   KVQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer, workspace too small */
   KVQ_ERR_UNSUPPORTED = 2, /* head_dim != 128, page_size != 64, S outside 1..8, too many rows */
-  KVQ_ERR_CUDA = 3         /* a CUDA runtime call or launch failed */
+  KVQ_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  KVQ_ERR_SCRATCH_TOO_SMALL = 4 /* kvq_decode_attn_int4_noalloc: request needs more than its fixed scratch */
 } kvq_status;
 
 typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
@@ -205,6 +206,32 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
                                    const void* v_new, float k_scale, float v_scale, float sm_scale, float* out,
                                    void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                    kvq_stream_t stream);
+
+/*
+ * kvq_decode_attn_int4_noalloc -- the same computation as kvq_decode_attn_int4 for callers
+ * that cannot allocate device memory at decode time (an engine that hands all free GPU
+ * memory to its KV pool at start-up, a thread that must not touch the device allocator, an
+ * environment where cudaMalloc or a framework allocator is unavailable). The paper has no
+ * counterpart: this is a packaging variant of the workspace handling only.
+ * The workspace comes from a fixed scratch array inside this library's device image, of
+ * KVQ_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds that much until the
+ * process exits. The call allocates nothing; the caller still passes every input and output.
+ *   - Arguments and results are those of kvq_decode_attn_int4 without (workspace,
+ *     workspace_bytes).
+ *   - Requests whose workspace (kvq_decode_workspace_bytes) exceeds the scratch return
+ *     KVQ_ERR_SCRATCH_TOO_SMALL and launch nothing.
+ *   - The first call on each device looks up the scratch's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls on a device share the one scratch array, which keeps the last call's
+ *     contents (no call needs it zeroed). Calls whose execution overlaps on the GPU race on
+ *     it: serialise them (one stream, or explicit ordering between streams and threads).
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+kvq_status kvq_decode_attn_int4_noalloc(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                        kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                        const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                        float* q_rot_out, int32_t* dev_err, kvq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -64,6 +64,9 @@ def _load():
                                        f32, vp, vp, sz, vp, vp, vp]
     L.kvq_fp8_append.restype = i32
     L.kvq_fp8_append.argtypes = [ctypes.POINTER(Fp8Ring), vp, vp, i32, i32, vp, vp, f32, f32, vp, vp]
+    L.kvq_decode_attn_int4_noalloc.restype = i32
+    L.kvq_decode_attn_int4_noalloc.argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
+                                               f32, f32, vp, vp, vp, vp]
     L.kvq_decode_attn_fp8_swa.restype = i32
     L.kvq_decode_attn_fp8_swa.argtypes = [ctypes.POINTER(Fp8Ring), vp, i32, i32, i32, i32, vp, i32, vp, vp, f32,
                                           f32, f32, vp, vp, sz, vp, vp]
@@ -191,6 +194,23 @@ def kvq_decode_attn_int4(cache: Int4Cache, Mq, Mk, q, ctx_len, out, workspace, d
            lib.kvq_decode_attn_int4(ctypes.byref(cache), _ptr(Mq), _ptr(Mk), _ptr(q), _dtype_code(q), B, S, Hq,
                                     _ptr(ctx_len), _ptr(k_new), _ptr(v_new), sm_scale, eps, _ptr(out),
                                     _ptr(workspace), ws_bytes, _ptr(q_rot_out), _ptr(dev_err), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+ERR_SCRATCH_TOO_SMALL = 4
+
+
+def kvq_decode_attn_int4_noalloc(cache: Int4Cache, Mq, Mk, q, ctx_len, out, dev_err, k_new=None, v_new=None,
+                                 sm_scale: float = HEAD_DIM ** -0.5, eps: float = 1e-6, q_rot_out=None, stream=None):
+    """kvq_decode_attn_int4 without a caller workspace: for callers that cannot allocate device
+    memory while decoding. Uses the library's fixed scratch (NOALLOC_SCRATCH_BYTES per device);
+    calls that overlap on the GPU race on it. The first call on a device must precede any
+    stream capture."""
+    B, S, Hq, _ = q.shape
+    _check("kvq_decode_attn_int4_noalloc",
+           lib.kvq_decode_attn_int4_noalloc(ctypes.byref(cache), _ptr(Mq), _ptr(Mk), _ptr(q), _dtype_code(q), B, S,
+                                            Hq, _ptr(ctx_len), _ptr(k_new), _ptr(v_new), sm_scale, eps, _ptr(out),
+                                            _ptr(q_rot_out), _ptr(dev_err), _stream(stream)))
 
 
 def kvq_fp8_append(ring: Fp8Ring, k, v, seq_ids, positions, k_scale: float, v_scale: float, dev_err, stream=None):

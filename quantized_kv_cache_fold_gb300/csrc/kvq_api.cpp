@@ -63,6 +63,8 @@ const char* kvq_status_string(kvq_status s) {
     case KVQ_ERR_INVALID_ARG: return "invalid argument";
     case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
     case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_SCRATCH_TOO_SMALL:
+      return "request exceeds the fixed scratch of kvq_decode_attn_int4_noalloc (KVQ_NOALLOC_SCRATCH_BYTES)";
   }
   return "unknown status";
 }
