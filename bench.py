@@ -62,6 +62,20 @@ def barrier(world):
         dist.barrier()
 
 
+def aggregate(ms_local, units_local, world, device="cpu"):
+    """Whole-job figure of a weak-scaling run: the slowest rank's time and the units all ranks
+    processed divided by it. Returns (ms_max, units_per_second)."""
+    ms = max_over_ranks(ms_local, world, device)
+    units = units_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(units_local)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        units = float(t.item())
+    return ms, units / (ms * 1e-3)
+
+
 def max_over_ranks(x, world, device="cpu"):
     if world == 1:
         return x
@@ -350,9 +364,7 @@ def run_kvq(args, rank, world, local):
     ms_local = start.elapsed_time(end)
     err = bench.st.read_error()
     assert err == 0, f"device error word {err:#x}"
-    ms = max_over_ranks(ms_local, world, device)
-    t = ms * 1e-3
-    value = world * bench.w.B * K / t
+    ms, value = aggregate(ms_local, bench.w.B * K, world, device)
     call_bytes = [bench.int4_call_bytes(W + j // n_int4) for j in range(n_int4 * K)]
     if evs is not None:
         call_ms = [evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(n_int4 * K)]
@@ -404,8 +416,7 @@ def run_kvq(args, rank, world, local):
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
-    te = max_over_ranks(e0.elapsed_time(e1), world, device) * 1e-3
-    e2e_value = world * bench.w.B * Ke / te
+    _, e2e_value = aggregate(e0.elapsed_time(e1), bench.w.B * Ke, world, device)
     assert bench.st.read_error() == 0
     del g2
     launches_per_step = bench.launches_per_step()
