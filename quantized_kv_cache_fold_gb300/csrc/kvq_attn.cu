@@ -39,6 +39,10 @@ namespace {
 #ifndef KVQ_STAGES_INT4
 #define KVQ_STAGES_INT4 8
 #endif
+// K codes enter QK^T as 1024+c (no per-element bias subtraction); see unpack8_biased.
+#ifndef KVQ_K_BIASED
+#define KVQ_K_BIASED 1
+#endif
 #ifndef KVQ_INT4_MAXREG
 #define KVQ_INT4_MAXREG 168
 #endif
@@ -364,6 +368,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
     // ---- segment setup: query fragments and per-row limits
     uint32_t qf[NT][8][2];
     float qs[NT][2];
+    float negbias[NT][2];  // biased K path: -1024 * sum of the row's query fragment values
     int lim_lo[NT][2], lim_hi[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -404,15 +409,27 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
       for (int i = 0; i < 32; ++i) part += qv[i];
       if (FMT == 0) {
-        // k-step 2wi+e, slots (2t,2t+1) <- dims (8wi+2e, +4), slots (2t+8,2t+9) <- (+1, +5)
+        // k-step 2wi+e, slots (2t,2t+1) <- dims (8wi+2e, +4), slots (2t+8,2t+9) <- (+1, +5);
+        // the second pair meets high nibbles, read as 16*code in the biased K path, so its
+        // query values are divided by 16 (exact).
+        const float hs = KVQ_K_BIASED ? 0.0625f : 1.0f;
+        float bsum = 0.0f;
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int d0 = 8 * wi + 2 * e;
-            qf[nt][2 * wi + e][0] = pack_f16x2(qv[d0], qv[d0 + 4]);
-            qf[nt][2 * wi + e][1] = pack_f16x2(qv[d0 + 1], qv[d0 + 5]);
+            const uint32_t b0 = pack_f16x2(qv[d0], qv[d0 + 4]);
+            const uint32_t b1 = pack_f16x2(qv[d0 + 1] * hs, qv[d0 + 5] * hs);
+            qf[nt][2 * wi + e][0] = b0;
+            qf[nt][2 * wi + e][1] = b1;
+            bsum += (h2f_lo(b0) + h2f_hi(b0)) + (h2f_lo(b1) + h2f_hi(b1));
           }
+        bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+        bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          negbias[nt][j] = KVQ_K_BIASED ? -1024.0f * __shfl_sync(0xffffffffu, bsum, (2 * t + j) * 4) : 0.0f;
       } else {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -485,7 +502,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
                 const uint32_t mk = Km[tok], mv = Vm[tok];
                 const float sk = h2f_lo(mk), ok_ = h2f_hi(mk), sv = h2f_lo(mv), ovv = h2f_hi(mv);
                 ka[u][hh] = sk * p.score_scale;
-                kb[u][hh] = fmaf(8.0f, sk, ok_);
+                kb[u][hh] = KVQ_K_BIASED ? ok_ : fmaf(8.0f, sk, ok_);
                 va[u][hh] = sv;
                 vb[u][hh] = fmaf(8.0f, sv, ovv);
               }
@@ -517,14 +534,19 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
               for (int u = 0; u < MTU; ++u)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) d[nt][u][c] = 0.0f;
+                for (int c = 0; c < 4; ++c) d[nt][u][c] = negbias[nt][c & 1];
 #pragma unroll
             for (int wi = 0; wi < 4; ++wi) {
               uint32_t ha[MTU][4], hb[MTU][4];
 #pragma unroll
               for (int u = 0; u < MTU; ++u) {
-                unpack8_centred(A[u][wi], ha[u]);
-                unpack8_centred(Bw[u][wi], hb[u]);
+                if (KVQ_K_BIASED) {
+                  unpack8_biased(A[u][wi], ha[u]);
+                  unpack8_biased(Bw[u][wi], hb[u]);
+                } else {
+                  unpack8_centred(A[u][wi], ha[u]);
+                  unpack8_centred(Bw[u][wi], hb[u]);
+                }
               }
 #pragma unroll
               for (int e = 0; e < 2; ++e)

@@ -165,6 +165,20 @@ __device__ __forceinline__ void unpack8_centred(uint32_t x, uint32_t (&h)[4]) {
   h[3] = hfma2_u(lop3<0xEA>(x8, 0x00F000F0u, kMagic), kSixteenth, kNeg72);
 }
 
+// Eight 4-bit codes -> four f16x2 without the bias subtraction (one lop3 each):
+// h[0] = (1024+n0, 1024+n4), h[1] = (1024+16 n1, 1024+16 n5), h[2] = (1024+n2, 1024+n6),
+// h[3] = (1024+16 n3, 1024+16 n7). Used for K against query fragments whose high-nibble slots
+// are pre-divided by 16 and an accumulator started at -1024 * (sum of the query fragment), so
+// the 1024 bias cancels inside the fp32 accumulation.
+__device__ __forceinline__ void unpack8_biased(uint32_t x, uint32_t (&h)[4]) {
+  constexpr uint32_t kMagic = 0x64006400u;
+  const uint32_t x8 = x >> 8;
+  h[0] = lop3<0xEA>(x, 0x000F000Fu, kMagic);
+  h[1] = lop3<0xEA>(x, 0x00F000F0u, kMagic);
+  h[2] = lop3<0xEA>(x8, 0x000F000Fu, kMagic);
+  h[3] = lop3<0xEA>(x8, 0x00F000F0u, kMagic);
+}
+
 // Two e4m3 bytes (low byte first) -> f16x2 (exact: e4m3 is a subset of f16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t d;
