@@ -126,6 +126,15 @@ __device__ __forceinline__ int seg_pages(const AttnParams& p, int ctxb, int fmt)
 __device__ void build_prefix(const AttnParams& p, int fmt, int* pre, volatile int* flags) {
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
+  if (fmt == 1) {  // every window segment spans the whole ring: no context lengths needed
+    const int nblk = p.cap / kPage;
+    for (int b = lane; b <= p.B; b += 32) pre[b] = b * nblk;
+    if (lane == 0) {
+      flags[0] = 0;
+      flags[1] = 0;
+    }
+    return;
+  }
   int carry = 0;
   bool bad = false;
   for (int base = 0; base < p.B; base += 32) {
@@ -224,7 +233,8 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   build_prefix(p, FMT, pre, flags);
   if (threadIdx.x < nst) {
     mbar_init(&full[threadIdx.x], 1);
-    mbar_init(&empty[threadIdx.x], p.ntg);
+    // in the one-CTA window mode `empty` serves as the landing barrier of each block's copy
+    mbar_init(&empty[threadIdx.x], (FMT == 1 && p.direct) ? 1 : p.ntg);
   }
   fence_barrier_init();
   __syncthreads();
@@ -241,51 +251,67 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   // loads in parallel); lane 0 then issues one bulk copy per page, in order, as stages free.
   if (warp == nwc) {
     if (FMT == 1 && p.direct) {
-      // Whole ring of one (sequence, KV head); one stage per block. Blocks without a new row
-      // are requested first; the new rows are then written into the ring, ordered before the
-      // bulk copies that read them back (proxy fence), and their blocks requested last.
+      // Whole ring of one (sequence, KV head) per CTA, one stage per block. Every block's copy
+      // is issued at once. When rows are appended, the copies land on `empty` (landing
+      // barrier); meanwhile the warp converts the new rows, writes them to the ring for later
+      // steps, and once a block has landed patches its new rows into the stage before
+      // releasing it to its consumer on `full`.
       const uint64_t pol = policy_evict_first();
-      int b, h, lp, np;
-      decode_page(pre, p.B, p.Hkv, p0, b, h, lp, np);
-      bool dummy = false;
-      const int c0 = eff_ctx(p, b, dummy, FMT);
+      const int seg = (int)blockIdx.x;
+      const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
       const int nblk = p.cap / kPage;
-      uint32_t newmask = 0;
-      if (p.k_new != nullptr)
-        for (int r = 0; r < p.S; ++r) newmask |= 1u << (((c0 + r) % p.cap) / kPage);
-      const uint8_t* seg_base = p.blocks + ((size_t)b * p.Hkv + h) * nblk * (size_t)kStage8;
+      uint8_t* seg_base = const_cast<uint8_t*>(p.blocks) + (size_t)seg * nblk * kStage8;
+      const bool patch = p.k_new != nullptr;
+      uint64_t* land = patch ? empty : full;
       if (lane == 0) {
         for (int j = 0; j < nblk; ++j) {
-          if (newmask >> j & 1u) continue;
           valid[j] = 1;
-          mbar_arrive_expect_tx(&full[j], kStage8);
-          bulk_g2s(stages + (size_t)j * kStage, seg_base + (size_t)j * kStage8, kStage8, &full[j], pol);
+          mbar_arrive_expect_tx(&land[j], kStage8);
+          bulk_g2s(stages + (size_t)j * kStage, seg_base + (size_t)j * kStage8, kStage8, &land[j], pol);
         }
       }
-      if (newmask) {
-        for (int r = 0; r < p.S; ++r) {
+      if (patch) {
+        bool bad = false;
+        const int c0 = eff_ctx(p, b, bad, FMT);
+        if (bad && lane == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
+        uint32_t code[8][2];
+        uint32_t ok = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r >= p.S) break;
           const int slot = (c0 + r) % p.cap;
-          uint8_t* blk = const_cast<uint8_t*>(seg_base) + (size_t)(slot / kPage) * kStage8;
           const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
+#pragma unroll
           for (int which = 0; which < 2; ++which) {
             float x[4];
             load_row4(which ? p.v_new : p.k_new, p.kv_bf16, row, lane, x);
+            code[r][which] = 0;
             if (!warp_all_finite(x)) {
               if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
               continue;
             }
-            fp8_store_row(blk + which * kPage * kRec8, slot, x, which ? p.v_scale : p.k_scale, lane);
+            code[r][which] = fp8_encode4(x, which ? p.v_scale : p.k_scale);
+            ok |= 1u << (2 * r + which);
+            *reinterpret_cast<uint32_t*>(seg_base + (size_t)(slot / kPage) * kStage8 + which * kPage * kRec8 +
+                                         fp8_lane_offset(slot, lane)) = code[r][which];
           }
         }
-        fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) {
-          for (int j = 0; j < nblk; ++j) {
-            if (!(newmask >> j & 1u)) continue;
-            valid[j] = 1;
-            mbar_arrive_expect_tx(&full[j], kStage8);
-            bulk_g2s(stages + (size_t)j * kStage, seg_base + (size_t)j * kStage8, kStage8, &full[j], pol);
+        for (int j = 0; j < nblk; ++j) {
+          if (lane == 0 && !mbar_wait_bounded(&land[j], 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+          __syncwarp();
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r >= p.S) break;
+            const int slot = (c0 + r) % p.cap;
+            if (slot / kPage != j) continue;
+#pragma unroll
+            for (int which = 0; which < 2; ++which)
+              if (ok >> (2 * r + which) & 1u)
+                *reinterpret_cast<uint32_t*>(stages + (size_t)j * kStage + which * kPage * kRec8 +
+                                             fp8_lane_offset(slot, lane)) = code[r][which];
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[j]);
         }
       }
       if (lane == 0)
@@ -362,8 +388,9 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
     decode_page(pre, p.B, p.Hkv, seg_start, b, h, lp0, np);
     const long long seg_end = min(p1, seg_start + (np - lp0));
     const int seg = b * p.Hkv + h;
-    bool dummy = false;
-    const int ctxb = eff_ctx(p, b, dummy, FMT);
+    bool bad_ctx = false;
+    const int ctxb = eff_ctx(p, b, bad_ctx, FMT);
+    if (FMT == 1 && bad_ctx && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
 
     // ---- segment setup: query fragments and per-row limits
     uint32_t qf[NT][8][2];
@@ -711,7 +738,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0 && !(FMT == 1 && p.direct)) mbar_arrive(&empty[s]);
     }
 
     // ---- segment end: reduce this warp's partial, merge token groups, write the CTA partial

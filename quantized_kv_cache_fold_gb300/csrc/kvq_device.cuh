@@ -218,15 +218,23 @@ __device__ __forceinline__ void set_err(int32_t* dev_err, int bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }
 
-// One 128-element row (lane l holds x[4l..4l+3]) as e4m3(x / scale): IEEE division, nearest
-// even, saturating; stored into the record of `slot` of a 64-slot ring block half (K or V),
-// with the record's 16-byte chunks in XOR order (chunk c at c ^ (slot & 7)).
-__device__ __forceinline__ void fp8_store_row(uint8_t* block_half, int slot, const float (&x)[4], float scale,
-                                              int lane) {
+// FP8 cache write (stock format): lane l's four elements of a 128-element row as e4m3(x /
+// scale) -- IEEE division, nearest even, saturating -- packed low element first.
+__device__ __forceinline__ uint32_t fp8_encode4(const float (&x)[4], float scale) {
   const uint32_t lo = pack_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
   const uint32_t hi = pack_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
-  const int off = (slot % kPage) * kRec8 + ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
-  *reinterpret_cast<uint32_t*>(block_half + off) = lo | (hi << 16);
+  return lo | (hi << 16);
+}
+
+// Byte offset of lane l's four codes of the record in `slot` within a 64-slot ring block
+// half (K or V): the record's 16-byte chunks are stored in XOR order (chunk c at c ^ (slot & 7)).
+__device__ __forceinline__ int fp8_lane_offset(int slot, int lane) {
+  return (slot % kPage) * kRec8 + ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
+}
+
+__device__ __forceinline__ void fp8_store_row(uint8_t* block_half, int slot, const float (&x)[4], float scale,
+                                              int lane) {
+  *reinterpret_cast<uint32_t*>(block_half + fp8_lane_offset(slot, lane)) = fp8_encode4(x, scale);
 }
 
 // Lane l's four elements of row `row` of a [rows][128] tensor of fp32 or bf16.
