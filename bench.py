@@ -324,7 +324,9 @@ def run_kvq(args, rank, world, local):
     peak, peak_kind = measured_peak()
 
     # ---- device-resident timed region: the K steps are captured once into a CUDA graph (as a
-    # serving engine would) and replayed; event-record nodes bracket every int4 layer call.
+    # serving engine would) and replayed. Event-record nodes bracket the int4 layer calls of
+    # every 64th step and of the last one: each such node drains the GPU's work queue (several
+    # microseconds), so bracketing every call would slow the very steps being timed.
     for t in range(W):
         bench.step(t)
     torch.cuda.synchronize()
@@ -336,7 +338,8 @@ def run_kvq(args, rank, world, local):
         except TypeError:
             return None
 
-    evs = [timing_event() for _ in range(2 * n_int4 * K)]
+    sampled = [i for i in range(K) if i % 64 == 63 or i == K - 1]
+    evs = [timing_event() for _ in range(2 * n_int4 * len(sampled))]
     if any(e is None for e in evs):
         evs = None
     cap = torch.cuda.Stream()
@@ -345,7 +348,8 @@ def run_kvq(args, rank, world, local):
     with torch.cuda.stream(cap):
         with torch.cuda.graph(graph, stream=cap):
             for i in range(K):
-                bench.step(W + i, None if evs is None else evs[2 * n_int4 * i: 2 * n_int4 * (i + 1)])
+                si = sampled.index(i) if (evs is not None and i in sampled) else -1
+                bench.step(W + i, None if si < 0 else evs[2 * n_int4 * si: 2 * n_int4 * (si + 1)])
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -365,9 +369,9 @@ def run_kvq(args, rank, world, local):
     err = bench.st.read_error()
     assert err == 0, f"device error word {err:#x}"
     ms, value = aggregate(ms_local, bench.w.B * K, world, device)
-    call_bytes = [bench.int4_call_bytes(W + j // n_int4) for j in range(n_int4 * K)]
+    call_bytes = [bench.int4_call_bytes(W + sampled[j // n_int4]) for j in range(n_int4 * len(sampled))]
     if evs is not None:
-        call_ms = [evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(n_int4 * K)]
+        call_ms = [evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(n_int4 * len(sampled))]
     else:  # no event nodes in graphs on this torch: time the same calls eagerly right after
         call_ms = []
         for j in range(min(n_int4 * K, 100)):
@@ -447,7 +451,9 @@ def run_kvq(args, rank, world, local):
                     "how": "per step: q, k_new, v_new of all 50 layers copied from pinned host memory, the step, "
                            "all outputs copied back to pinned host memory; captured in one CUDA graph"},
             "timing": "K steps captured in one CUDA graph and replayed; CUDA events on the replay stream; "
-                      "int4 call durations from event-record nodes inside the graph",
+                      "int4 call durations from event-record nodes inside the graph around the int4 calls of "
+                      "every 64th timed step and the last one",
+            "int4_calls_timed": len(call_ms),
             "cpu_baseline": {k: v for k, v in cpu.items() if k != "seconds_per_session_step"},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,

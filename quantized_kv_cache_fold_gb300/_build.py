@@ -13,7 +13,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
-SOURCES = ["kvq_attn.cu", "kvq_prep.cu", "kvq_api.cpp", "kvq_noalloc.cu"]
+SOURCES = ["kvq_attn.cu", "kvq_swa.cu", "kvq_prep.cu", "kvq_api.cpp", "kvq_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
          "-I", CSRC]

@@ -235,11 +235,10 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
   if (workspace_bytes < kvq_decode_workspace_bytes(B, S, num_q_heads, ring->num_kv_heads))
     return KVQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  // The attention kernel appends the new rows itself when one CTA owns each (sequence, KV
-  // head); beyond that many segments the rows are appended by a separate launch first.
-  const bool fused_append =
-      (long long)B * ring->num_kv_heads <= kvq::kMaxCtas && ring->capacity / KVQ_PAGE_SIZE <= kvq::kFp8DirectBlocks;
-  if (k_new && !fused_append) {
+  // Rings that one cluster per (sequence, KV head) covers: one launch that appends the new
+  // rows and attends. Larger rings: a separate append, then the split-K path and its combine.
+  const bool cluster = kvq::swa_cluster_path(ring->capacity, S, num_q_heads, ring->num_kv_heads);
+  if (k_new && !cluster) {
     kvq::Fp8AppendJob j{};
     j.ring = *ring;
     j.k = k_new;
@@ -267,13 +266,13 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
   a.ctx = pos0;
   a.q = q;
   a.q_bf16 = dtype == KVQ_BF16;
-  a.k_new = fused_append ? k_new : nullptr;
-  a.v_new = fused_append ? v_new : nullptr;
+  a.k_new = cluster ? k_new : nullptr;
+  a.v_new = cluster ? v_new : nullptr;
   a.sm_scale = sm_scale;
   a.out = out;
   a.partials = reinterpret_cast<float*>(ws + kvq::workspace_qrot_bytes(B, S, num_q_heads));
   a.dev_err = dev_err;
-  return from_cuda(kvq::launch_attention(a, s));
+  return from_cuda(cluster ? kvq::launch_swa_cluster(a, s) : kvq::launch_attention(a, s));
 }
 
 }  // extern "C"

@@ -1,8 +1,9 @@
 // Split-K flash-decoding attention over the rotated int4 cache and the FP8 ring.
 //
 // "Serving Kolibri-1 with a 4-bit KV cache", section "What we do": decode reads the 4-bit
-// codes directly and nothing is rotated back. The sliding-window layers read their stock
-// FP8 cache through the same kernel (FMT = 1).
+// codes directly and nothing is rotated back. Sliding-window layers whose FP8 ring is too
+// large for one thread-block cluster per (sequence, KV head) (kvq_swa.cu) read it through
+// the same kernel (FMT = 1).
 //
 // Work split (stream-K over pages): every (sequence b, KV head h) is a segment of np_b
 // pages; the segments are laid end to end and each CTA takes an equal contiguous range of
@@ -73,13 +74,6 @@ struct AttnParams {
   int32_t* dev_err;
   int ntg, nkg, nstages, rows_pad;
   int n_cta;
-  // direct: every CTA covers whole segments and writes the normalised output itself
-  int direct;
-  // fp8 only: rows to append before attending ([B][S][Hkv][128] or null), their dtype and scale
-  const void* k_new;
-  const void* v_new;
-  int kv_bf16;
-  float k_scale;
 };
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -179,20 +173,6 @@ __device__ __forceinline__ void decode_page(const int* pre, int B, int Hkv, long
 // CTA whose page range [floor(i P / n), floor((i+1) P / n)) contains page pg (n <= P).
 __device__ __forceinline__ long long cta_of(long long pg, long long P, int n) { return ((pg + 1) * n - 1) / P; }
 
-__device__ __forceinline__ float warp_sum_g(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 4);
-  v += __shfl_xor_sync(0xffffffffu, v, 8);
-  v += __shfl_xor_sync(0xffffffffu, v, 16);
-  return v;
-}
-
-__device__ __forceinline__ float warp_max_g(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-  return v;
-}
-
 __device__ __forceinline__ float h2f_lo(uint32_t x) {
   return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu)));
 }
@@ -205,12 +185,8 @@ __device__ __forceinline__ int out_dim(int mt, int row) {
   return 16 * mt + 2 * (row & 7) + (row >> 3);
 }
 
-// FP8 window layers: one CTA per (sequence, KV head) when the ring has at most kFp8Groups
-// 64-slot blocks; one consumer warp and one stage per block, output written directly.
-constexpr int kFp8Groups = kFp8DirectBlocks;
-
 // Register caps: the int4 single-tile CTA (5 warps) must fit twice per SM, i.e. 3 warps per
-// SM sub-partition -> at most 170 registers; the window CTA has up to 11 warps (<= 186).
+// SM sub-partition -> at most 170 registers.
 template <int FMT, int NT>
 __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
     attn_kernel(const AttnParams p) {
@@ -233,8 +209,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   build_prefix(p, FMT, pre, flags);
   if (threadIdx.x < nst) {
     mbar_init(&full[threadIdx.x], 1);
-    // in the one-CTA window mode `empty` serves as the landing barrier of each block's copy
-    mbar_init(&empty[threadIdx.x], (FMT == 1 && p.direct) ? 1 : p.ntg);
+    mbar_init(&empty[threadIdx.x], p.ntg);
   }
   fence_barrier_init();
   __syncthreads();
@@ -250,75 +225,6 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   // The 32 lanes resolve the source blocks of 32 consecutive pages at once (block-table
   // loads in parallel); lane 0 then issues one bulk copy per page, in order, as stages free.
   if (warp == nwc) {
-    if (FMT == 1 && p.direct) {
-      // Whole ring of one (sequence, KV head) per CTA, one stage per block. Every block's copy
-      // is issued at once. When rows are appended, the copies land on `empty` (landing
-      // barrier); meanwhile the warp converts the new rows, writes them to the ring for later
-      // steps, and once a block has landed patches its new rows into the stage before
-      // releasing it to its consumer on `full`.
-      const uint64_t pol = policy_evict_first();
-      const int seg = (int)blockIdx.x;
-      const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
-      const int nblk = p.cap / kPage;
-      uint8_t* seg_base = const_cast<uint8_t*>(p.blocks) + (size_t)seg * nblk * kStage8;
-      const bool patch = p.k_new != nullptr;
-      uint64_t* land = patch ? empty : full;
-      if (lane == 0) {
-        for (int j = 0; j < nblk; ++j) {
-          valid[j] = 1;
-          mbar_arrive_expect_tx(&land[j], kStage8);
-          bulk_g2s(stages + (size_t)j * kStage, seg_base + (size_t)j * kStage8, kStage8, &land[j], pol);
-        }
-      }
-      if (patch) {
-        bool bad = false;
-        const int c0 = eff_ctx(p, b, bad, FMT);
-        if (bad && lane == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
-        uint32_t code[8][2];
-        uint32_t ok = 0;
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          if (r >= p.S) break;
-          const int slot = (c0 + r) % p.cap;
-          const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            float x[4];
-            load_row4(which ? p.v_new : p.k_new, p.kv_bf16, row, lane, x);
-            code[r][which] = 0;
-            if (!warp_all_finite(x)) {
-              if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
-              continue;
-            }
-            code[r][which] = fp8_encode4(x, which ? p.v_scale : p.k_scale);
-            ok |= 1u << (2 * r + which);
-            *reinterpret_cast<uint32_t*>(seg_base + (size_t)(slot / kPage) * kStage8 + which * kPage * kRec8 +
-                                         fp8_lane_offset(slot, lane)) = code[r][which];
-          }
-        }
-        for (int j = 0; j < nblk; ++j) {
-          if (lane == 0 && !mbar_wait_bounded(&land[j], 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-          __syncwarp();
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            if (r >= p.S) break;
-            const int slot = (c0 + r) % p.cap;
-            if (slot / kPage != j) continue;
-#pragma unroll
-            for (int which = 0; which < 2; ++which)
-              if (ok >> (2 * r + which) & 1u)
-                *reinterpret_cast<uint32_t*>(stages + (size_t)j * kStage + which * kPage * kRec8 +
-                                             fp8_lane_offset(slot, lane)) = code[r][which];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[j]);
-        }
-      }
-      if (lane == 0)
-        for (int j = 0; j < nblk; ++j)
-          if (!mbar_wait_bounded(&full[j], 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-      return;
-    }
     const uint64_t pol = policy_evict_first();
     const int npages = (int)(p1 - p0);
     int issued = 0;
@@ -738,7 +644,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
         }
       }
       __syncwarp();
-      if (lane == 0 && !(FMT == 1 && p.direct)) mbar_arrive(&empty[s]);
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
 
     // ---- segment end: reduce this warp's partial, merge token groups, write the CTA partial
@@ -765,42 +671,23 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
       }
     }
     named_barrier(1, nwc * 32);
-    if (p.direct) {
-      // whole segment in this CTA: merge the token groups and write the normalised output
-      for (int e = threadIdx.x; e < R * kD; e += nwc * 32) {
-        const int row = e / kD, d = e - row * kD;
-        float M = -INFINITY;
-        for (int kk = 0; kk < p.nkg; ++kk) M = fmaxf(M, red[((size_t)kk * p.rows_pad + row) * kPartialStride]);
+    float* dstp = p.partials + ((size_t)(blockIdx.x + seg) * R) * kPartialStride;
+    for (int e = threadIdx.x; e < R * kPartialStride; e += nwc * 32) {
+      const int row = e / kPartialStride, c = e - row * kPartialStride;
+      float M = -INFINITY;
+      for (int kk = 0; kk < p.nkg; ++kk) M = fmaxf(M, red[((size_t)kk * p.rows_pad + row) * kPartialStride]);
+      float v;
+      if (c == 0) {
+        v = M;
+      } else {
         const float Mu = M == -INFINITY ? 0.0f : M;
-        float lsum = 0.0f, a = 0.0f;
+        v = 0.0f;
         for (int kk = 0; kk < p.nkg; ++kk) {
           const float* src = red + ((size_t)kk * p.rows_pad + row) * kPartialStride;
-          const float w = fast_exp2(src[0] - Mu);
-          lsum += w * src[1];
-          a += w * src[2 + d];
+          v += fast_exp2(src[0] - Mu) * src[c];
         }
-        const int r = row / G, gi = row - (row / G) * G;
-        p.out[(((size_t)b * p.S + r) * p.Hq + h * G + gi) * kD + d] = a / lsum;
       }
-    } else {
-      float* dstp = p.partials + ((size_t)(blockIdx.x + seg) * R) * kPartialStride;
-      for (int e = threadIdx.x; e < R * kPartialStride; e += nwc * 32) {
-        const int row = e / kPartialStride, c = e - row * kPartialStride;
-        float M = -INFINITY;
-        for (int kk = 0; kk < p.nkg; ++kk) M = fmaxf(M, red[((size_t)kk * p.rows_pad + row) * kPartialStride]);
-        float v;
-        if (c == 0) {
-          v = M;
-        } else {
-          const float Mu = M == -INFINITY ? 0.0f : M;
-          v = 0.0f;
-          for (int kk = 0; kk < p.nkg; ++kk) {
-            const float* src = red + ((size_t)kk * p.rows_pad + row) * kPartialStride;
-            v += fast_exp2(src[0] - Mu) * src[c];
-          }
-        }
-        dstp[e] = v;
-      }
+      dstp[e] = v;
     }
     named_barrier(1, nwc * 32);
     seg_start = seg_end;
@@ -875,11 +762,10 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   const int occ = dc.occ[FMT][NT];
   long long grid = std::min<long long>((long long)dc.sm * occ, kMaxCtas);
   grid = std::max<long long>(1, std::min(grid, p_max));
-  if (p.direct) grid = std::min<long long>((long long)p.B * p.Hkv, kMaxCtas);
   p.n_cta = (int)grid;
   attn_kernel<FMT, NT><<<(unsigned)grid, threads, smem, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess || p.direct) return e;
+  if (e != cudaSuccess) return e;
   const size_t csmem = (p.B + 1 + 4) * sizeof(int);
   combine_kernel<FMT><<<(unsigned)(p.B * p.Hkv * p.R), 128, csmem, stream>>>(p);
   return cudaGetLastError();
@@ -938,23 +824,9 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p.nkg = 2;
     p.nstages = 4;
   }
-  if (job.fmt == 1) {
-    // window layers: when the ring has at most kFp8Groups blocks, one CTA per (sequence, KV head)
-    // with one stage (and, for one query tile, one consumer warp) per block, output written
-    // directly; otherwise the general split with a combine pass
-    const int nblk = p.cap / kPage;
-    p.direct = ((long long)p.B * p.Hkv <= kMaxCtas && nblk <= kFp8Groups) ? 1 : 0;
-    if (p.direct) {
-      p.nkg = NT == 1 ? nblk : std::min(2, nblk);
-      p.nstages = nblk;
-    } else {
-      p.nkg = NT == 1 ? 4 : 2;
-      p.nstages = 4;
-    }
-    p.k_new = job.k_new;
-    p.v_new = job.v_new;
-    p.kv_bf16 = job.q_bf16;
-    p.k_scale = job.k_scale;
+  if (job.fmt == 1) {  // window rings too large for one cluster per (sequence, KV head)
+    p.nkg = NT == 1 ? 4 : 2;
+    p.nstages = 4;
   }
   p.rows_pad = p.ntg * NT * 8;
   const int threads = (p.ntg * p.nkg + 1) * 32;

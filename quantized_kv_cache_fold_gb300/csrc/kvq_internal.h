@@ -13,7 +13,6 @@ namespace kvq {
 constexpr int kMaxCtas = 1024;       // cap on attention CTAs (sizes the partial-result workspace)
 constexpr int kMaxRows = 48;         // S * (num_q_heads / num_kv_heads) rows per KV head and sequence
 constexpr int kPartialStride = 130;  // floats per partial row: m, l, acc[128]
-constexpr int kFp8DirectBlocks = 10; // window rings up to this many 64-slot blocks take the one-CTA path
 
 // Job description for the prologue/quantise kernel.
 struct PrepJobs {
@@ -69,7 +68,7 @@ struct AttnJob {
   const float* q_rot;  // int4: rotated queries [B][S][Hq][128] fp32 (workspace)
   const void* q;       // fp8: queries as given
   int q_bf16;
-  const void* k_new;   // fp8: rows appended inside the attention kernel (null: none)
+  const void* k_new;   // fp8 cluster path: rows appended inside the attention kernel (null: none)
   const void* v_new;
   float sm_scale;
   float* out;
@@ -78,6 +77,13 @@ struct AttnJob {
 };
 
 cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream);
+
+// FP8 window attention with one thread-block cluster per (sequence, KV head), appending
+// job.k_new / job.v_new itself. swa_cluster_path() says whether a ring of this capacity and
+// these head counts takes it; larger rings go through launch_attention (fmt 1) after a
+// separate append.
+bool swa_cluster_path(int capacity, int S, int Hq, int Hkv);
+cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream);
 
 // Workspace layout shared by the API and the launchers.
 size_t workspace_qrot_bytes(int B, int S, int Hq);

@@ -1,0 +1,590 @@
+// FP8 sliding-window decode attention: one thread-block cluster per (sequence, KV head).
+//
+// "Serving Kolibri-1 with a 4-bit KV cache", section on the sliding-window layers: those
+// layers keep the stock FP8 (e4m3) cache and attend over the newest `window` positions. The
+// cache is a ring of `cap` slots per (sequence, KV head), position p in slot p mod cap, stored
+// as 64-slot blocks of 16384 bytes (64 K records of 128 e4m3 codes, then 64 V records; the
+// 16-byte chunks of slot s's record in XOR order, chunk c at c ^ (s & 7)).
+//
+// A window is a few hundred positions, so one (sequence, KV head) is far too little work to
+// split across a whole grid and merge through global memory, and far too much latency for a
+// single SM to pull alone (one SM ingests a 576-slot ring at ~30 GB/s). Here the ring is
+// spread over the CTAs of one cluster (at most 8), their warps reading disjoint blocks, and
+// the partial softmax states are merged through distributed shared memory:
+//
+//   warp (block stream w, tile group tg): streams the blocks j = w, w + NS, w + 2 NS, ...
+//     (NS = streams in the cluster) through its own one- or two-stage shared-memory buffer,
+//     each block one bulk copy (TMA engine) completing on the warp's own mbarrier;
+//     if the call appends rows, the stream owning a new row's block encodes it (e4m3 of
+//     x / scale), stores it into the ring for later steps (tile group 0 only) and patches
+//     it into the landed copy, so the appended rows are attended in the same launch;
+//     QK^T and PV on tensor cores (mma.m16n8k16, e4m3 -> f16 exactly), online softmax in
+//     exp2 form, query rows masked outside [max(0, p_r - window + 1), p_r];
+//   partial (m, l, acc[128]) of every stream and query row -> the warp's own stage buffer;
+//   each CTA merges its streams' partials per (row, 4 dims) with log-sum-exp weights and
+//   pushes the result into CTA 0 of the cluster with asynchronous remote stores (st.async)
+//   that complete a byte count on CTA 0's receive mbarrier, then exits; CTA 0 waits for
+//   all bytes, merges the cluster's partials from its own shared memory and writes the
+//   normalised output.
+//
+// Every mbarrier wait is bounded (KVQ_DEVERR_TIMEOUT). The one cluster barrier (arrive at
+// start, wait before the first remote store) only publishes CTA 0's receive barrier, and
+// every thread reaches both halves unconditionally.
+
+#include <algorithm>
+#include <cmath>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+// Block streams (warps per query-tile group) per CTA.
+#ifndef KVQ_SWA_STREAMS
+#define KVQ_SWA_STREAMS 4
+#endif
+
+constexpr int kBlk = 2 * kPage * kRec8;  // 16384 bytes per 64-slot ring block
+constexpr int kRedStride = 132;          // floats per partial row: m, l, 2 pad, acc[128] (16-byte aligned)
+constexpr int kPushBytes = 8 + 4 * kD;   // bytes pushed per query row: (m, l) and acc
+constexpr int kMaxCluster = 8;
+constexpr int kMaxBlocksPerStream = 4;   // beyond this the split-K path with a combine pass is used
+constexpr size_t kSmemCap = 200 * 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct SwaParams {
+  const uint8_t* ring;  // [num_seqs][Hkv][nblk][kBlk]
+  int cap, nblk, window;
+  int B, S, Hq, Hkv, G, R;
+  const int32_t* pos0;
+  const void* q;
+  int bf16;  // q, k_new, v_new are bf16 (else fp32)
+  const void* k_new;
+  const void* v_new;
+  float k_scale, v_scale, score_scale;
+  float* out;
+  int32_t* dev_err;
+  int cs, nws, ntg, nst, rows_pad;
+};
+
+struct SwaPlan {
+  int NT, ntg, nws, cs, nst, rows_pad, bps;
+  size_t smem;
+};
+
+// Shared memory: stages [warp][nst][kBlk] (a warp's partial reuses its first stage), the
+// warps' copy barriers [warp][nst], the receive barrier, the receive area [cs][rows_pad][132].
+__host__ __device__ __forceinline__ size_t swa_bar_offset(int nw, int nst) { return (size_t)nw * nst * kBlk; }
+__host__ __device__ __forceinline__ size_t swa_recv_offset(int nw, int nst) {
+  return (swa_bar_offset(nw, nst) + 8 * ((size_t)nw * nst + 1) + 15) / 16 * 16;
+}
+
+SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
+  SwaPlan pl{};
+  const int nblk = cap / kPage;
+  const int R = S * (Hq / Hkv);
+  const int ntiles = (R + 7) / 8;
+  if (ntiles <= 3) {
+    pl.NT = ntiles;
+    pl.ntg = 1;
+  } else {
+    pl.NT = (ntiles + 1) / 2;
+    pl.ntg = 2;
+  }
+  pl.rows_pad = pl.ntg * pl.NT * 8;
+  for (int nws = KVQ_SWA_STREAMS; nws >= 1; --nws) {
+    pl.nws = nws;
+    pl.cs = std::min(kMaxCluster, (nblk + nws - 1) / nws);
+    const int ns = pl.cs * nws;
+    pl.bps = (nblk + ns - 1) / ns;
+    const int nw = nws * pl.ntg;
+    for (pl.nst = std::min(2, pl.bps); pl.nst >= 1; --pl.nst) {
+      pl.smem = swa_recv_offset(nw, pl.nst) + (size_t)pl.cs * pl.rows_pad * kRedStride * 4;
+      if (pl.smem <= kSmemCap) return pl;
+    }
+  }
+  pl.smem = 0;  // does not fit (cannot happen for rows_pad <= 48)
+  return pl;
+}
+
+// Output dim of accumulator row `row` (0..15) of PV m-tile `mt` (0..7): m-tile mt covers the
+// 16 dims 16 mt .. 16 mt + 15, its row r holding dim 16 mt + 2 (r & 7) + (r >> 3) because V's
+// e4m3 bytes are split into even/odd dims by the byte permute before conversion.
+__device__ __forceinline__ int swa_out_dim(int mt, int row) { return 16 * mt + 2 * (row & 7) + (row >> 3); }
+
+// One 64-slot block (K half then V half at `st`) against the warp's query tiles.
+template <int NT>
+__device__ __forceinline__ void attend_block(const uint8_t* st, int j, int p_last, int slot_last, int cap,
+                                             float score_scale, const uint32_t (&qf)[NT][8][2],
+                                             const int (&lim_lo)[NT][2], const int (&lim_hi)[NT][2],
+                                             float (&m)[NT][2], float (&l)[NT][2], float (&acc)[NT][8][4],
+                                             int lane) {
+  constexpr int MTU = NT == 1 ? 4 : 2;  // 16-slot m-tiles per online-softmax update
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int mt0 = 0; mt0 < 4; mt0 += MTU) {
+    // ---- scores: S[slot][row] = sum_d K[slot][d] q[row][d], K and q in f16 (exact for e4m3)
+    float sc[NT][MTU][4];
+#pragma unroll
+    for (int u = 0; u < MTU; ++u) {
+      const int mt = mt0 + u;
+      float d[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
+      const int ta = 16 * mt + g, tb = ta + 8;  // both slots have (slot & 7) == g
+      const uint4 a0 = *reinterpret_cast<const uint4*>(st + ta * kRec8 + 16 * ((2 * t) ^ g));
+      const uint4 a1 = *reinterpret_cast<const uint4*>(st + ta * kRec8 + 16 * ((2 * t + 1) ^ g));
+      const uint4 b0 = *reinterpret_cast<const uint4*>(st + tb * kRec8 + 16 * ((2 * t) ^ g));
+      const uint4 b1 = *reinterpret_cast<const uint4*>(st + tb * kRec8 + 16 * ((2 * t + 1) ^ g));
+      const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint32_t Bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t x0 = e4m3x2_to_f16x2(A[ks] & 0xFFFFu), x2 = e4m3x2_to_f16x2(A[ks] >> 16);
+        const uint32_t x1 = e4m3x2_to_f16x2(Bw[ks] & 0xFFFFu), x3 = e4m3x2_to_f16x2(Bw[ks] >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt], x0, x1, x2, x3, qf[nt][ks][0], qf[nt][ks][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[nt][u][c] = d[nt][c] * score_scale;
+    }
+    // ---- window mask: slot -> position through the newest slot
+#pragma unroll
+    for (int u = 0; u < MTU; ++u)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int slot = j * kPage + 16 * (mt0 + u) + g + 8 * hh;
+        int back = slot_last - slot;
+        if (back < 0) back += cap;
+        const int pos = p_last - back;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            if (pos < lim_lo[nt][jj] || pos > lim_hi[nt][jj]) sc[nt][u][2 * hh + jj] = -INFINITY;
+      }
+    // ---- online softmax
+    float muse[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < MTU; ++u) mx = fmaxf(mx, fmaxf(sc[nt][u][jj], sc[nt][u][2 + jj]));
+        mx = warp_max_g(mx);
+        const float mnew = fmaxf(m[nt][jj], mx);
+        muse[nt][jj] = mnew == -INFINITY ? 0.0f : mnew;
+        const float alpha = fast_exp2(m[nt][jj] - muse[nt][jj]);
+        m[nt][jj] = mnew;
+        if (alpha != 1.0f) {
+          l[nt][jj] *= alpha;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc[nt][i][jj] *= alpha;
+            acc[nt][i][2 + jj] *= alpha;
+          }
+        }
+      }
+    // ---- P (transposed into a B fragment) and PV
+#pragma unroll
+    for (int u = 0; u < MTU; ++u) {
+      const int mt = mt0 + u;
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float pr[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[nt][u][c] - muse[nt][c & 1]);
+        l[nt][0] += pr[0] + pr[2];
+        l[nt][1] += pr[1] + pr[3];
+        pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
+        pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
+      }
+      const uint8_t* Vs = st + kPage * kRec8;
+      const int qi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int cprime = 2 * cc + (qi >> 1), th = qi & 1;
+        const int slot = 16 * mt + 8 * th + r8;
+        uint32_t rr[4];
+        ldsm_x4_trans(rr, smem_addr(Vs + slot * kRec8 + 16 * (cprime ^ r8)));
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+          const uint32_t y0 = prmt(rr[2 * ci], 0u, 0x3120u);
+          const uint32_t y1 = prmt(rr[2 * ci + 1], 0u, 0x3120u);
+          const uint32_t v0 = e4m3x2_to_f16x2(y0 & 0xFFFFu), v1 = e4m3x2_to_f16x2(y0 >> 16);
+          const uint32_t v2 = e4m3x2_to_f16x2(y1 & 0xFFFFu), v3 = e4m3x2_to_f16x2(y1 >> 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt][2 * cc + ci], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+        }
+      }
+    }
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int nw = p.nws * p.ntg;
+  const int ws = warp / p.ntg, tg = warp - (warp / p.ntg) * p.ntg;
+  const int rank = (int)cluster_ctarank();
+  const int pair = blockIdx.x / p.cs;  // (sequence, KV head) of this cluster
+  const int b = pair / p.Hkv, h = pair - (pair / p.Hkv) * p.Hkv;
+  const int stream = rank * p.nws + ws, nstream = p.cs * p.nws;
+  const int nb = stream < p.nblk ? (p.nblk - 1 - stream) / nstream + 1 : 0;  // blocks of this stream
+  uint8_t* wst = smem + (size_t)warp * p.nst * kBlk;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + swa_bar_offset(nw, p.nst));
+  uint64_t* wfull = bars + warp * p.nst;
+  uint64_t* recv_bar = bars + nw * p.nst;
+  float* recv = reinterpret_cast<float*>(smem + swa_recv_offset(nw, p.nst));
+  uint8_t* seg = const_cast<uint8_t*>(p.ring) + (size_t)pair * p.nblk * kBlk;
+
+  // ---- prologue, which may overlap the previous grid on the stream: barriers, and L2
+  // prefetches of this stream's ring blocks and of the query and appended rows (L2 is
+  // coherent, so a grid still writing them cannot leave stale copies). Nothing is read
+  // before griddep_wait().
+  const size_t rb = (size_t)kD * (p.bf16 ? 2 : 4);  // bytes per q / k / v row
+  if (lane == 0) {
+    for (int s = 0; s < p.nst; ++s) mbar_init(&wfull[s], 1);
+    if (warp == 0) {
+      mbar_init(recv_bar, 1);
+      if (rank == 0) mbar_arrive_expect_tx(recv_bar, (uint32_t)((p.cs - 1) * p.R * kPushBytes));
+    }
+    fence_barrier_init();
+    fence_proxy_async_shared();
+    if (tg == 0)
+      for (int i = 0; i < nb; ++i) prefetch_l2_bulk(seg + (size_t)(stream + i * nstream) * kBlk, kBlk);
+    if (warp == 0 && rank == 0) {
+      prefetch_l2(p.pos0 + b);
+      for (int r = 0; r < p.S; ++r)  // the G query rows of this KV head are contiguous
+        prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) + (((size_t)b * p.S + r) * p.Hq + (size_t)h * p.G) * rb,
+                         (uint32_t)(p.G * rb));
+    }
+  }
+  if (p.k_new != nullptr && warp == 0 && lane < 2 * p.S) {
+    const size_t row = ((size_t)b * p.S + (lane >> 1)) * p.Hkv + h;
+    prefetch_l2_bulk(static_cast<const uint8_t*>((lane & 1) ? p.v_new : p.k_new) + row * rb, (uint32_t)rb);
+  }
+  __syncwarp();
+  cluster_arrive_relaxed();
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // ---- this warp's first copies (L2 hits when the prefetch had time to land)
+  if (lane == 0) {
+    const uint64_t pol = policy_evict_first();
+    for (int i = 0; i < min(p.nst, nb); ++i) {
+      mbar_arrive_expect_tx(&wfull[i], kBlk);
+      bulk_g2s(wst + (size_t)i * kBlk, seg + (size_t)(stream + i * nstream) * kBlk, kBlk, &wfull[i], pol);
+    }
+  }
+  __syncwarp();
+
+  int c0 = p.pos0[b];
+  if (c0 < 0) {
+    if (rank == 0 && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
+    c0 = 0;
+  }
+  const int p_last = c0 + p.S - 1;  // newest position after the append
+  const int slot_last = p_last % p.cap;
+
+  // ---- query fragments (B operand, 8 rows per tile) and per-row window limits
+  uint32_t qf[NT][8][2];
+  int lim_lo[NT][2], lim_hi[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int tile = tg * NT + nt;
+    const int nB = 8 * tile + g;
+    float qv[32];
+    if (nB < p.R) {
+      const size_t row = ((size_t)b * p.S + nB / p.G) * p.Hq + h * p.G + nB % p.G;
+      if (!p.bf16) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + row * kD + 32 * t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = src[i];
+          qv[4 * i] = v.x;
+          qv[4 * i + 1] = v.y;
+          qv[4 * i + 2] = v.z;
+          qv[4 * i + 3] = v.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + row * kD + 32 * t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = src[i];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            qv[8 * i + 2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
+            qv[8 * i + 2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+    }
+    // k-step ks covers dims 32 t' + 4 ks .. +3 of lane t' (the K words are read in the
+    // matching order, so the dot product pairs every dim with itself)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[nt][ks][0] = pack_f16x2(qv[4 * ks], qv[4 * ks + 1]);
+      qf[nt][ks][1] = pack_f16x2(qv[4 * ks + 2], qv[4 * ks + 3]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int nC = 8 * tile + 2 * t + jj;
+      const int r = nC < p.R ? nC / p.G : 0;
+      lim_hi[nt][jj] = c0 + r;
+      lim_lo[nt][jj] = max(0, c0 + r - p.window + 1);
+    }
+  }
+
+  // ---- appended rows that fall in this stream's blocks: encode now (the loads overlap the copies)
+  uint32_t code[8][2];
+  uint32_t have = 0;  // bit 2 r + which: code[r][which] is valid and belongs to one of my blocks
+  if (p.k_new != nullptr) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      code[r][0] = code[r][1] = 0;
+      if (r >= p.S) continue;
+      const int slot = (c0 + r) % p.cap;
+      const int j = slot / kPage;
+      if (j < stream || (j - stream) % nstream != 0) continue;
+      const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float x[4];
+        load_row4(which ? p.v_new : p.k_new, p.bf16, row, lane, x);
+        if (!warp_all_finite(x)) {
+          if (lane == 0 && tg == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
+          continue;
+        }
+        code[r][which] = fp8_encode4(x, which ? p.v_scale : p.k_scale);
+        have |= 1u << (2 * r + which);
+        if (tg == 0)  // the ring copy for later steps, written once per block
+          *reinterpret_cast<uint32_t*>(seg + (size_t)j * kBlk + which * kPage * kRec8 + fp8_lane_offset(slot, lane)) =
+              code[r][which];
+      }
+    }
+  }
+
+  float m[NT][2], l[NT][2], acc[NT][8][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      m[nt][jj] = -INFINITY;
+      l[nt][jj] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[nt][i][c] = 0.0f;
+  }
+
+  int done = 0;  // blocks consumed
+  for (int i = 0; i < nb; ++i) {
+    const int s = i % p.nst;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&wfull[s], (uint32_t)(i / p.nst) & 1u));
+    if (!ok) {
+      if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+      break;
+    }
+    uint8_t* st = wst + (size_t)s * kBlk;
+    const int j = stream + i * nstream;
+    if (have) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r >= p.S) break;
+        const int slot = (c0 + r) % p.cap;
+        if (slot / kPage != j) continue;
+#pragma unroll
+        for (int which = 0; which < 2; ++which)
+          if (have >> (2 * r + which) & 1u)
+            *reinterpret_cast<uint32_t*>(st + which * kPage * kRec8 + fp8_lane_offset(slot, lane)) = code[r][which];
+      }
+      __syncwarp();
+    }
+    attend_block<NT>(st, j, p_last, slot_last, p.cap, p.score_scale, qf, lim_lo, lim_hi, m, l, acc, lane);
+    done = i + 1;
+    __syncwarp();
+    if (lane == 0 && i + p.nst < nb) {  // refill this stage with the stream's block i + nst
+      fence_proxy_async_shared();
+      mbar_arrive_expect_tx(&wfull[s], kBlk);
+      bulk_g2s(st, seg + (size_t)(j + p.nst * nstream) * kBlk, kBlk, &wfull[s], policy_evict_first());
+    }
+  }
+  if (done < nb && lane == 0) {  // gave up: let the copies still in flight land before leaving
+    for (int i = done; i < min(nb, done + p.nst); ++i)
+      if (!mbar_wait_bounded(&wfull[i % p.nst], (uint32_t)(i / p.nst) & 1u)) break;
+  }
+
+  // ---- this stream's partial for its tile group's rows, into its own first stage (all of
+  // the warp's copies have landed or been waited for)
+  float* part = reinterpret_cast<float*>(wst);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const float lt = warp_sum_g(l[nt][jj]);
+      float* dst = part + (8 * nt + 2 * t + jj) * kRedStride;
+      if (g == 0) {
+        dst[0] = m[nt][jj];
+        dst[1] = lt;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dst[4 + swa_out_dim(i, g)] = acc[nt][i][jj] * p.v_scale;
+        dst[4 + swa_out_dim(i, g + 8)] = acc[nt][i][2 + jj] * p.v_scale;
+      }
+    }
+  }
+  __syncthreads();
+  cluster_wait();  // CTA 0's receive barrier is initialised and armed
+
+  // ---- merge: item = (query row, 4 consecutive dims). Every CTA merges its own streams; the
+  // other CTAs push that into CTA 0, which merges the cluster and writes the output.
+  const uint32_t bar0 = map_cluster(smem_addr(recv_bar), 0);
+  const uint32_t recv0 = map_cluster(smem_addr(recv), 0);
+  if (rank == 0 && !mbar_wait_bounded(recv_bar, 0) && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+  for (int e = threadIdx.x; e < p.R * 32; e += blockDim.x) {
+    const int row = e >> 5, c4 = e & 31;
+    const int tgr = (row >> 3) / NT;  // tile group holding this row
+    const int rl = row - 8 * NT * tgr;
+    float M = -INFINITY;
+    for (int w2 = 0; w2 < p.nws; ++w2)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + (size_t)(w2 * p.ntg + tgr) * p.nst * kBlk)[rl * kRedStride]);
+    const float Mu = M == -INFINITY ? 0.0f : M;
+    float lsum = 0.0f;
+    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int w2 = 0; w2 < p.nws; ++w2) {
+      const float* src = reinterpret_cast<const float*>(smem + (size_t)(w2 * p.ntg + tgr) * p.nst * kBlk) +
+                         rl * kRedStride;
+      const float wgt = fast_exp2(src[0] - Mu);
+      const float4 v = reinterpret_cast<const float4*>(src + 4)[c4];
+      lsum += wgt * src[1];
+      a.x += wgt * v.x;
+      a.y += wgt * v.y;
+      a.z += wgt * v.z;
+      a.w += wgt * v.w;
+    }
+    if (rank != 0) {
+      const uint32_t dst = recv0 + 4u * (uint32_t)((rank * p.rows_pad + row) * kRedStride);
+      if (c4 == 0) st_async_f32x2(dst, M, lsum, bar0);
+      st_async_f32x4(dst + 16 + 16 * c4, a, bar0);
+      continue;
+    }
+    // CTA 0: fold in the other CTAs' partials (relative to their own maxima)
+    float Mc = M;
+    for (int rr = 1; rr < p.cs; ++rr) Mc = fmaxf(Mc, recv[(rr * p.rows_pad + row) * kRedStride]);
+    const float Mcu = Mc == -INFINITY ? 0.0f : Mc;
+    const float w0 = fast_exp2(M - Mcu);
+    lsum *= w0;
+    a.x *= w0;
+    a.y *= w0;
+    a.z *= w0;
+    a.w *= w0;
+    for (int rr = 1; rr < p.cs; ++rr) {
+      const float* src = recv + (rr * p.rows_pad + row) * kRedStride;
+      const float wgt = fast_exp2(src[0] - Mcu);
+      const float4 v = reinterpret_cast<const float4*>(src + 4)[c4];
+      lsum += wgt * src[1];
+      a.x += wgt * v.x;
+      a.y += wgt * v.y;
+      a.z += wgt * v.z;
+      a.w += wgt * v.w;
+    }
+    const int r = row / p.G, gi = row - (row / p.G) * p.G;
+    const float inv = 1.0f / lsum;
+    float4* dst = reinterpret_cast<float4*>(p.out + (((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD) + c4;
+    *dst = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+  }
+}
+
+struct SwaDevCache {
+  bool attr[4] = {false};
+};
+SwaDevCache g_swa_dev[64];
+
+template <int NT>
+cudaError_t launch_swa_t(const SwaParams& p, size_t smem, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  SwaDevCache& dc = g_swa_dev[(dev >= 0 && dev < 64) ? dev : 0];
+  if (!dc.attr[NT]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(swa_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
+    if (e != cudaSuccess) return e;
+    dc.attr[NT] = true;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((long long)p.B * p.Hkv * p.cs), 1, 1);
+  cfg.blockDim = dim3((unsigned)(p.nws * p.ntg * 32), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // the prologue (barriers, L2 prefetches) may overlap the previous grid on the stream
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, swa_cluster_kernel<NT>, p);
+}
+
+}  // namespace
+
+bool swa_cluster_path(int capacity, int S, int Hq, int Hkv) {
+  const SwaPlan pl = make_plan(capacity, S, Hq, Hkv);
+  return pl.smem != 0 && pl.bps <= kMaxBlocksPerStream;
+}
+
+cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream) {
+  const SwaPlan pl = make_plan(job.ring.capacity, job.S, job.Hq, job.Hkv);
+  SwaParams p{};
+  p.ring = job.ring.data;
+  p.cap = job.ring.capacity;
+  p.nblk = p.cap / kPage;
+  p.window = job.window;
+  p.B = job.B;
+  p.S = job.S;
+  p.Hq = job.Hq;
+  p.Hkv = job.Hkv;
+  p.G = job.Hq / job.Hkv;
+  p.R = p.S * p.G;
+  p.pos0 = job.ctx;
+  p.q = job.q;
+  p.bf16 = job.q_bf16;
+  p.k_new = job.k_new;
+  p.v_new = job.v_new;
+  p.k_scale = job.k_scale;
+  p.v_scale = job.v_scale;
+  p.score_scale = job.sm_scale * kLog2e * job.k_scale;
+  p.out = job.out;
+  p.dev_err = job.dev_err;
+  p.cs = pl.cs;
+  p.nws = pl.nws;
+  p.ntg = pl.ntg;
+  p.nst = pl.nst;
+  p.rows_pad = pl.rows_pad;
+  switch (pl.NT) {
+    case 1: return launch_swa_t<1>(p, pl.smem, stream);
+    case 2: return launch_swa_t<2>(p, pl.smem, stream);
+    default: return launch_swa_t<3>(p, pl.smem, stream);
+  }
+}
+
+}  // namespace kvq

@@ -12,7 +12,7 @@ import torch
 import synth
 from gpu_util import (assert_close, device_kv, device_new_kv, device_q, oracle_int4_seq, oracle_layer_params,
                       oracle_swa_seq, unpack_fp8, unpack_int4)
-from quantized_kv_cache_fold_gb300 import DEVERR_NONFINITE, DEVERR_PAGE, KvqError
+from quantized_kv_cache_fold_gb300 import DEVERR_NONFINITE, DEVERR_PAGE, DEVERR_POS, KvqError
 from quantized_kv_cache_fold_gb300.runner import DecodeStack
 from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, Workload, config
 
@@ -225,10 +225,55 @@ def test_swa_small_window(orc):
     check_swa(orc, w, 1, 2, window=16, cap=64)
 
 
+@pytest.mark.parametrize("cap", [1024, 2048, 4096])
+def test_swa_cluster_streams(orc, cap):
+    """Rings of 16, 32 and 64 blocks over one 8-CTA cluster per (sequence, KV head): 1, 2 and 4
+    blocks per warp stream (one- and two-stage buffers, refills after a patched stage)."""
+    w = Workload(f"swa-ring{cap}", 23, 3, 20, 4, 2, np.array([40, cap - 300, 3 * cap + 17]), True)
+    check_swa(orc, w, 2, 2, window=cap - 500, cap=cap)
+
+
 def test_swa_large_ring_general_path(orc):
-    """A 1024-slot ring (16 blocks) takes the split path with a separate append and a combine pass."""
-    w = Workload("swa-ring1024", 23, 3, 20, 4, 2, np.array([40, 700, 3000]), True)
-    check_swa(orc, w, 2, 2, window=513, cap=1024)
+    """An 8192-slot ring (128 blocks) is beyond one cluster: separate append, split-K path and
+    a combine pass."""
+    w = Workload("swa-ring8192", 25, 2, 20, 4, 2, np.array([5000, 20000]), True)
+    check_swa(orc, w, 3, 2, window=4097, cap=8192)
+
+
+def test_swa_many_sequences(orc):
+    """40 sequences x 4 KV heads: 160 clusters of 5 CTAs, more CTAs than SMs."""
+    ctx = (np.arange(40) * 97 % 1500).astype(np.int64)
+    w = Workload("swa-many", 26, len(ctx), 20, 4, 1, ctx, True)
+    check_swa(orc, w, 4, 1)
+
+
+def test_swa_nonfinite_row_and_bad_position_flagged(orc):
+    """A NaN in one appended window key is flagged and that row is neither stored nor attended;
+    the other (sequence, KV head) pairs stay exact. A negative position is flagged and clamped."""
+    w = Workload("swa-err", 27, 2, 20, 4, 1, np.array([700, 900]), True)
+    st = build_swa(w, 5, 1)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    q = device_q(w, 5, 1, w.ctx, swa=True)
+    k_new = device_new_kv(w, 5, 1, w.ctx, "swa_k")
+    v_new = device_new_kv(w, 5, 1, w.ctx, "swa_v")
+    k_new[1, 0, 3, 7] = float("nan")
+    out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device="cuda")
+    st.decode_layer(0, q, ctx, out, k_new=k_new, v_new=v_new)
+    torch.cuda.synchronize()
+    assert st.read_error() == DEVERR_NONFINITE
+    got = out.cpu().numpy()
+    for b, h in [(0, 0), (0, 3), (1, 0), (1, 2)]:
+        kc, vc, positions, ref = oracle_swa_seq(orc, w, 5, b, h, 1, int(w.ctx[b]), 513)
+        gk, gv = unpack_fp8(st.layers[0].tensors, b, h, positions)
+        assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+        assert_close(got[b, :, h * w.G:(h + 1) * w.G], ref, f"swa seq {b} head {h}")
+    assert np.isfinite(got).all()
+    st.dev_err.zero_()
+    bad = torch.tensor([-5, 900], dtype=torch.int32, device="cuda")
+    st.decode_layer(0, q, bad, out)
+    torch.cuda.synchronize()
+    assert st.read_error() == DEVERR_POS
+    assert np.isfinite(out.cpu().numpy()).all()
 
 
 def test_int4_many_segments_single_cta(orc):
