@@ -206,6 +206,9 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   const int nwc = p.ntg * p.nkg;
   const int nst = p.nstages;
 
+  // launched with programmatic serialisation: nothing is read before the previous grid is done
+  griddep_wait();
+  griddep_launch_dependents();
   build_prefix(p, FMT, pre, flags);
   if (threadIdx.x < nst) {
     mbar_init(&full[threadIdx.x], 1);
@@ -700,6 +703,8 @@ template <int FMT>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
   volatile int* flags = cpre + p.B + 1;
+  griddep_wait();
+  griddep_launch_dependents();
   build_prefix(p, FMT, cpre, flags);
   __syncthreads();
   const int R = p.R;
@@ -763,12 +768,24 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   long long grid = std::min<long long>((long long)dc.sm * occ, kMaxCtas);
   grid = std::max<long long>(1, std::min(grid, p_max));
   p.n_cta = (int)grid;
-  attn_kernel<FMT, NT><<<(unsigned)grid, threads, smem, stream>>>(p);
-  e = cudaGetLastError();
+  // both grids may start while the previous one on the stream finishes (each waits for it
+  // before reading anything)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_kernel<FMT, NT>, p);
   if (e != cudaSuccess) return e;
-  const size_t csmem = (p.B + 1 + 4) * sizeof(int);
-  combine_kernel<FMT><<<(unsigned)(p.B * p.Hkv * p.R), 128, csmem, stream>>>(p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
 }
 
 }  // namespace

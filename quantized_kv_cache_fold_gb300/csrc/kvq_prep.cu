@@ -116,6 +116,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   const PrepJobs& j = p.j;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
+  // may overlap the previous grid on the stream: only an L2 prefetch of the matrix before the wait
+  if (threadIdx.x == 0) prefetch_l2_bulk(M, kD * kD * 4);
+  griddep_wait();
+  griddep_launch_dependents();
   {
     // 16 independent 16-byte loads per thread, then the padded (conflict-free) shared stores
     constexpr int kPer = kD * kD / 4 / kPrepThreads;
@@ -279,8 +283,17 @@ cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  prep_kernel<<<p.kv_blocks + q_blocks, kPrepThreads, kPrepSmem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(p.kv_blocks + q_blocks), 1, 1);
+  cfg.blockDim = dim3(kPrepThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPrepSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prep_kernel, p);
 }
 
 cudaError_t launch_fp8_append(const Fp8AppendJob& job, cudaStream_t stream) {

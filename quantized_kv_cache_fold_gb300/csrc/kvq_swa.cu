@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   }
   __syncwarp();
   cluster_arrive_relaxed();
-  griddep_launch_dependents();
   griddep_wait();
+  griddep_launch_dependents();  // after the wait: at most one grid runs ahead
 
   // ---- this warp's first copies (L2 hits when the prefetch had time to land)
   if (lane == 0) {
