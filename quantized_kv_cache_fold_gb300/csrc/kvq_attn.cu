@@ -47,6 +47,11 @@ namespace {
 #ifndef KVQ_INT4_MAXREG
 #define KVQ_INT4_MAXREG 168
 #endif
+// A consumer warp takes pages kg, kg + nkg, ... and page k lands in stage k mod nstages with
+// phase parity (k / nstages) & 1. Parity only tells adjacent phases apart, so every stage
+// must belong to one consumer warp (nstages a multiple of nkg); otherwise a warp running
+// ahead could pass the wait for round f while round f - 1 of that stage is still in flight.
+static_assert(KVQ_STAGES_INT4 % KVQ_TOKEN_GROUPS == 0, "stages must be a multiple of the token groups");
 
 constexpr int kStage4 = 2 * kPage * kRec4 + 2 * kPage * 4;  // 8704 bytes: K codes, V codes, K meta, V meta
 constexpr int kStage8 = 2 * kPage * kRec8;                  // 16384 bytes: K and V e4m3
@@ -846,6 +851,7 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p.nstages = 4;
   }
   p.rows_pad = p.ntg * NT * 8;
+  if (p.nstages % p.nkg != 0) return cudaErrorInvalidConfiguration;  // see the static_assert above
   const int threads = (p.ntg * p.nkg + 1) * 32;
   const SmemLayout L(job.fmt, p.nstages, p.B, p.nkg, p.rows_pad);
   const size_t smem = L.total;

@@ -6,30 +6,31 @@
 // as 64-slot blocks of 16384 bytes (64 K records of 128 e4m3 codes, then 64 V records; the
 // 16-byte chunks of slot s's record in XOR order, chunk c at c ^ (s & 7)).
 //
-// A window is a few hundred positions, so one (sequence, KV head) is far too little work to
-// split across a whole grid and merge through global memory, and far too much latency for a
-// single SM to pull alone (one SM ingests a 576-slot ring at ~30 GB/s). Here the ring is
-// spread over the CTAs of one cluster (at most 8), their warps reading disjoint blocks, and
-// the partial softmax states are merged through distributed shared memory:
+// A window is a few hundred positions: far too little work to spread over a whole grid and
+// merge through global memory, and far too much latency for one SM to pull and process alone.
+// Here the ring is cut into 32-slot units spread over the warps of one cluster (at most 8
+// CTAs), and the partial softmax states are merged on chip:
 //
-//   warp (block stream w, tile group tg): streams the blocks j = w, w + NS, w + 2 NS, ...
+//   warp (unit stream w, tile group tg): streams the units u = w, w + NS, w + 2 NS, ...
 //     (NS = streams in the cluster) through its own one- or two-stage shared-memory buffer,
-//     each block one bulk copy (TMA engine) completing on the warp's own mbarrier;
-//     if the call appends rows, the stream owning a new row's block encodes it (e4m3 of
+//     each unit two bulk copies (TMA engine; its 32 K records and its 32 V records)
+//     completing on the warp's own mbarrier;
+//     if the call appends rows, the stream owning a new row's unit encodes it (e4m3 of
 //     x / scale), stores it into the ring for later steps (tile group 0 only) and patches
 //     it into the landed copy, so the appended rows are attended in the same launch;
 //     QK^T and PV on tensor cores (mma.m16n8k16, e4m3 -> f16 exactly), online softmax in
 //     exp2 form, query rows masked outside [max(0, p_r - window + 1), p_r];
-//   partial (m, l, acc[128]) of every stream and query row -> the warp's own stage buffer;
-//   each CTA merges its streams' partials per (row, 4 dims) with log-sum-exp weights and
-//   pushes the result into CTA 0 of the cluster with asynchronous remote stores (st.async)
-//   that complete a byte count on CTA 0's receive mbarrier, then exits; CTA 0 waits for
-//   all bytes, merges the cluster's partials from its own shared memory and writes the
-//   normalised output.
+//   partial (m, l, acc[128]) per stream and query row -> shared memory;
+//   each CTA merges its streams per (row, 8 dims) with log-sum-exp weights and pushes the
+//   result into CTA 0 of the cluster with asynchronous remote stores (st.async) that complete
+//   a byte count on CTA 0's receive mbarrier, then exits; CTA 0 waits for all bytes, merges
+//   the cluster's partials from its own shared memory and writes the normalised output.
 //
-// Every mbarrier wait is bounded (KVQ_DEVERR_TIMEOUT). The one cluster barrier (arrive at
-// start, wait before the first remote store) only publishes CTA 0's receive barrier, and
-// every thread reaches both halves unconditionally.
+// Launch with programmatic stream serialisation: the prologue (barrier set-up and L2
+// prefetches, which read nothing into the SM) may overlap the previous grid; everything else
+// follows griddepcontrol.wait. Every mbarrier wait is bounded (KVQ_DEVERR_TIMEOUT). The one
+// cluster barrier (arrive at start, wait before the first remote store) only publishes CTA
+// 0's receive barrier, and every thread reaches both halves unconditionally.
 
 #include <algorithm>
 #include <cmath>
@@ -40,22 +41,26 @@
 namespace kvq {
 namespace {
 
-// Block streams (warps per query-tile group) per CTA.
+// Unit streams (warps per query-tile group) per CTA.
 #ifndef KVQ_SWA_STREAMS
-#define KVQ_SWA_STREAMS 4
+#define KVQ_SWA_STREAMS 6
 #endif
 
-constexpr int kBlk = 2 * kPage * kRec8;  // 16384 bytes per 64-slot ring block
+constexpr int kBlk = 2 * kPage * kRec8;  // 16384 bytes per 64-slot ring block (K half, V half)
+constexpr int kUnit = 32;                // slots per work unit
+constexpr int kHalf = kUnit * kRec8;     // 4096 bytes: one unit's K (or V) records
+constexpr int kStg = 2 * kHalf;          // 8192 bytes per stage: the unit's K then V records
 constexpr int kRedStride = 132;          // floats per partial row: m, l, 2 pad, acc[128] (16-byte aligned)
 constexpr int kPushBytes = 8 + 4 * kD;   // bytes pushed per query row: (m, l) and acc
 constexpr int kMaxCluster = 8;
-constexpr int kMaxBlocksPerStream = 4;   // beyond this the split-K path with a combine pass is used
+constexpr int kMaxStreams = 8;           // unit streams per CTA (merge loops are unrolled to this)
+constexpr int kMaxUnitsPerStream = 4;    // beyond this the split-K path with a combine pass is used
 constexpr size_t kSmemCap = 200 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct SwaParams {
   const uint8_t* ring;  // [num_seqs][Hkv][nblk][kBlk]
-  int cap, nblk, window;
+  int cap, nblk, nunits, window;
   int B, S, Hq, Hkv, G, R;
   const int32_t* pos0;
   const void* q;
@@ -69,20 +74,25 @@ struct SwaParams {
 };
 
 struct SwaPlan {
-  int NT, ntg, nws, cs, nst, rows_pad, bps;
+  int NT, ntg, nws, cs, nst, rows_pad, ups;
   size_t smem;
 };
 
-// Shared memory: stages [warp][nst][kBlk] (a warp's partial reuses its first stage), the
-// warps' copy barriers [warp][nst], the receive barrier, the receive area [cs][rows_pad][132].
-__host__ __device__ __forceinline__ size_t swa_bar_offset(int nw, int nst) { return (size_t)nw * nst * kBlk; }
-__host__ __device__ __forceinline__ size_t swa_recv_offset(int nw, int nst) {
-  return (swa_bar_offset(nw, nst) + 8 * ((size_t)nw * nst + 1) + 15) / 16 * 16;
-}
+// Shared memory: stages [warp][nst][kStg], the warps' copy barriers [warp][nst] and the
+// receive barrier, partials [warp][NT*8][132], the receive area [cs][rows_pad][132].
+struct SwaSmem {
+  size_t bars, part, recv, total;
+  __host__ __device__ SwaSmem(int nw, int nst, int NT, int cs, int rows_pad) {
+    bars = (size_t)nw * nst * kStg;
+    part = (bars + 8 * ((size_t)nw * nst + 1) + 15) / 16 * 16;
+    recv = part + (size_t)nw * NT * 8 * kRedStride * 4;
+    total = recv + (size_t)cs * rows_pad * kRedStride * 4;
+  }
+};
 
 SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
   SwaPlan pl{};
-  const int nblk = cap / kPage;
+  const int nunits = cap / kUnit;
   const int R = S * (Hq / Hkv);
   const int ntiles = (R + 7) / 8;
   if (ntiles <= 3) {
@@ -93,14 +103,14 @@ SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
     pl.ntg = 2;
   }
   pl.rows_pad = pl.ntg * pl.NT * 8;
-  for (int nws = KVQ_SWA_STREAMS; nws >= 1; --nws) {
+  for (int nws = std::min(KVQ_SWA_STREAMS, kMaxStreams); nws >= 1; --nws) {
+    if (nws * pl.ntg * 32 > 256) continue;
     pl.nws = nws;
-    pl.cs = std::min(kMaxCluster, (nblk + nws - 1) / nws);
+    pl.cs = std::min(kMaxCluster, (nunits + nws - 1) / nws);
     const int ns = pl.cs * nws;
-    pl.bps = (nblk + ns - 1) / ns;
-    const int nw = nws * pl.ntg;
-    for (pl.nst = std::min(2, pl.bps); pl.nst >= 1; --pl.nst) {
-      pl.smem = swa_recv_offset(nw, pl.nst) + (size_t)pl.cs * pl.rows_pad * kRedStride * 4;
+    pl.ups = (nunits + ns - 1) / ns;
+    for (pl.nst = std::min(2, pl.ups); pl.nst >= 1; --pl.nst) {
+      pl.smem = SwaSmem(nws * pl.ntg, pl.nst, pl.NT, pl.cs, pl.rows_pad).total;
       if (pl.smem <= kSmemCap) return pl;
     }
   }
@@ -113,119 +123,125 @@ SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
 // e4m3 bytes are split into even/odd dims by the byte permute before conversion.
 __device__ __forceinline__ int swa_out_dim(int mt, int row) { return 16 * mt + 2 * (row & 7) + (row >> 3); }
 
-// One 64-slot block (K half then V half at `st`) against the warp's query tiles.
+// Byte offset of lane l's four codes of the record in ring slot `slot` within a unit's K (or
+// V) records: same chunk order as in the ring block (chunk c at c ^ (slot & 7)).
+__device__ __forceinline__ int unit_lane_offset(int slot, int lane) {
+  return (slot & (kUnit - 1)) * kRec8 + ((lane >> 2) ^ (slot & 7)) * 16 + ((4 * lane) & 15);
+}
+
+// One 32-slot unit (K records then V records at `st`, unit index u) against the warp's query tiles.
 template <int NT>
-__device__ __forceinline__ void attend_block(const uint8_t* st, int j, int p_last, int slot_last, int cap,
-                                             float score_scale, const uint32_t (&qf)[NT][8][2],
-                                             const int (&lim_lo)[NT][2], const int (&lim_hi)[NT][2],
-                                             float (&m)[NT][2], float (&l)[NT][2], float (&acc)[NT][8][4],
-                                             int lane) {
-  constexpr int MTU = NT == 1 ? 4 : 2;  // 16-slot m-tiles per online-softmax update
+__device__ __forceinline__ void attend_unit(const uint8_t* st, int u, int p_last, int slot_last, int cap,
+                                            float score_scale, const uint32_t (&qf)[NT][8][2],
+                                            const int (&lim_lo)[NT][2], const int (&lim_hi)[NT][2],
+                                            float (&m)[NT][2], float (&l)[NT][2], float (&acc)[NT][8][4],
+                                            int lane) {
   const int g = lane >> 2, t = lane & 3;
+  // ---- scores: S[slot][row] = sum_d K[slot][d] q[row][d], K and q in f16 (exact for e4m3)
+  float sc[NT][2][4];
 #pragma unroll
-  for (int mt0 = 0; mt0 < 4; mt0 += MTU) {
-    // ---- scores: S[slot][row] = sum_d K[slot][d] q[row][d], K and q in f16 (exact for e4m3)
-    float sc[NT][MTU][4];
-#pragma unroll
-    for (int u = 0; u < MTU; ++u) {
-      const int mt = mt0 + u;
-      float d[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
-      const int ta = 16 * mt + g, tb = ta + 8;  // both slots have (slot & 7) == g
-      const uint4 a0 = *reinterpret_cast<const uint4*>(st + ta * kRec8 + 16 * ((2 * t) ^ g));
-      const uint4 a1 = *reinterpret_cast<const uint4*>(st + ta * kRec8 + 16 * ((2 * t + 1) ^ g));
-      const uint4 b0 = *reinterpret_cast<const uint4*>(st + tb * kRec8 + 16 * ((2 * t) ^ g));
-      const uint4 b1 = *reinterpret_cast<const uint4*>(st + tb * kRec8 + 16 * ((2 * t + 1) ^ g));
-      const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const uint32_t Bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t x0 = e4m3x2_to_f16x2(A[ks] & 0xFFFFu), x2 = e4m3x2_to_f16x2(A[ks] >> 16);
-        const uint32_t x1 = e4m3x2_to_f16x2(Bw[ks] & 0xFFFFu), x3 = e4m3x2_to_f16x2(Bw[ks] >> 16);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt], x0, x1, x2, x3, qf[nt][ks][0], qf[nt][ks][1]);
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) sc[nt][u][c] = d[nt][c] * score_scale;
-    }
-    // ---- window mask: slot -> position through the newest slot
-#pragma unroll
-    for (int u = 0; u < MTU; ++u)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int slot = j * kPage + 16 * (mt0 + u) + g + 8 * hh;
-        int back = slot_last - slot;
-        if (back < 0) back += cap;
-        const int pos = p_last - back;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj)
-            if (pos < lim_lo[nt][jj] || pos > lim_hi[nt][jj]) sc[nt][u][2 * hh + jj] = -INFINITY;
-      }
-    // ---- online softmax
-    float muse[NT][2];
+  for (int mt = 0; mt < 2; ++mt) {
+    float d[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        float mx = -INFINITY;
+      for (int c = 0; c < 4; ++c) d[nt][c] = 0.0f;
+    const int ta = 16 * mt + g, tb = ta + 8;  // both slots have (slot & 7) == g
+    const uint4 a0 = *reinterpret_cast<const uint4*>(st + ta * kRec8 + 16 * ((2 * t) ^ g));
+    const uint4 a1 = *reinterpret_cast<const uint4*>(st + ta * kRec8 + 16 * ((2 * t + 1) ^ g));
+    const uint4 b0 = *reinterpret_cast<const uint4*>(st + tb * kRec8 + 16 * ((2 * t) ^ g));
+    const uint4 b1 = *reinterpret_cast<const uint4*>(st + tb * kRec8 + 16 * ((2 * t + 1) ^ g));
+    const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t Bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-        for (int u = 0; u < MTU; ++u) mx = fmaxf(mx, fmaxf(sc[nt][u][jj], sc[nt][u][2 + jj]));
-        mx = warp_max_g(mx);
-        const float mnew = fmaxf(m[nt][jj], mx);
-        muse[nt][jj] = mnew == -INFINITY ? 0.0f : mnew;
-        const float alpha = fast_exp2(m[nt][jj] - muse[nt][jj]);
-        m[nt][jj] = mnew;
-        if (alpha != 1.0f) {
-          l[nt][jj] *= alpha;
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t x0 = e4m3x2_to_f16x2(A[ks] & 0xFFFFu), x2 = e4m3x2_to_f16x2(A[ks] >> 16);
+      const uint32_t x1 = e4m3x2_to_f16x2(Bw[ks] & 0xFFFFu), x3 = e4m3x2_to_f16x2(Bw[ks] >> 16);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc[nt][i][jj] *= alpha;
-            acc[nt][i][2 + jj] *= alpha;
-          }
-        }
-      }
-    // ---- P (transposed into a B fragment) and PV
+      for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt], x0, x1, x2, x3, qf[nt][ks][0], qf[nt][ks][1]);
+    }
 #pragma unroll
-    for (int u = 0; u < MTU; ++u) {
-      const int mt = mt0 + u;
-      uint32_t pb[NT][2];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float pr[4];
+      for (int c = 0; c < 4; ++c) sc[nt][mt][c] = d[nt][c] * score_scale;
+  }
+  // ---- window mask: slot -> position through the newest slot
 #pragma unroll
-        for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[nt][u][c] - muse[nt][c & 1]);
-        l[nt][0] += pr[0] + pr[2];
-        l[nt][1] += pr[1] + pr[3];
-        pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
-        pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
-      }
-      const uint8_t* Vs = st + kPage * kRec8;
-      const int qi = lane >> 3, r8 = lane & 7;
+  for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int cprime = 2 * cc + (qi >> 1), th = qi & 1;
-        const int slot = 16 * mt + 8 * th + r8;
-        uint32_t rr[4];
-        ldsm_x4_trans(rr, smem_addr(Vs + slot * kRec8 + 16 * (cprime ^ r8)));
+    for (int hh = 0; hh < 2; ++hh) {
+      const int slot = u * kUnit + 16 * mt + g + 8 * hh;
+      int back = slot_last - slot;
+      if (back < 0) back += cap;
+      const int pos = p_last - back;
 #pragma unroll
-        for (int ci = 0; ci < 2; ++ci) {
-          const uint32_t y0 = prmt(rr[2 * ci], 0u, 0x3120u);
-          const uint32_t y1 = prmt(rr[2 * ci + 1], 0u, 0x3120u);
-          const uint32_t v0 = e4m3x2_to_f16x2(y0 & 0xFFFFu), v1 = e4m3x2_to_f16x2(y0 >> 16);
-          const uint32_t v2 = e4m3x2_to_f16x2(y1 & 0xFFFFu), v3 = e4m3x2_to_f16x2(y1 >> 16);
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt][2 * cc + ci], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+        for (int jj = 0; jj < 2; ++jj)
+          if (pos < lim_lo[nt][jj] || pos > lim_hi[nt][jj]) sc[nt][mt][2 * hh + jj] = -INFINITY;
+    }
+  // ---- online softmax
+  float muse[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      float mx = fmaxf(fmaxf(sc[nt][0][jj], sc[nt][0][2 + jj]), fmaxf(sc[nt][1][jj], sc[nt][1][2 + jj]));
+      mx = warp_max_g(mx);
+      const float mnew = fmaxf(m[nt][jj], mx);
+      muse[nt][jj] = mnew == -INFINITY ? 0.0f : mnew;
+      const float alpha = fast_exp2(m[nt][jj] - muse[nt][jj]);
+      m[nt][jj] = mnew;
+      if (alpha != 1.0f) {
+        l[nt][jj] *= alpha;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[nt][i][jj] *= alpha;
+          acc[nt][i][2 + jj] *= alpha;
         }
       }
     }
+  // ---- P (transposed into a B fragment) and PV
+  const uint8_t* Vs = st + kHalf;
+  const int qi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float pr[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[nt][mt][c] - muse[nt][c & 1]);
+      l[nt][0] += pr[0] + pr[2];
+      l[nt][1] += pr[1] + pr[3];
+      pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
+      pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int cprime = 2 * cc + (qi >> 1), th = qi & 1;
+      const int slot = 16 * mt + 8 * th + r8;
+      uint32_t rr[4];
+      ldsm_x4_trans(rr, smem_addr(Vs + slot * kRec8 + 16 * (cprime ^ r8)));
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci) {
+        const uint32_t y0 = prmt(rr[2 * ci], 0u, 0x3120u);
+        const uint32_t y1 = prmt(rr[2 * ci + 1], 0u, 0x3120u);
+        const uint32_t v0 = e4m3x2_to_f16x2(y0 & 0xFFFFu), v1 = e4m3x2_to_f16x2(y0 >> 16);
+        const uint32_t v2 = e4m3x2_to_f16x2(y1 & 0xFFFFu), v3 = e4m3x2_to_f16x2(y1 >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt][2 * cc + ci], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+      }
+    }
   }
+}
+
+// Issues the two bulk copies of unit u of this (sequence, KV head) into stage `st`.
+__device__ __forceinline__ void load_unit(uint8_t* st, const uint8_t* seg, int u, uint64_t* bar, uint64_t pol) {
+  const uint8_t* blk = seg + (size_t)(u >> 1) * kBlk + (u & 1) * kHalf;
+  mbar_arrive_expect_tx(bar, kStg);
+  bulk_g2s(st, blk, kHalf, bar, pol);
+  bulk_g2s(st + kHalf, blk + kPage * kRec8, kHalf, bar, pol);
 }
 
 template <int NT>
@@ -239,18 +255,20 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   const int pair = blockIdx.x / p.cs;  // (sequence, KV head) of this cluster
   const int b = pair / p.Hkv, h = pair - (pair / p.Hkv) * p.Hkv;
   const int stream = rank * p.nws + ws, nstream = p.cs * p.nws;
-  const int nb = stream < p.nblk ? (p.nblk - 1 - stream) / nstream + 1 : 0;  // blocks of this stream
-  uint8_t* wst = smem + (size_t)warp * p.nst * kBlk;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + swa_bar_offset(nw, p.nst));
+  const int nu = stream < p.nunits ? (p.nunits - 1 - stream) / nstream + 1 : 0;  // units of this stream
+  const SwaSmem L(nw, p.nst, NT, p.cs, p.rows_pad);
+  uint8_t* wst = smem + (size_t)warp * p.nst * kStg;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* wfull = bars + warp * p.nst;
   uint64_t* recv_bar = bars + nw * p.nst;
-  float* recv = reinterpret_cast<float*>(smem + swa_recv_offset(nw, p.nst));
+  float* part = reinterpret_cast<float*>(smem + L.part);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
   uint8_t* seg = const_cast<uint8_t*>(p.ring) + (size_t)pair * p.nblk * kBlk;
 
   // ---- prologue, which may overlap the previous grid on the stream: barriers, and L2
-  // prefetches of this stream's ring blocks and of the query and appended rows (L2 is
-  // coherent, so a grid still writing them cannot leave stale copies). Nothing is read
-  // before griddep_wait().
+  // prefetches of this stream's units and of the query and appended rows (L2 is coherent,
+  // so a grid still writing them cannot leave stale copies). Nothing is read before
+  // griddep_wait().
   const size_t rb = (size_t)kD * (p.bf16 ? 2 : 4);  // bytes per q / k / v row
   if (lane == 0) {
     for (int s = 0; s < p.nst; ++s) mbar_init(&wfull[s], 1);
@@ -261,7 +279,12 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     fence_barrier_init();
     fence_proxy_async_shared();
     if (tg == 0)
-      for (int i = 0; i < nb; ++i) prefetch_l2_bulk(seg + (size_t)(stream + i * nstream) * kBlk, kBlk);
+      for (int i = 0; i < nu; ++i) {
+        const int u = stream + i * nstream;
+        const uint8_t* blk = seg + (size_t)(u >> 1) * kBlk + (u & 1) * kHalf;
+        prefetch_l2_bulk(blk, kHalf);
+        prefetch_l2_bulk(blk + kPage * kRec8, kHalf);
+      }
     if (warp == 0 && rank == 0) {
       prefetch_l2(p.pos0 + b);
       for (int r = 0; r < p.S; ++r)  // the G query rows of this KV head are contiguous
@@ -281,10 +304,8 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   // ---- this warp's first copies (L2 hits when the prefetch had time to land)
   if (lane == 0) {
     const uint64_t pol = policy_evict_first();
-    for (int i = 0; i < min(p.nst, nb); ++i) {
-      mbar_arrive_expect_tx(&wfull[i], kBlk);
-      bulk_g2s(wst + (size_t)i * kBlk, seg + (size_t)(stream + i * nstream) * kBlk, kBlk, &wfull[i], pol);
-    }
+    for (int i = 0; i < min(p.nst, nu); ++i)
+      load_unit(wst + (size_t)i * kStg, seg, stream + i * nstream, &wfull[i], pol);
   }
   __syncwarp();
 
@@ -349,17 +370,17 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     }
   }
 
-  // ---- appended rows that fall in this stream's blocks: encode now (the loads overlap the copies)
+  // ---- appended rows that fall in this stream's units: encode now (the loads overlap the copies)
   uint32_t code[8][2];
-  uint32_t have = 0;  // bit 2 r + which: code[r][which] is valid and belongs to one of my blocks
+  uint32_t have = 0;  // bit 2 r + which: code[r][which] is valid and belongs to one of my units
   if (p.k_new != nullptr) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       code[r][0] = code[r][1] = 0;
       if (r >= p.S) continue;
       const int slot = (c0 + r) % p.cap;
-      const int j = slot / kPage;
-      if (j < stream || (j - stream) % nstream != 0) continue;
+      const int u = slot / kUnit;
+      if (u < stream || (u - stream) % nstream != 0) continue;
       const size_t row = ((size_t)b * p.S + r) * p.Hkv + h;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -371,9 +392,9 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
         }
         code[r][which] = fp8_encode4(x, which ? p.v_scale : p.k_scale);
         have |= 1u << (2 * r + which);
-        if (tg == 0)  // the ring copy for later steps, written once per block
-          *reinterpret_cast<uint32_t*>(seg + (size_t)j * kBlk + which * kPage * kRec8 + fp8_lane_offset(slot, lane)) =
-              code[r][which];
+        if (tg == 0)  // the ring copy for later steps, written once per unit
+          *reinterpret_cast<uint32_t*>(seg + (size_t)(slot / kPage) * kBlk + which * kPage * kRec8 +
+                                       fp8_lane_offset(slot, lane)) = code[r][which];
       }
     }
   }
@@ -392,52 +413,50 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       for (int c = 0; c < 4; ++c) acc[nt][i][c] = 0.0f;
   }
 
-  int done = 0;  // blocks consumed
-  for (int i = 0; i < nb; ++i) {
+  int done = 0;  // units consumed
+  for (int i = 0; i < nu; ++i) {
     const int s = i % p.nst;
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&wfull[s], (uint32_t)(i / p.nst) & 1u));
     if (!ok) {
       if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
       break;
     }
-    uint8_t* st = wst + (size_t)s * kBlk;
-    const int j = stream + i * nstream;
+    uint8_t* st = wst + (size_t)s * kStg;
+    const int u = stream + i * nstream;
     if (have) {
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         if (r >= p.S) break;
         const int slot = (c0 + r) % p.cap;
-        if (slot / kPage != j) continue;
+        if (slot / kUnit != u) continue;
 #pragma unroll
         for (int which = 0; which < 2; ++which)
           if (have >> (2 * r + which) & 1u)
-            *reinterpret_cast<uint32_t*>(st + which * kPage * kRec8 + fp8_lane_offset(slot, lane)) = code[r][which];
+            *reinterpret_cast<uint32_t*>(st + which * kHalf + unit_lane_offset(slot, lane)) = code[r][which];
       }
       __syncwarp();
     }
-    attend_block<NT>(st, j, p_last, slot_last, p.cap, p.score_scale, qf, lim_lo, lim_hi, m, l, acc, lane);
+    attend_unit<NT>(st, u, p_last, slot_last, p.cap, p.score_scale, qf, lim_lo, lim_hi, m, l, acc, lane);
     done = i + 1;
     __syncwarp();
-    if (lane == 0 && i + p.nst < nb) {  // refill this stage with the stream's block i + nst
+    if (lane == 0 && i + p.nst < nu) {  // refill this stage with the stream's unit i + nst
       fence_proxy_async_shared();
-      mbar_arrive_expect_tx(&wfull[s], kBlk);
-      bulk_g2s(st, seg + (size_t)(j + p.nst * nstream) * kBlk, kBlk, &wfull[s], policy_evict_first());
+      load_unit(st, seg, u + p.nst * nstream, &wfull[s], policy_evict_first());
     }
   }
-  if (done < nb && lane == 0) {  // gave up: let the copies still in flight land before leaving
-    for (int i = done; i < min(nb, done + p.nst); ++i)
+  if (done < nu && lane == 0) {  // gave up: let the copies still in flight land before leaving
+    for (int i = done; i < min(nu, done + p.nst); ++i)
       if (!mbar_wait_bounded(&wfull[i % p.nst], (uint32_t)(i / p.nst) & 1u)) break;
   }
 
-  // ---- this stream's partial for its tile group's rows, into its own first stage (all of
-  // the warp's copies have landed or been waited for)
-  float* part = reinterpret_cast<float*>(wst);
+  // ---- this stream's partial for its tile group's rows
+  float* mypart = part + (size_t)warp * NT * 8 * kRedStride;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       const float lt = warp_sum_g(l[nt][jj]);
-      float* dst = part + (8 * nt + 2 * t + jj) * kRedStride;
+      float* dst = mypart + (8 * nt + 2 * t + jj) * kRedStride;
       if (g == 0) {
         dst[0] = m[nt][jj];
         dst[1] = lt;
@@ -452,62 +471,84 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   __syncthreads();
   cluster_wait();  // CTA 0's receive barrier is initialised and armed
 
-  // ---- merge: item = (query row, 4 consecutive dims). Every CTA merges its own streams; the
+  // ---- merge: item = (query row, 8 consecutive dims). Every CTA merges its own streams; the
   // other CTAs push that into CTA 0, which merges the cluster and writes the output.
   const uint32_t bar0 = map_cluster(smem_addr(recv_bar), 0);
   const uint32_t recv0 = map_cluster(smem_addr(recv), 0);
   if (rank == 0 && !mbar_wait_bounded(recv_bar, 0) && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-  for (int e = threadIdx.x; e < p.R * 32; e += blockDim.x) {
-    const int row = e >> 5, c4 = e & 31;
+  for (int e = threadIdx.x; e < p.R * 16; e += blockDim.x) {
+    const int row = e >> 4, c8 = e & 15;
     const int tgr = (row >> 3) / NT;  // tile group holding this row
     const int rl = row - 8 * NT * tgr;
-    float M = -INFINITY;
-    for (int w2 = 0; w2 < p.nws; ++w2)
-      M = fmaxf(M, reinterpret_cast<const float*>(smem + (size_t)(w2 * p.ntg + tgr) * p.nst * kBlk)[rl * kRedStride]);
+    float mk[kMaxStreams];
+#pragma unroll
+    for (int w2 = 0; w2 < kMaxStreams; ++w2)
+      mk[w2] = w2 < p.nws ? part[((size_t)(w2 * p.ntg + tgr) * NT * 8 + rl) * kRedStride] : -INFINITY;
+    float M = mk[0];
+#pragma unroll
+    for (int w2 = 1; w2 < kMaxStreams; ++w2) M = fmaxf(M, mk[w2]);
     const float Mu = M == -INFINITY ? 0.0f : M;
     float lsum = 0.0f;
-    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int w2 = 0; w2 < p.nws; ++w2) {
-      const float* src = reinterpret_cast<const float*>(smem + (size_t)(w2 * p.ntg + tgr) * p.nst * kBlk) +
-                         rl * kRedStride;
-      const float wgt = fast_exp2(src[0] - Mu);
-      const float4 v = reinterpret_cast<const float4*>(src + 4)[c4];
-      lsum += wgt * src[1];
-      a.x += wgt * v.x;
-      a.y += wgt * v.y;
-      a.z += wgt * v.z;
-      a.w += wgt * v.w;
+    float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int w2 = 0; w2 < kMaxStreams; ++w2) {
+      if (w2 >= p.nws) break;
+      const float* src = part + ((size_t)(w2 * p.ntg + tgr) * NT * 8 + rl) * kRedStride;
+      const float wgt = fast_exp2(mk[w2] - Mu);
+      const float4 v0 = reinterpret_cast<const float4*>(src + 4)[2 * c8];
+      const float4 v1 = reinterpret_cast<const float4*>(src + 4)[2 * c8 + 1];
+      lsum = fmaf(wgt, src[1], lsum);
+      a[0] = fmaf(wgt, v0.x, a[0]);
+      a[1] = fmaf(wgt, v0.y, a[1]);
+      a[2] = fmaf(wgt, v0.z, a[2]);
+      a[3] = fmaf(wgt, v0.w, a[3]);
+      a[4] = fmaf(wgt, v1.x, a[4]);
+      a[5] = fmaf(wgt, v1.y, a[5]);
+      a[6] = fmaf(wgt, v1.z, a[6]);
+      a[7] = fmaf(wgt, v1.w, a[7]);
     }
     if (rank != 0) {
       const uint32_t dst = recv0 + 4u * (uint32_t)((rank * p.rows_pad + row) * kRedStride);
-      if (c4 == 0) st_async_f32x2(dst, M, lsum, bar0);
-      st_async_f32x4(dst + 16 + 16 * c4, a, bar0);
+      if (c8 == 0) st_async_f32x2(dst, M, lsum, bar0);
+      st_async_f32x4(dst + 16 + 32 * c8, make_float4(a[0], a[1], a[2], a[3]), bar0);
+      st_async_f32x4(dst + 32 + 32 * c8, make_float4(a[4], a[5], a[6], a[7]), bar0);
       continue;
     }
     // CTA 0: fold in the other CTAs' partials (relative to their own maxima)
+    float mr[kMaxCluster];
     float Mc = M;
-    for (int rr = 1; rr < p.cs; ++rr) Mc = fmaxf(Mc, recv[(rr * p.rows_pad + row) * kRedStride]);
+#pragma unroll
+    for (int rr = 1; rr < kMaxCluster; ++rr) {
+      mr[rr] = rr < p.cs ? recv[(rr * p.rows_pad + row) * kRedStride] : -INFINITY;
+      Mc = fmaxf(Mc, mr[rr]);
+    }
     const float Mcu = Mc == -INFINITY ? 0.0f : Mc;
     const float w0 = fast_exp2(M - Mcu);
     lsum *= w0;
-    a.x *= w0;
-    a.y *= w0;
-    a.z *= w0;
-    a.w *= w0;
-    for (int rr = 1; rr < p.cs; ++rr) {
-      const float* src = recv + (rr * p.rows_pad + row) * kRedStride;
-      const float wgt = fast_exp2(src[0] - Mcu);
-      const float4 v = reinterpret_cast<const float4*>(src + 4)[c4];
-      lsum += wgt * src[1];
-      a.x += wgt * v.x;
-      a.y += wgt * v.y;
-      a.z += wgt * v.z;
-      a.w += wgt * v.w;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] *= w0;
+#pragma unroll
+    for (int rr = 1; rr < kMaxCluster; ++rr) {
+      if (rr >= p.cs) break;
+      const float* sr = recv + (rr * p.rows_pad + row) * kRedStride;
+      const float wgt = fast_exp2(mr[rr] - Mcu);
+      const float4 v0 = reinterpret_cast<const float4*>(sr + 4)[2 * c8];
+      const float4 v1 = reinterpret_cast<const float4*>(sr + 4)[2 * c8 + 1];
+      lsum = fmaf(wgt, sr[1], lsum);
+      a[0] = fmaf(wgt, v0.x, a[0]);
+      a[1] = fmaf(wgt, v0.y, a[1]);
+      a[2] = fmaf(wgt, v0.z, a[2]);
+      a[3] = fmaf(wgt, v0.w, a[3]);
+      a[4] = fmaf(wgt, v1.x, a[4]);
+      a[5] = fmaf(wgt, v1.y, a[5]);
+      a[6] = fmaf(wgt, v1.z, a[6]);
+      a[7] = fmaf(wgt, v1.w, a[7]);
     }
     const int r = row / p.G, gi = row - (row / p.G) * p.G;
     const float inv = 1.0f / lsum;
-    float4* dst = reinterpret_cast<float4*>(p.out + (((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD) + c4;
-    *dst = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    float4* dst = reinterpret_cast<float4*>(p.out + (((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD) + 2 * c8;
+    dst[0] = make_float4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv);
+    dst[1] = make_float4(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv);
   }
 }
 
@@ -549,7 +590,7 @@ cudaError_t launch_swa_t(const SwaParams& p, size_t smem, cudaStream_t stream) {
 
 bool swa_cluster_path(int capacity, int S, int Hq, int Hkv) {
   const SwaPlan pl = make_plan(capacity, S, Hq, Hkv);
-  return pl.smem != 0 && pl.bps <= kMaxBlocksPerStream;
+  return pl.smem != 0 && pl.ups <= kMaxUnitsPerStream;
 }
 
 cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream) {
@@ -558,6 +599,7 @@ cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream) {
   p.ring = job.ring.data;
   p.cap = job.ring.capacity;
   p.nblk = p.cap / kPage;
+  p.nunits = p.cap / kUnit;
   p.window = job.window;
   p.B = job.B;
   p.S = job.S;
