@@ -220,6 +220,29 @@ class Stack256k:
         return 3 * len(self.int4) + (self.nL - len(self.int4))
 
 
+# DRAM counters of the int4 attention kernel from one ncu capture on the 64k workload (one
+# launch, cold cache): read + write bytes against its algorithmic bytes. The 256k call's traffic
+# is that ratio times its own algorithmic bytes (traffic grows with the pages read). The
+# counters belong to the kernel sources whose hash is recorded; after any change to them the
+# traffic is reported as null until a new capture.
+ATTN_CAPTURE = {"dram_read": 906237184, "dram_write": 3241984, "algorithmic": 905157248,
+                "sources": ["quantized_kv_cache_fold_gb300/csrc/kvq_attn.cu",
+                            "quantized_kv_cache_fold_gb300/csrc/kvq_device.cuh"],
+                "sources_sha256_16": "c42f398c69aa1d27"}
+
+
+def attn_traffic(call_bytes):
+    import hashlib
+    hs = hashlib.sha256()
+    for f in ATTN_CAPTURE["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            hs.update(fh.read())
+    if hs.hexdigest()[:16] != ATTN_CAPTURE["sources_sha256_16"]:
+        return None
+    c = ATTN_CAPTURE
+    return int(round(call_bytes * (c["dram_read"] + c["dram_write"]) / c["algorithmic"]))
+
+
 def run_64k(device, steps=30, warmup=3):
     """The 64k point: 32 sequences, context U[32768, 65536], one int4 layer, random page order."""
     import torch
@@ -263,6 +286,73 @@ def run_64k(device, steps=30, warmup=3):
                         int(w.ctx.mean()),
             "int4_call_us": round(t * 1e6, 1), "hbm_gbs": round(by / t / 1e9, 1),
             "session_layer_steps_per_s": round(w.B / t, 1), "algorithmic_bytes": by}
+
+
+def run_swa(device, steps=30, warmup=3):
+    """The 40 FP8 window-513 layers of the 256k step alone (8 sequences x 4 KV heads, 576-slot
+    rings, one query row, appended row inside the call), steps captured in one CUDA graph. A
+    small case (a few hundred MB) for profiling the window kernel."""
+    import torch
+
+    import synth
+    from quantized_kv_cache_fold_gb300 import kvq_fp8_append
+    from quantized_kv_cache_fold_gb300.runner import DecodeStack
+    from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, config
+
+    w = config(5)
+    B, S, nL = w.B, 1, w.swa_layers
+    st = DecodeStack(B, w.Hq, w.Hkv, S, 1, n_layers=nL, full_every=nL + 1, ring_capacity=w.ring_capacity,
+                     window=w.window, swa_k_scale=SWA_K_SCALE, swa_v_scale=SWA_V_SCALE, device=device)
+    stream = torch.cuda.current_stream().cuda_stream
+    cap = w.ring_capacity
+    for l in range(nL):
+        L = st.layers[l]
+        for b in range(B):
+            P = int(w.ctx[b])
+            k = torch.empty((cap, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+            v = torch.empty_like(k)
+            synth.kv_rows_device(w.seed, l, b, P - cap, cap, w.Hkv, "swa_k", True, k.data_ptr(), stream)
+            synth.kv_rows_device(w.seed, l, b, P - cap, cap, w.Hkv, "swa_v", True, v.data_ptr(), stream)
+            seq = torch.full((cap,), b, dtype=torch.int32, device=device)
+            pos = torch.arange(P - cap, P, dtype=torch.int32, device=device)
+            kvq_fp8_append(L.ring, k, v, seq, pos, SWA_K_SCALE, SWA_V_SCALE, st.dev_err)
+    total = warmup + steps
+    q = torch.empty((total, nL, B, S, w.Hq, 128), dtype=torch.bfloat16, device=device)
+    kn = torch.empty((total, nL, B, S, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+    vn = torch.empty_like(kn)
+    for buf, sid in ((q, synth.S_QUERIES), (kn, synth.S_KEYS), (vn, synth.S_VALUES)):
+        synth.normals_device(synth.key(w.seed + 1000, sid), 0, buf.numel(), buf.data_ptr(), None, True, stream)
+    pos0 = (torch.from_numpy(w.ctx.astype(np.int32)).to(device)[None, :] +
+            torch.arange(total, dtype=torch.int32, device=device)[:, None]).contiguous()
+    out = torch.empty((nL, B, S, w.Hq, 128), dtype=torch.float32, device=device)
+
+    def step(t):
+        for l in range(nL):
+            st.decode_layer(l, q[t, l], pos0[t], out[l], k_new=kn[t, l], v_new=vn[t, l])
+
+    for t in range(warmup):
+        step(t)
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(steps):
+                step(warmup + i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    assert st.read_error() == 0, f"device error word {st.read_error():#x}"
+    us = e0.elapsed_time(e1) * 1e3 / (steps * nL)
+    by = int(np.minimum(w.ctx + 1, w.window).sum()) * w.Hkv * 256
+    return {"workload": f"{nL} FP8 window-{w.window} layers of the 256k step: {B} sequences x {w.Hkv} KV heads, "
+                        f"{cap}-slot rings, 1 query row, appended row in the call",
+            "window_layer_us": round(us, 2), "bytes_per_layer": by, "layers_per_step": nL,
+            "window_us_per_step": round(us * nL, 1)}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -441,7 +531,11 @@ def run_kvq(args, rank, world, local):
                        "global_batch": 8 * world, "seq_len": int(bench_ctx0()), "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (11.4 GB of int4 cache read per step)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(frac, 4), "traffic": None, "peak_kind": peak_kind,
+                         "frac": round(frac, 4), "traffic": attn_traffic(int(np.mean(call_bytes))),
+                         "traffic_how": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the attention kernel "
+                                        "on the 64k workload, scaled to this call by algorithmic bytes "
+                                        "(profiles/attn_int4_64k.md); null once its sources changed",
+                         "peak_kind": peak_kind,
                          "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
                          "kernel": "kvq_decode_attn_int4 call (query prologue/append + split-K attention + combine kernels)",
                          "bytes_per_call": int(np.mean(call_bytes)), "avg_call_us": round(1e3 * np.mean(call_ms), 2)},
@@ -514,8 +608,9 @@ def main():
     ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--only", default=None, choices=["64k"],
-                    help="run only the 64k single-layer point (a small case for profiling)")
+    ap.add_argument("--only", default=None, choices=["64k", "swa"],
+                    help="run only the 64k single-layer int4 point or only the 40 window layers of the "
+                         "256k step (small cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -524,6 +619,10 @@ def main():
         import torch
         torch.cuda.set_device(local)
         print(json.dumps(run_64k(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+    elif args.only == "swa":
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_swa(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
