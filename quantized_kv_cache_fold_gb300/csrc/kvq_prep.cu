@@ -116,10 +116,30 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   const PrepJobs& j = p.j;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
-  // may overlap the previous grid on the stream: only an L2 prefetch of the matrix before the wait
+  // may overlap the previous grid on the stream: only L2 prefetches (the matrix, and the rows of
+  // this warp's first job) before the wait
+  const size_t rbytes = (size_t)kD * ((kv_role ? j.kv_bf16 : j.q_bf16) ? 2 : 4);
+  const int job0 = kv_role ? (int)blockIdx.x * kPrepWarps + warp
+                           : ((int)blockIdx.x - p.kv_blocks) * kPrepWarps + warp;
+  const bool has_job0 = job0 < (kv_role ? p.kv_jobs : p.q_jobs);
+  const uint8_t* r0a = nullptr;  // first job's rows (key and value, or query)
+  const uint8_t* r0b = nullptr;
+  if (has_job0) {
+    if (kv_role) {
+      r0a = static_cast<const uint8_t*>(j.k) + (size_t)job0 * rbytes;  // row index = token * Hkv + head = job
+      r0b = static_cast<const uint8_t*>(j.v) + (size_t)job0 * rbytes;
+    } else {
+      r0a = static_cast<const uint8_t*>(j.q) + (size_t)job0 * rbytes;
+    }
+  }
   if (threadIdx.x == 0) prefetch_l2_bulk(M, kD * kD * 4);
+  if (lane == 0 && r0a) prefetch_l2_bulk(r0a, (uint32_t)rbytes);
+  if (lane == 0 && r0b) prefetch_l2_bulk(r0b, (uint32_t)rbytes);
   griddep_wait();
   griddep_launch_dependents();
+  // the first job's rows into L1 while the matrix is staged in shared memory
+  if (r0a) prefetch_l1(r0a + (lane * rbytes) / 32);
+  if (r0b) prefetch_l1(r0b + (lane * rbytes) / 32);
   {
     // 16 independent 16-byte loads per thread, then the padded (conflict-free) shared stores
     constexpr int kPer = kD * kD / 4 / kPrepThreads;
