@@ -355,6 +355,139 @@ def run_swa(device, steps=30, warmup=3):
             "window_us_per_step": round(us * nL, 1)}
 
 
+def run_ab(device, steps=30, warmup=3):
+    """A/B of the full-attention formats on the 64k workload (32 sequences, context U[32768,
+    65536], one layer, outlier keys): rotated int4 (the method), unrotated int4 (R = I) and FP8
+    e4m3 keys and values (the stock format; full attention through the window kernel with the
+    window above the context). Per variant: bytes and time per call, and the output's relative L2
+    error against exact fp64 attention on unquantised keys and values (torch, sequence 0, all KV
+    heads). The FP8 variant's inputs g_k n(k) and g_q n(q) are prepared with torch."""
+    import torch
+
+    import synth
+    from quantized_kv_cache_fold_gb300 import kvq_fp8_append
+    from quantized_kv_cache_fold_gb300.runner import DecodeStack
+    from synth.workloads import config
+
+    w = config(3)
+    stream = torch.cuda.current_stream().cuda_stream
+    gq, gk = synth.gains(w.seed, 0)
+    gq_t, gk_t = torch.from_numpy(gq).to(device), torch.from_numpy(gk).to(device)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).to(device)
+    q = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.bfloat16, device=device)
+    synth.normals_device(synth.key(w.seed + 1000, synth.S_QUERIES), 0, q.numel(), q.data_ptr(), None, True, stream)
+    kn = torch.empty((w.B, 1, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+    vn = torch.empty_like(kn)
+    for b in range(w.B):
+        synth.kv_rows_device(w.seed, 0, b, int(w.ctx[b]), 1, w.Hkv, "k", True, kn[b].data_ptr(), stream)
+        synth.kv_rows_device(w.seed, 0, b, int(w.ctx[b]), 1, w.Hkv, "v", True, vn[b].data_ptr(), stream)
+
+    def nrm(x):  # n(x) in float32 over the last axis
+        x = x.float()
+        return x * torch.rsqrt((x * x).mean(dim=-1, keepdim=True) + 1e-6)
+
+    def timed(call):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms) * 1e3
+
+    # exact reference for sequence 0: softmax(g_q n(q) . g_k n(k) / sqrt(128)) v over positions 0..ctx0
+    L0 = int(w.ctx[0]) + 1
+    k0 = torch.empty((L0, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+    v0 = torch.empty_like(k0)
+    synth.kv_rows_device(w.seed, 0, 0, 0, L0, w.Hkv, "k", True, k0.data_ptr(), stream)
+    synth.kv_rows_device(w.seed, 0, 0, 0, L0, w.Hkv, "v", True, v0.data_ptr(), stream)
+    kx = (nrm(k0) * gk_t).double()
+    qx = (nrm(q[0, 0]) * gq_t).double()
+    exact = []
+    for h in range(w.Hkv):
+        qh = qx[h * w.G:(h + 1) * w.G]
+        p = torch.softmax(qh @ kx[:, h].T * 128 ** -0.5, dim=-1)
+        exact.append(p @ v0[:, h].double())
+
+    def err_of(out):
+        e = []
+        for h in range(w.Hkv):
+            o = out[0, 0, h * w.G:(h + 1) * w.G].double()
+            e.append(((o - exact[h]).norm(dim=-1) / exact[h].norm(dim=-1)).mean().item())
+        return float(np.mean(e))
+
+    res = {}
+    int4_bytes = int((w.ctx + 1).sum()) * w.Hkv * 136
+    for name, rotate in (("int4_rotated", True), ("int4_unrotated", False)):
+        perm = lambda l, n: synth.page_permutation(w.seed, 0, n)  # noqa: E731
+        st = DecodeStack(w.B, w.Hq, w.Hkv, 1, w.max_pages(), 1, 1, page_perm=perm, device=device)
+        st.set_int4_params(0, synth.rotation_seed(w.seed, 0), gq, gk, rotate=rotate)
+
+        def fill(b, p0, T, kb, vb):
+            synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "k", True, kb.data_ptr(), stream)
+            synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "v", True, vb.data_ptr(), stream)
+
+        st.prefill_int4(0, w.ctx, fill, chunk_tokens=32768)
+        out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device=device)
+        st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)  # the appended row, then time without appends
+        torch.cuda.synchronize()
+        err = err_of(out)
+        us = timed(lambda: st.decode_layer(0, q, ctx, out))
+        assert st.read_error() == 0
+        res[name] = {"bytes_per_call": int4_bytes, "call_us": round(us, 1),
+                     "hbm_gbs": round(int4_bytes / us / 1e3, 1), "rel_l2_err_vs_exact": round(err, 4)}
+        del st
+        torch.cuda.empty_cache()
+
+    # FP8 keys g_k n(k) and values v for the whole context, per-tensor scales max|x| / 448
+    cap = int(-(-(int(w.ctx.max()) + 1) // 64) * 64)
+    chunk = 32768
+    kbuf = torch.empty((chunk, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+    vbuf = torch.empty_like(kbuf)
+    kmax = vmax = 0.0
+    for b in range(w.B):
+        for p0 in range(0, int(w.ctx[b]) + 1, chunk):
+            T = min(chunk, int(w.ctx[b]) + 1 - p0)
+            synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "k", True, kbuf.data_ptr(), stream)
+            synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "v", True, vbuf.data_ptr(), stream)
+            kmax = max(kmax, (nrm(kbuf[:T]) * gk_t).abs().max().item())
+            vmax = max(vmax, vbuf[:T].float().abs().max().item())
+    ks8, vs8 = kmax / 448.0, vmax / 448.0
+    st = DecodeStack(w.B, w.Hq, w.Hkv, 1, 1, n_layers=1, full_every=2, ring_capacity=cap, window=cap,
+                     swa_k_scale=ks8, swa_v_scale=vs8, device=device)
+    ring = st.layers[0].ring
+    for b in range(w.B):
+        for p0 in range(0, int(w.ctx[b]), chunk):
+            T = min(chunk, int(w.ctx[b]) - p0)
+            synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "k", True, kbuf.data_ptr(), stream)
+            synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "v", True, vbuf.data_ptr(), stream)
+            seq = torch.full((T,), b, dtype=torch.int32, device=device)
+            pos = torch.arange(p0, p0 + T, dtype=torch.int32, device=device)
+            kvq_fp8_append(ring, (nrm(kbuf[:T]) * gk_t).contiguous(), vbuf[:T].float().contiguous(), seq, pos,
+                           ks8, vs8, st.dev_err)
+    q8 = (nrm(q) * gq_t).contiguous()
+    kn8 = (nrm(kn) * gk_t).contiguous()
+    vn8 = vn.float().contiguous()
+    out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device=device)
+    st.decode_layer(0, q8, ctx, out, k_new=kn8, v_new=vn8)
+    torch.cuda.synchronize()
+    err = err_of(out)
+    us = timed(lambda: st.decode_layer(0, q8, ctx, out))
+    assert st.read_error() == 0
+    fp8_bytes = int((w.ctx + 1).sum()) * w.Hkv * 256
+    res["fp8"] = {"bytes_per_call": fp8_bytes, "call_us": round(us, 1), "hbm_gbs": round(fp8_bytes / us / 1e3, 1),
+                  "rel_l2_err_vs_exact": round(err, 4)}
+    del st
+    torch.cuda.empty_cache()
+    return {"workload": "one full-attention layer, 32 sequences, context U[32768,65536] (mean %d), outlier keys"
+                        % int(w.ctx.mean()), "variants": res}
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(seconds_budget=20.0):
@@ -608,9 +741,9 @@ def main():
     ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--only", default=None, choices=["64k", "swa"],
-                    help="run only the 64k single-layer int4 point or only the 40 window layers of the "
-                         "256k step (small cases for profiling)")
+    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab"],
+                    help="run only the 64k single-layer int4 point, only the 40 window layers of the 256k "
+                         "step (small cases for profiling), or the A/B of full-layer formats (ab)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -619,6 +752,10 @@ def main():
         import torch
         torch.cuda.set_device(local)
         print(json.dumps(run_64k(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+    elif args.only == "ab":
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_ab(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
     elif args.only == "swa":
         import torch
         torch.cuda.set_device(local)

@@ -64,9 +64,10 @@ class DecodeStack:
     def swa_layers(self):
         return [i for i, L in enumerate(self.layers) if isinstance(L, SwaLayer)]
 
-    def set_int4_params(self, l, rot_seed, g_q, g_k):
-        """Build R from the seed and fold the gains (host), upload M_q and M_k."""
-        R, _ = kvq_build_rotation(rot_seed)
+    def set_int4_params(self, l, rot_seed, g_q, g_k, rotate=True):
+        """Build R from the seed and fold the gains (host), upload M_q and M_k. rotate=False folds
+        R = I instead: the unrotated int4 baseline (M_q = diag(g_q g_k), M_k = I)."""
+        R = kvq_build_rotation(rot_seed)[0] if rotate else np.eye(HEAD_DIM, dtype=np.float32)
         Mq, Mk = kvq_fold_qk(R, g_q, g_k)
         L = self.layers[l]
         L.R = R

@@ -19,14 +19,14 @@ from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, Workload, config
 pytestmark = pytest.mark.gpu
 
 
-def build_int4(w, layer, S, page_perm=True):
+def build_int4(w, layer, S, page_perm=True, rotate=True):
     max_pages = w.max_pages()
     perm = None
     if page_perm and w.page_order == "random":
         perm = lambda l, n: synth.page_permutation(w.seed, layer, n)  # noqa: E731
     st = DecodeStack(w.B, w.Hq, w.Hkv, S, max_pages, 1, 1, page_perm=perm)
     gq, gk = synth.gains(w.seed, layer)
-    st.set_int4_params(0, synth.rotation_seed(w.seed, layer), gq, gk)
+    st.set_int4_params(0, synth.rotation_seed(w.seed, layer), gq, gk, rotate=rotate)
 
     def fill(b, p0, T, kb, vb):
         device_kv(w, layer, b, p0, T, "k", kb[:T])
