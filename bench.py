@@ -488,6 +488,114 @@ def run_ab(device, steps=30, warmup=3):
                         % int(w.ctx.mean()), "variants": res}
 
 
+def run_capacity(device, budget_gb=160.0, steps=32, warmup=3):
+    """Capacity and throughput of a fixed KV pool, rotated int4 full layers against FP8 everywhere.
+
+    A pool of `budget_gb` holds as many sessions as fit at 64k and at 256k context, 50 layers per
+    session (10 full-attention layers: int4 pages, 136 B per token-head, or FP8 rings, 256 B; 40
+    window-513 layers: 576-slot FP8 rings). The pools are zero-filled (valid codes: zero scale,
+    offset and e4m3 values; the kernels' time does not depend on the values). Then the decode step
+    (all 50 layers, one query row, the new key/value row appended in each call) is timed for B
+    sessions, B from the pool's maximum down to one: each step is one replay of a one-step CUDA
+    graph bracketed by events, giving the median step time and the slowest tenth over the median."""
+    import torch
+
+    import synth
+    from quantized_kv_cache_fold_gb300.runner import DecodeStack
+    from synth.workloads import SWA_K_SCALE, SWA_V_SCALE
+
+    Hq, Hkv, G, n_full, n_swa, ring, window = 20, 4, 5, 10, 40, 576, 513
+    stream = torch.cuda.current_stream().cuda_stream
+    result = {"budget_gb": budget_gb, "points": []}
+    for ctx_len in (65536, 262144):
+        per_session = {
+            "int4": n_full * Hkv * ctx_len * 136 + n_swa * Hkv * ring * 256,
+            "fp8": n_full * Hkv * ctx_len * 256 + n_swa * Hkv * ring * 256,
+        }
+        for fmt in ("int4", "fp8"):
+            n_max = int(budget_gb * 1e9 // per_session[fmt])
+            max_pages = (ctx_len + 1 + 63) // 64
+            cap_full = max_pages * 64
+            if fmt == "int4":
+                full = DecodeStack(n_max, Hq, Hkv, 1, max_pages, n_layers=n_full, full_every=1, device=device)
+                for l in range(n_full):
+                    gq, gk = synth.gains(7, l)
+                    full.set_int4_params(l, synth.rotation_seed(7, l), gq, gk)
+            else:
+                full = DecodeStack(n_max, Hq, Hkv, 1, 1, n_layers=n_full, full_every=n_full + 1,
+                                   ring_capacity=cap_full, window=cap_full, swa_k_scale=SWA_K_SCALE,
+                                   swa_v_scale=SWA_V_SCALE, device=device)
+            swa = DecodeStack(n_max, Hq, Hkv, 1, 1, n_layers=n_swa, full_every=n_swa + 1, ring_capacity=ring,
+                              window=window, swa_k_scale=SWA_K_SCALE, swa_v_scale=SWA_V_SCALE, device=device)
+            held = torch.cuda.memory_allocated() / 1e9
+            q = torch.empty((n_max, 1, Hq, 128), dtype=torch.bfloat16, device=device)
+            kn = torch.empty((n_max, 1, Hkv, 128), dtype=torch.bfloat16, device=device)
+            vn = torch.empty_like(kn)
+            for buf, sid in ((q, synth.S_QUERIES), (kn, synth.S_KEYS), (vn, synth.S_VALUES)):
+                synth.normals_device(synth.key(7, sid), 0, buf.numel(), buf.data_ptr(), None, True, stream)
+            ctx = torch.full((n_max,), ctx_len, dtype=torch.int32, device=device)
+            out = torch.empty((n_max, 1, Hq, 128), dtype=torch.float32, device=device)
+            # halvings from the pool's maximum, plus the other format's maximum (equal-batch
+            # comparison) and 8 sessions (the 256k step's batch)
+            other = int(budget_gb * 1e9 // per_session["fp8" if fmt == "int4" else "int4"])
+            sizes = sorted({max(1, n_max >> i) for i in range(12)} | {b for b in (other, 8) if b <= n_max},
+                           reverse=True)
+            for B in sizes:
+                def step(B=B):
+                    # model order: every fifth layer is full attention
+                    for l in range(n_full + n_swa):
+                        st, idx = (full, l // 5) if l % 5 == 4 else (swa, l - (l + 1) // 5)
+                        st.decode_layer(idx, q[:B], ctx[:B], out[:B], k_new=kn[:B], v_new=vn[:B])
+                for _ in range(warmup):
+                    step()
+                torch.cuda.synchronize()
+                cs = torch.cuda.Stream()
+                cs.wait_stream(torch.cuda.current_stream())
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(cs):
+                    with torch.cuda.graph(g, stream=cs):
+                        step()
+                torch.cuda.synchronize()
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(steps)]
+                for e0, e1 in evs:
+                    e0.record()
+                    g.replay()
+                    e1.record()
+                torch.cuda.synchronize()
+                ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+                med = float(np.median(ms))
+                assert full.read_error() == 0 and swa.read_error() == 0
+                result["points"].append({
+                    "context": ctx_len, "format": fmt, "sessions_max": n_max, "bytes_per_session": per_session[fmt],
+                    "pool_gb_held": round(held, 1), "sessions": B, "ms_per_step": round(med, 3),
+                    "session_steps_per_s": round(B / med * 1e3, 1),
+                    "p90_over_median": round(float(np.percentile(ms, 90)) / med, 3)})
+                del g
+            del full, swa, q, kn, vn, out
+            torch.cuda.empty_cache()
+    pts = result["points"]
+
+    def at(ctx_len, fmt, B=None):
+        c = [p for p in pts if p["context"] == ctx_len and p["format"] == fmt]
+        return c[0] if B is None else min(c, key=lambda p: abs(p["sessions"] - B))
+
+    summary = {}
+    for ctx_len in (65536, 262144):
+        i4, f8 = at(ctx_len, "int4"), at(ctx_len, "fp8")
+        same_b = at(ctx_len, "int4", f8["sessions"])
+        summary[str(ctx_len)] = {
+            "sessions_int4": i4["sessions_max"], "sessions_fp8": f8["sessions_max"],
+            "sessions_gain": round(i4["sessions_max"] / f8["sessions_max"] - 1, 3),
+            "throughput_at_full_memory_gain": round(i4["session_steps_per_s"] / f8["session_steps_per_s"] - 1, 3),
+            "fp8_over_int4_step_time_at_equal_batch": round(f8["ms_per_step"] / same_b["ms_per_step"], 3)
+            if same_b["sessions"] == f8["sessions"] else None,
+            "equal_batch_sessions": f8["sessions"],
+            "worst_p90_over_median": max(p["p90_over_median"] for p in pts if p["context"] == ctx_len)}
+    result["summary"] = summary
+    return result
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(seconds_budget=20.0):
@@ -741,9 +849,10 @@ def main():
     ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab"],
+    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity"],
                     help="run only the 64k single-layer int4 point, only the 40 window layers of the 256k "
-                         "step (small cases for profiling), or the A/B of full-layer formats (ab)")
+                         "step (small cases for profiling), the A/B of full-layer formats (ab), or the "
+                         "capacity and throughput sweep of a fixed KV pool (capacity)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -752,6 +861,10 @@ def main():
         import torch
         torch.cuda.set_device(local)
         print(json.dumps(run_64k(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+    elif args.only == "capacity":
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_capacity(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
     elif args.only == "ab":
         import torch
         torch.cuda.set_device(local)
