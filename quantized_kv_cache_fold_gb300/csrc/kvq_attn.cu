@@ -190,6 +190,74 @@ __device__ __forceinline__ int out_dim(int mt, int row) {
   return 16 * mt + 2 * (row & 7) + (row >> 3);
 }
 
+// Producer warp of the split kernels: the 32 lanes resolve the source blocks of 32 consecutive
+// pages of the CTA's range [p0, p1) at once (block-table loads in parallel); lane 0 then issues
+// one bulk copy per page into the ring of `nst` stages, in order, as stages free (`empty`, one
+// phase per round), signalling `full`. A page whose block-table entry is out of range is
+// flagged and delivered as invalid (valid[s] = 0, no copy). Waits for its own copies before
+// returning.
+template <int FMT>
+__device__ __forceinline__ void produce_pages(const AttnParams& p, const int* pre, uint8_t* stages, uint64_t* full,
+                                              uint64_t* empty, volatile int* valid, volatile int* flags, int nst,
+                                              long long p0, long long p1, int lane) {
+  constexpr int kStage = FMT == 0 ? kStage4 : kStage8;
+  const uint64_t pol = policy_evict_first();
+  const int npages = (int)(p1 - p0);
+  int issued = 0;
+  int s = 0, f = 0;  // stage and fill round of the next page
+  for (int base = 0; base < npages; base += 32) {
+    const int mine = base + lane;
+    long long src = -1;  // byte offset of the page's block; -1 = invalid page
+    if (mine < npages) {
+      int b, h, lp, np;
+      decode_page(pre, p.B, p.Hkv, p0 + mine, b, h, lp, np);
+      if (FMT == 0) {
+        const int phys = p.block_table[(size_t)b * p.max_pages + lp];
+        if (phys >= 0 && phys < p.num_pages)
+          src = ((long long)phys * p.Hkv + h) * kStage4;
+        else
+          set_err(p.dev_err, KVQ_DEVERR_PAGE);
+      } else {
+        src = (((long long)b * p.Hkv + h) * (p.cap / kPage) + lp) * kStage8;
+      }
+    }
+    const int n = min(32, npages - base);
+    int halt = 0;
+    for (int j = 0; j < n; ++j) {
+      const long long sj = __shfl_sync(0xffffffffu, src, j);
+      if (lane == 0 && !halt) {
+        if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
+          set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+          flags[0] = 1;
+          halt = 1;
+        } else {
+          if (sj < 0) {
+            valid[s] = 0;
+            mbar_arrive(&full[s]);
+          } else {
+            valid[s] = 1;
+            mbar_arrive_expect_tx(&full[s], kStage);
+            bulk_g2s(stages + (size_t)s * kStage, p.blocks + sj, kStage, &full[s], pol);
+          }
+          ++issued;
+          if (++s == nst) {
+            s = 0;
+            ++f;
+          }
+        }
+      }
+    }
+    if (__shfl_sync(0xffffffffu, halt | flags[0], 0)) break;
+  }
+  // Do not retire while copies into this CTA's shared memory may be in flight.
+  if (lane == 0) {
+    for (int st = 0; st < nst && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / nst) * nst;
+      if (!mbar_wait_bounded(&full[st], (last / nst) & 1)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+    }
+  }
+}
+
 // Register caps: the int4 single-tile CTA (5 warps) must fit twice per SM, i.e. 3 warps per
 // SM sub-partition -> at most 170 registers.
 template <int FMT, int NT>
@@ -230,64 +298,8 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   const long long p1 = (long long)(blockIdx.x + 1) * P / n_eff;
 
   // ------------------------------------------------------------ producer warp
-  // The 32 lanes resolve the source blocks of 32 consecutive pages at once (block-table
-  // loads in parallel); lane 0 then issues one bulk copy per page, in order, as stages free.
   if (warp == nwc) {
-    const uint64_t pol = policy_evict_first();
-    const int npages = (int)(p1 - p0);
-    int issued = 0;
-    int s = 0, f = 0;  // stage and fill round of the next page
-    for (int base = 0; base < npages; base += 32) {
-      const int mine = base + lane;
-      long long src = -1;  // byte offset of the page's block; -1 = invalid page
-      if (mine < npages) {
-        int b, h, lp, np;
-        decode_page(pre, p.B, p.Hkv, p0 + mine, b, h, lp, np);
-        if (FMT == 0) {
-          const int phys = p.block_table[(size_t)b * p.max_pages + lp];
-          if (phys >= 0 && phys < p.num_pages)
-            src = ((long long)phys * p.Hkv + h) * kStage4;
-          else
-            set_err(p.dev_err, KVQ_DEVERR_PAGE);
-        } else {
-          src = (((long long)b * p.Hkv + h) * (p.cap / kPage) + lp) * kStage8;
-        }
-      }
-      const int n = min(32, npages - base);
-      int halt = 0;
-      for (int j = 0; j < n; ++j) {
-        const long long sj = __shfl_sync(0xffffffffu, src, j);
-        if (lane == 0 && !halt) {
-          if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
-            set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-            flags[0] = 1;
-            halt = 1;
-          } else {
-            if (sj < 0) {
-              valid[s] = 0;
-              mbar_arrive(&full[s]);
-            } else {
-              valid[s] = 1;
-              mbar_arrive_expect_tx(&full[s], kStage);
-              bulk_g2s(stages + (size_t)s * kStage, p.blocks + sj, kStage, &full[s], pol);
-            }
-            ++issued;
-            if (++s == nst) {
-              s = 0;
-              ++f;
-            }
-          }
-        }
-      }
-      if (__shfl_sync(0xffffffffu, halt | flags[0], 0)) break;
-    }
-    // Do not retire while copies into this CTA's shared memory may be in flight.
-    if (lane == 0) {
-      for (int st = 0; st < nst && st < issued; ++st) {
-        const int last = st + ((issued - 1 - st) / nst) * nst;
-        if (!mbar_wait_bounded(&full[st], (last / nst) & 1)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-      }
-    }
+    produce_pages<FMT>(p, pre, stages, full, empty, valid, flags, nst, p0, p1, lane);
     return;
   }
 
@@ -703,6 +715,352 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 
 }
 
+// ------------------------------------------------------------ many query rows per KV head
+// For S x G > 8 query rows (verify blocks) the rows span several 8-row tiles. Converting each
+// page's 4-bit codes once per tile would repeat the dominant ALU work, so here the conversion
+// is done once per page into shared f16 tiles that every tile warp reads with ldmatrix:
+//
+//   warp 0          producer: page-head blocks into kVStages int4 stages (produce_pages)
+//   kConvWarps      converters: K codes -> f16 biased (1024 + c / 1024 + 16c, see
+//                   unpack8_biased), V codes -> f16 centred (c - 8), per-token scale/offset ->
+//                   fp32, into one of kVBufs tile buffers; each converts an equal share of the
+//                   64 tokens
+//   T tile warps    one per 8 query rows: QK^T, online softmax and PV on tensor
+//                   cores over every page of the CTA's range, partial per segment and row
+//
+// A tile buffer holds K16 [64 tokens][16 chunks of 16 B], V16 the same, meta [64] float4. Chunk
+// j of a token row holds the eight f16 values of code word j (dims 8j .. 8j+7) in the order the
+// unpack produces them (dims 8j + {0,4,1,5,2,6,3,7}) and sits at chunk position j ^ (token & 7),
+// so the eight rows an ldmatrix 8x8 matrix reads fall in eight different bank groups.
+constexpr int kVStages = 8;
+constexpr int kVBufs = 3;
+constexpr int kTileRow = 256;                                // bytes per token row of an f16 tile
+constexpr int kVBuf = 2 * kPage * kTileRow + kPage * 16;     // K16, V16, meta
+#ifndef KVQ_VERIFY_CONV
+#define KVQ_VERIFY_CONV 2
+#endif
+// row tiles (8 query rows each) from which the shared-tile kernel is used
+#ifndef KVQ_VERIFY_MIN_TILES
+#define KVQ_VERIFY_MIN_TILES 4
+#endif
+constexpr int kConvWarps = KVQ_VERIFY_CONV;  // 64 / kConvWarps tokens each
+static_assert(64 % (2 * kConvWarps) == 0, "converter warps split the page's tokens in pairs of rows");
+
+struct VerifyLayout {
+  size_t bufs, full, empty, ready, freeb, valid, vvalid, pre, flags, total;
+  __host__ __device__ explicit VerifyLayout(int B) {
+    bufs = (size_t)kVStages * kStage4;  // int4 stages first, from offset 0
+    full = bufs + (size_t)kVBufs * kVBuf;
+    empty = full + 8 * kVStages;
+    ready = empty + 8 * kVStages;
+    freeb = ready + 8 * kVBufs;
+    valid = freeb + 8 * kVBufs;
+    vvalid = valid + 4 * kVStages;
+    pre = vvalid + 4 * kVBufs;
+    flags = align_up(pre + 4 * (size_t)(B + 1), 16);
+    total = flags + 16;
+  }
+};
+
+// Dim held by element e (0..7) of chunk j of a tile row.
+__device__ __forceinline__ int tile_dim(int j, int e) { return 8 * j + (e >> 1) + 4 * (e & 1); }
+
+__global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kernel(const AttnParams p) {
+  constexpr int kTokPerConv = kPage / kConvWarps;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const VerifyLayout L(p.B);
+  uint8_t* stages = smem;
+  uint8_t* bufs = smem + L.bufs;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  uint64_t* ready = reinterpret_cast<uint64_t*>(smem + L.ready);
+  uint64_t* freeb = reinterpret_cast<uint64_t*>(smem + L.freeb);
+  volatile int* valid = reinterpret_cast<volatile int*>(smem + L.valid);
+  volatile int* vvalid = reinterpret_cast<volatile int*>(smem + L.vvalid);
+  int* pre = reinterpret_cast<int*>(smem + L.pre);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.ntg;  // tile warps
+
+  griddep_wait();
+  griddep_launch_dependents();
+  build_prefix(p, 0, pre, flags);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConvWarps);
+    }
+    for (int b = 0; b < kVBufs; ++b) {
+      mbar_init(&ready[b], kConvWarps);
+      mbar_init(&freeb[b], T);
+    }
+  }
+  fence_barrier_init();
+  __syncthreads();
+
+  if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
+  const long long P = (long long)p.Hkv * pre[p.B];
+  const int n_eff = (int)min((long long)p.n_cta, P);
+  if ((int)blockIdx.x >= n_eff) return;
+  const long long p0 = (long long)blockIdx.x * P / n_eff;
+  const long long p1 = (long long)(blockIdx.x + 1) * P / n_eff;
+  const int npages = (int)(p1 - p0);
+
+  if (warp == 0) {
+    produce_pages<0>(p, pre, stages, full, empty, valid, flags, kVStages, p0, p1, lane);
+    return;
+  }
+
+  // ------------------------------------------------------------ converter warps
+  if (warp <= kConvWarps) {
+    const int cw = warp - 1;
+    for (int k = 0; k < npages; ++k) {
+      const int s = k % kVStages, b = k % kVBufs;
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(k / kVStages) & 1u));
+      if (ok && k >= kVBufs)  // the buffer's previous page has been released by every tile warp
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&freeb[b], (uint32_t)(k / kVBufs - 1) & 1u));
+      if (!ok) {
+        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+        flags[0] = 1;
+        break;
+      }
+      const uint8_t* st4 = stages + (size_t)s * kStage4;
+      uint8_t* buf = bufs + (size_t)b * kVBuf;
+      const int vpage = valid[s];
+      if (cw == 0 && lane == 0) vvalid[b] = vpage;
+      if (vpage) {
+        // lane = (row of a token pair, code word j); all loads of the share are issued first
+        constexpr int kIt = kTokPerConv / 2;
+        const int j = lane & 15;
+        uint32_t kw[kIt], vw[kIt];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+          const int tok = kTokPerConv * cw + 2 * it + (lane >> 4);
+          kw[it] = *reinterpret_cast<const uint32_t*>(st4 + tok * kRec4 + 4 * j);
+          // V records: 16-byte chunk c of slot s stored at chunk c ^ ((s >> 1) & 3)
+          vw[it] = *reinterpret_cast<const uint32_t*>(st4 + kPage * kRec4 + tok * kRec4 +
+                                                      16 * ((j >> 2) ^ ((tok >> 1) & 3)) + 4 * (j & 3));
+        }
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+          const int tok = kTokPerConv * cw + 2 * it + (lane >> 4);
+          uint32_t h[4];
+          unpack8_biased(kw[it], h);
+          *reinterpret_cast<uint4*>(buf + tok * kTileRow + 16 * (j ^ (tok & 7))) = make_uint4(h[0], h[1], h[2], h[3]);
+          unpack8_centred(vw[it], h);
+          *reinterpret_cast<uint4*>(buf + kPage * kTileRow + tok * kTileRow + 16 * (j ^ (tok & 7))) =
+              make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        if (lane < kTokPerConv) {
+          const int tok = kTokPerConv * cw + lane;
+          const uint32_t* meta = reinterpret_cast<const uint32_t*>(st4 + 2 * kPage * kRec4);
+          const uint32_t mk = meta[tok], mv = meta[kPage + tok];
+          const float sv = h2f_lo(mv);
+          reinterpret_cast<float4*>(buf + 2 * kPage * kTileRow)[tok] =
+              make_float4(h2f_lo(mk) * p.score_scale, h2f_hi(mk), sv, fmaf(8.0f, sv, h2f_hi(mv)));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ready[b]);
+        mbar_arrive(&empty[s]);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ tile warps
+  const int tg = warp - 1 - kConvWarps;
+  const int g = lane >> 2, t = lane & 3;
+  const int R = p.R, G = p.G;
+  long long seg_start = p0;
+  int k = 0;  // page index within the CTA's range
+  while (seg_start < p1) {
+    int b, h, lp0, np;
+    decode_page(pre, p.B, p.Hkv, seg_start, b, h, lp0, np);
+    const long long seg_end = min(p1, seg_start + (np - lp0));
+    const int seg = b * p.Hkv + h;
+    bool bad_ctx = false;
+    const int ctxb = eff_ctx(p, b, bad_ctx, 0);
+
+    // ---- query fragments of this warp's 8 rows. Element pairs of k-step ks: b0 <- dims
+    // (16 ks + t, 16 ks + t + 4), b1 <- (16 ks + 8 + t, 16 ks + 12 + t) (the tile's dim order);
+    // odd t meets high nibbles (1024 + 16c), so those query values are divided by 16 (exact).
+    uint32_t qf[8][2];
+    float qs[2], negbias[2];
+    int lim_hi[2];
+    {
+      const int nB = 8 * tg + g;
+      float qv[32];  // qv[4 ks + i] = q~[dim 16 ks + t + 4 i]
+      if (nB < R) {
+        const float* qrow = p.q_rot + (((size_t)b * p.S + nB / G) * p.Hq + h * G + nB % G) * kD;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) qv[m] = qrow[4 * m + t];
+      } else {
+#pragma unroll
+        for (int m = 0; m < 32; ++m) qv[m] = 0.0f;
+      }
+      float part = 0.0f, bsum = 0.0f;
+      const float hs = (t & 1) ? 0.0625f : 1.0f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t b0 = pack_f16x2(qv[4 * ks] * hs, qv[4 * ks + 1] * hs);
+        const uint32_t b1 = pack_f16x2(qv[4 * ks + 2] * hs, qv[4 * ks + 3] * hs);
+        qf[ks][0] = b0;
+        qf[ks][1] = b1;
+        bsum += (h2f_lo(b0) + h2f_hi(b0)) + (h2f_lo(b1) + h2f_hi(b1));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part += qv[4 * ks + i];
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+      bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        qs[j] = __shfl_sync(0xffffffffu, part, (2 * t + j) * 4) * p.score_scale;
+        negbias[j] = -1024.0f * __shfl_sync(0xffffffffu, bsum, (2 * t + j) * 4);
+        const int nC = 8 * tg + 2 * t + j;
+        lim_hi[j] = ctxb + (nC < R ? nC / G : 0);
+      }
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f}, ov[2] = {0.0f, 0.0f}, acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
+
+    for (long long pg = seg_start; pg < seg_end; ++pg, ++k) {
+      const int bi = k % kVBufs;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ready[bi], (uint32_t)(k / kVBufs) & 1u));
+      if (!ok) {
+        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+        flags[0] = 1;
+      }
+      if (__any_sync(0xffffffffu, flags[0] != 0)) break;
+      const int lp = lp0 + (int)(pg - seg_start);
+      if (vvalid[bi]) {
+        const uint8_t* buf = bufs + (size_t)bi * kVBuf;
+        const uint32_t Kt = smem_addr(buf), Vt = smem_addr(buf + kPage * kTileRow);
+        const float4* meta = reinterpret_cast<const float4*>(buf + 2 * kPage * kTileRow);
+        const bool need_mask = (lp + 1) * kPage > ctxb + 1;
+
+        // ---- scores for the page's 4 m-tiles (16 tokens each), chains interleaved over m-tiles
+        float d[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) d[u][c] = negbias[c & 1];
+        const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), achunk = lane >> 4;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t a[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int tok = 16 * u + arow, ch = 2 * ks + achunk;
+            ldsm_x4(a[u], Kt + tok * kTileRow + 16 * (ch ^ (tok & 7)));
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mma_16816(d[u], a[u][0], a[u][1], a[u][2], a[u][3], qf[ks][0], qf[ks][1]);
+        }
+        float sc[4][4], va[4][2], vb[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float4 mt = meta[16 * u + g + 8 * hh];
+            va[u][hh] = mt.z;
+            vb[u][hh] = mt.w;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) sc[u][2 * hh + j] = fmaf(d[u][2 * hh + j], mt.x, mt.y * qs[j]);
+          }
+        if (need_mask) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int pos = lp * kPage + 16 * u + g + 8 * hh;
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (pos > lim_hi[j]) sc[u][2 * hh + j] = -INFINITY;
+            }
+        }
+
+        // ---- online softmax
+        float muse[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mx = fmaxf(mx, fmaxf(sc[u][j], sc[u][2 + j]));
+          mx = warp_max_g(mx);
+          const float mnew = fmaxf(m[j], mx);
+          muse[j] = mnew == -INFINITY ? 0.0f : mnew;
+          const float alpha = fast_exp2(m[j] - muse[j]);
+          m[j] = mnew;
+          if (alpha != 1.0f) {
+            l[j] *= alpha;
+            ov[j] *= alpha;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc[i][j] *= alpha;
+              acc[i][2 + j] *= alpha;
+            }
+          }
+        }
+
+        // ---- P and PV (A = V^T from the f16 V tile with ldmatrix.trans)
+        const int vtok = (lane & 7) + 8 * (lane >> 4), vchunk = (lane >> 3) & 1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float pr[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[u][c] - muse[c & 1]);
+          l[0] += pr[0] + pr[2];
+          l[1] += pr[1] + pr[3];
+          ov[0] = fmaf(pr[0], vb[u][0], fmaf(pr[2], vb[u][1], ov[0]));
+          ov[1] = fmaf(pr[1], vb[u][0], fmaf(pr[3], vb[u][1], ov[1]));
+          const uint32_t pb0 = movmatrix_trans(pack_f16x2(pr[0] * va[u][0], pr[1] * va[u][0]));
+          const uint32_t pb1 = movmatrix_trans(pack_f16x2(pr[2] * va[u][1], pr[3] * va[u][1]));
+          const int tok = 16 * u + vtok;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const int ch = 2 * cc + vchunk;
+            uint32_t a[4];
+            ldsm_x4_trans(a, Vt + tok * kTileRow + 16 * (ch ^ (tok & 7)));
+            mma_16816(acc[cc], a[0], a[1], a[2], a[3], pb0, pb1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&freeb[bi]);
+    }
+
+    // ---- segment end: this warp's rows of the CTA partial
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float lt = warp_sum_g(l[j]);
+      const float ot = warp_sum_g(ov[j]);
+      const int row = 8 * tg + 2 * t + j;
+      if (row < R) {
+        float* dst = p.partials + ((size_t)(blockIdx.x + seg) * R + row) * kPartialStride;
+        if (g == 0) {
+          dst[0] = m[j];
+          dst[1] = lt;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          dst[2 + tile_dim(2 * i, g)] = acc[i][j] + ot;
+          dst[2 + tile_dim(2 * i + 1, g)] = acc[i][2 + j] + ot;
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, flags[0] != 0)) break;
+    seg_start = seg_end;
+  }
+}
+
 // One block per (segment, query row): merges the segment's CTA partials and normalises.
 template <int FMT>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
@@ -737,6 +1095,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
 
 struct DevCache {
   int sm = 0;
+  bool vattr = false;  // many-row kernel: shared-memory attribute set, occupancy cache
+  size_t vocc_smem = 0;
+  int vocc_threads = 0, vocc = 0;
   bool attr[2][4] = {{false}};
   size_t occ_smem[2][4] = {{0}};  // occupancy cache: last (smem, threads) queried per instantiation
   int occ_threads[2][4] = {{0}};
@@ -793,6 +1154,57 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
 }
 
+// int4 with S x G > 8 rows: the shared-tile kernel (T = row tiles), then the same combine.
+cudaError_t launch_verify(AttnParams& p, int T, long long p_max, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+  if (dc.sm == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    dc.sm = n > 0 ? n : 1;
+  }
+  p.ntg = T;
+  p.nkg = 1;
+  p.nstages = kVStages;
+  p.rows_pad = 8 * T;
+  const size_t smem = VerifyLayout(p.B).total;
+  const int threads = (1 + kConvWarps + T) * 32;
+  cudaError_t e = cudaSuccess;
+  if (!dc.vattr) {
+    e = cudaFuncSetAttribute(attn_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    dc.vattr = true;
+  }
+  if (dc.vocc_smem != smem || dc.vocc_threads != threads) {
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_verify_kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    dc.vocc = std::max(o, 1);
+    dc.vocc_smem = smem;
+    dc.vocc_threads = threads;
+  }
+  long long grid = std::min<long long>((long long)dc.sm * dc.vocc, kMaxCtas);
+  grid = std::max<long long>(1, std::min(grid, p_max));
+  p.n_cta = (int)grid;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_verify_kernel, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
+}
+
 }  // namespace
 
 size_t workspace_qrot_bytes(int B, int S, int Hq) { return align_up((size_t)B * S * Hq * kD * 4, 256); }
@@ -834,6 +1246,7 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p_max = (long long)p.Hkv * p.B * (p.cap / kPage);
   }
   const int ntiles = (p.R + 7) / 8;
+  if (job.fmt == 0 && ntiles >= KVQ_VERIFY_MIN_TILES) return launch_verify(p, ntiles, p_max, stream);
   int NT;
   if (ntiles <= 3) {
     NT = ntiles;

@@ -114,6 +114,14 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // Four 8x8 b16 matrices, transposed on load. Lane i gives the row address of row i%8 of
 // matrix i/8; register k of thread (g = lane/4, t = lane%4) receives element [2t][g] in
 // its low half and [2t+1][g] in its high half of matrix k.
+// Four 8x8 b16 matrices in the mma fragment layout (lanes 8i..8i+7 give the row addresses of
+// matrix i).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
