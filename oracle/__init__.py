@@ -52,6 +52,8 @@ def _bind(L):
     L.orc_rotation.argtypes = [u64, i32, vp, vp]
     L.orc_fold.argtypes = [vp, vp, vp, i32, vp, vp]
     L.orc_prologue.argtypes = [vp, vp, i64, f32, vp, i32]
+    L.orc_fold_fwht.argtypes = [vp, vp, vp, i32, vp, vp]
+    L.orc_prologue_fwht.argtypes = [vp, vp, i64, f32, vp, i32]
     L.orc_quantize_int4.argtypes = [vp, i64, vp, vp, vp, vp, i32]
     L.orc_dequant_int4.argtypes = [vp, vp, vp, i64, vp]
     L.orc_fp16_round_bits.argtypes = [f32, i32]
@@ -119,6 +121,25 @@ class Oracle:
         Mk = np.empty((n, n), np.float32)
         self.L.orc_fold(R32.ctypes.data, gq.ctypes.data, gk.ctypes.data, n, Mq.ctypes.data, Mk.ctypes.data)
         return Mq, Mk
+
+    def fold_fwht(self, s, gq, gk):
+        """Multipliers of the FWHT prologue: (w_q, w_k) = (fp32(s g_q g_k), s)."""
+        s = _c(s, np.int8)
+        gq, gk = _c(gq, np.float32), _c(gk, np.float32)
+        n = s.shape[0]
+        wq = np.empty(n, np.float32)
+        wk = np.empty(n, np.float32)
+        self.L.orc_fold_fwht(s.ctypes.data, gq.ctypes.data, gk.ctypes.data, n, wq.ctypes.data, wk.ctypes.data)
+        return wq, wk
+
+    def prologue_fwht(self, w, x, eps=1e-6):
+        """Second specification of the prologue: c * FWHT(w * n(x)), fp32 (see oracle.cpp)."""
+        w, x = _c(w, np.float32), _c(x, np.float32)
+        shp = x.shape
+        x2 = x.reshape(-1, 128)
+        y = np.empty_like(x2)
+        self.L.orc_prologue_fwht(w.ctypes.data, x2.ctypes.data, x2.shape[0], float(eps), y.ctypes.data, self.threads)
+        return y.reshape(shp)
 
     # -- codec
     def prologue(self, M, x, eps=1e-6):

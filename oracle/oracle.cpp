@@ -192,7 +192,8 @@ double e4m3_value(uint8_t c) {
 //   inv = 1 / sqrt(ss/128 + eps)       (IEEE division and square root)
 //   n_i = x_i * inv
 //   y_j = fma chain over i = 0..127 of M[j][i] * n_i, starting from 0
-void prologue_one(const float* M, const float* x, float eps, float* y) {
+// The normalisation n(x) of the specification above (shared by both prologue forms).
+void normalize_one(const float* x, float eps, float* n) {
   float t[32];
   for (int l = 0; l < 32; ++l) {
     const float* p = x + 4 * l;
@@ -209,13 +210,39 @@ void prologue_one(const float* M, const float* x, float eps, float* y) {
   }
   float ss = t[0];
   float inv = MUT(6) ? 1.0f : 1.0f / std::sqrt(ss / 128.0f + eps);
-  float n[128];
   for (int i = 0; i < 128; ++i) n[i] = x[i] * inv;
+}
+
+void prologue_one(const float* M, const float* x, float eps, float* y) {
+  float n[128];
+  normalize_one(x, eps, n);
   for (int j = 0; j < 128; ++j) {
     float acc = 0.0f;
     for (int i = 0; i < 128; ++i) acc = std::fmaf(M[j * 128 + i], n[i], acc);
     y[j] = acc;
   }
+}
+
+// Second codec specification: the same rotation through a fast Walsh-Hadamard transform.
+// Since R = H diag(s) / sqrt(128) (H Sylvester-ordered), R x = H (s * x) / sqrt(128) and
+// R diag(g) x = H (s * g * x) / sqrt(128), computed in fp32 as
+//   n = n(x) (as above);  u_i = w_i * n_i   (w = s for keys, w = fp32(s * g_q * g_k) for queries)
+//   for h = 1, 2, 4, ..., 64, for every i with (i & h) == 0:
+//       (u_i, u_{i+h}) <- (u_i + u_{i+h}, u_i - u_{i+h})
+//   y_j = c * u_j with c = fp32(1 / sqrt(128)).
+void prologue_fwht_one(const float* w, const float* x, float eps, float* y) {
+  float u[128];
+  normalize_one(x, eps, u);
+  for (int i = 0; i < 128; ++i) u[i] = w[i] * u[i];
+  for (int h = 1; h < 128; h <<= 1)
+    for (int i = 0; i < 128; ++i) {
+      if (i & h) continue;
+      const float a = u[i], b = u[i + h];
+      u[i] = a + b;
+      u[i + h] = MUT(13) ? b - a : a - b;
+    }
+  const float c = (float)(1.0 / std::sqrt(128.0));
+  for (int j = 0; j < 128; ++j) y[j] = MUT(14) ? u[j] : c * u[j];
 }
 
 bool all_finite(const float* x, int n) {
@@ -355,7 +382,31 @@ void orc_fold(const float* R32, const float* gq, const float* gk, int n, float* 
     }
 }
 
+// Multipliers of the FWHT prologue: w_k = s (keys), w_q = fp32(s * g_q * g_k) (the
+// product in fp64, rounded once), i.e. the diagonal that R = H diag(s)/sqrt(128) and the
+// gain fold put in front of H.
+void orc_fold_fwht(const int8_t* s, const float* gq, const float* gk, int n, float* wq, float* wk) {
+  for (int i = 0; i < n; ++i) {
+    const double sg = MUT(15) ? 1.0 : (double)s[i];
+    wq[i] = (float)(sg * (double)gq[i] * (double)gk[i]);
+    wk[i] = (float)s[i];
+  }
+}
+
 // ---------------------------------------------------------------- codec
+
+// y[v] = w-weighted FWHT prologue of x[v] (second specification); non-finite rows give NaN.
+void orc_prologue_fwht(const float* w, const float* x, int64_t nvec, float eps, float* y, int threads) {
+  for_range(nvec, threads, [&](int64_t a, int64_t b) {
+    for (int64_t v = a; v < b; ++v) {
+      if (!all_finite(x + v * 128, 128)) {
+        for (int i = 0; i < 128; ++i) y[v * 128 + i] = std::numeric_limits<float>::quiet_NaN();
+        continue;
+      }
+      prologue_fwht_one(w, x + v * 128, eps, y + v * 128);
+    }
+  });
+}
 
 // y[v] = M n(x[v]) with the fp32 specification above; x rows that are not all
 // finite give a row of NaN.

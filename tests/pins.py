@@ -120,6 +120,42 @@ def check_prologue(O):
     assert np.array_equal(ones, np.ones((1, 128), np.float32)), "n(c 1) = 1 for eps 0"
 
 
+def check_prologue_fwht(O):
+    """Second prologue specification, R n(x) = H (s n(x)) / sqrt(128) through the FWHT:
+    a one-hot input reproduces s_k times column k of the (independently built) Hadamard matrix
+    with equal magnitudes; random inputs stay within fp32 error of the fp64 products R n(x) and
+    R diag(g_q g_k) n(x); the multipliers are s and fp32(s g_q g_k)."""
+    H = O.hadamard(128).astype(np.int64)
+    for seed, k in ((5, 0), (5, 77), (31, 126)):
+        s = O.signs(seed, 128)
+        wq, wk = O.fold_fwht(s, np.ones(128, np.float32), np.ones(128, np.float32))
+        assert np.array_equal(wk, s.astype(np.float32)), "key multipliers are the signs"
+        x = np.zeros((1, 128), np.float32)
+        x[0, k] = 3.0
+        y = O.prologue_fwht(wk, x, 0.0)[0]
+        assert np.array_equal(np.sign(y).astype(np.int64), int(s[k]) * H[:, k]), "butterflies != Hadamard column"
+        assert np.all(np.abs(y) == np.abs(y[0])), "one-hot transform has unequal magnitudes"
+        assert abs(float(np.abs(y[0])) - 1.0) < 1e-6, "n(3 e_k) = sqrt(128) e_k, so |R n| = 1"
+    rng = _rng(6)
+    x = rng.standard_normal((32, 128)).astype(np.float32)
+    x[:, 3] *= 9.0
+    xd = x.astype(np.float64)
+    nd = xd / np.sqrt((xd ** 2).mean(1, keepdims=True) + 1e-6)
+    R64, _ = O.rotation(41)
+    s = O.signs(41, 128)
+    gq = rng.uniform(0.5, 1.5, 128).astype(np.float32)
+    gk = rng.uniform(0.5, 1.5, 128).astype(np.float32)
+    wq, wk = O.fold_fwht(s, gq, gk)
+    assert np.array_equal(wq, (s.astype(np.float64) * gq.astype(np.float64) * gk.astype(np.float64)).astype(np.float32))
+    for w, M in ((wk, R64), (wq, R64 * (gq.astype(np.float64) * gk.astype(np.float64))[None, :])):
+        y = O.prologue_fwht(w, x, 1e-6)
+        ref = nd @ M.T
+        assert np.abs(y - ref).max() <= 2e-6 * np.abs(ref).max(), "FWHT prologue far from its fp64 value"
+    y0 = O.prologue_fwht(wk, x, 0.0)
+    y4 = O.prologue_fwht(wk, x * np.float32(4.0), 0.0)
+    assert np.array_equal(y0, y4), "RMS norm must remove a power-of-two scale exactly"
+
+
 # ------------------------------------------------------------------ quantiser
 
 def _golden_quant_cases():
@@ -369,7 +405,8 @@ def check_claims(O):
 
 
 ALL_CHECKS = [
-    check_hadamard, check_signs, check_rotation, check_fold, check_prologue, check_quantizer_cases,
+    check_hadamard, check_signs, check_rotation, check_fold, check_prologue, check_prologue_fwht,
+    check_quantizer_cases,
     check_quantizer_bounds, check_quantizer_flags, check_fp16_converter, check_e4m3_converter,
     check_attention_closed_forms, check_attention_structure, check_attention_fp8, check_claims,
 ]

@@ -27,6 +27,9 @@ MUTATIONS = {
     10: "directed fp16 rounding ignores the sign",
     11: "fp16 offset rounded to nearest instead of down",
     12: "gains applied as diag(g) R instead of R diag(g)",
+    13: "FWHT butterfly difference taken the wrong way round",
+    14: "FWHT prologue without the 1/sqrt(128) scale",
+    15: "FWHT query multipliers without the signs",
     16: "softmax without max subtraction",
 }
 
