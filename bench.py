@@ -141,7 +141,7 @@ class ClockSampler:
 class Stack256k:
     """The 50-layer decode stack with synthetic caches and per-step inputs resident on the device."""
 
-    def __init__(self, steps_total, device):
+    def __init__(self, steps_total, device, prologue="matrix"):
         import torch
 
         import synth
@@ -162,7 +162,7 @@ class Stack256k:
         from quantized_kv_cache_fold_gb300 import kvq_fp8_append
         for l in st.int4_layers():
             gq, gk = synth.gains(w.seed, l)
-            st.set_int4_params(l, synth.rotation_seed(w.seed, l), gq, gk)
+            st.set_int4_params(l, synth.rotation_seed(w.seed, l), gq, gk, prologue=prologue)
 
             def fill(b, p0, T, kb, vb, l=l):
                 synth.kv_rows_device(w.seed, l, b, p0, T, w.Hkv, "k", True, kb.data_ptr(), stream)
@@ -651,7 +651,7 @@ def run_kvq(args, rank, world, local):
     device = f"cuda:{local}"
     K, W = args.steps, args.warmup
     total = K + W + 2 * min(K, 64)  # timed, warm-up and end-to-end steps each append one position
-    bench = Stack256k(total, device)
+    bench = Stack256k(total, device, prologue=args.prologue)
     peak, peak_kind = measured_peak()
 
     # ---- device-resident timed region: the K steps are captured once into a CUDA graph (as a
@@ -769,6 +769,7 @@ def run_kvq(args, rank, world, local):
             "vs_baseline": None, "dtype": "u4", "data": "synthetic",
             "config": {"workload": "decode step at 256k: 8 sequences x 262,144 context, 50 layers "
                                    "(10 rotated int4 + 40 FP8 window 513), 20/4 heads x 128, bf16 inputs, 1 query row",
+                       "prologue": args.prologue,
                        "global_batch": 8 * world, "seq_len": int(bench_ctx0()), "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (11.4 GB of int4 cache read per step)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -849,6 +850,9 @@ def main():
     ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--prologue", default="matrix", choices=["matrix", "fwht"],
+                    help="Q/K prologue of the int4 layers: the folded 128x128 matrices (default) or the "
+                         "fast Walsh-Hadamard form (second codec specification)")
     ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity"],
                     help="run only the 64k single-layer int4 point, only the 40 window layers of the 256k "
                          "step (small cases for profiling), the A/B of full-layer formats (ab), or the "

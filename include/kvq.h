@@ -129,6 +129,18 @@ kvq_status kvq_fold_qk(const float* R, const float* g_q, const float* g_k, int h
                        float* Mk_out);
 
 /*
+ * kvq_fold_qk_fwht -- the same rotation and gain fold for the fast Walsh-Hadamard prologue
+ * (kvq_rotate_quant_append_fwht, kvq_decode_attn_int4_fwht). Because R = H diag(s)/sqrt(128),
+ * R n = H (s n)/sqrt(128) and R diag(g_q g_k) n = H (s g_q g_k n)/sqrt(128): the folded form is
+ * one multiplier per channel in front of H.
+ *   s: host int8[128] of +1/-1 (from kvq_build_rotation); g_q, g_k: host float[128].
+ *   wq_out[i] = s[i]*g_q[i]*g_k[i] (fp64 product rounded once to fp32); wk_out[i] = s[i].
+ * Returns KVQ_ERR_INVALID_ARG for a NULL pointer or an s entry other than +1/-1.
+ */
+kvq_status kvq_fold_qk_fwht(const int8_t* s, const float* g_q, const float* g_k, int head_dim, float* wq_out,
+                            float* wk_out);
+
+/*
  * kvq_rotate_quant_append -- section "What we do": keys rotated (with their RMS norm) by
  * M_k and values unrotated, each quantised to 4-bit codes with fp16 scale/offset per
  * token and head, written into the page slot of (seq_ids[t], positions[t]).
@@ -152,6 +164,18 @@ kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk,
  * B sequences, S query rows each, num_q_heads query heads over num_kv_heads KV heads.
  * Returns 0 for arguments no call would accept.
  */
+/*
+ * kvq_rotate_quant_append_fwht -- kvq_rotate_quant_append with the second prologue
+ * specification: y = c FWHT(wk n(k)), c = fp32(1/sqrt(128)) (R n(k) up to rounding).
+ *   wk: device float[128], 16-byte aligned (kvq_fold_qk_fwht's wk_out).
+ * Arithmetic (bit-exact specification, fp32): n(k) as in kvq_rotate_quant_append; u_i = wk_i*n_i;
+ *   for h = 1, 2, 4, ..., 64 and every i with (i & h) == 0: (u_i, u_i+h) <- (u_i + u_i+h, u_i - u_i+h);
+ *   y_j = c*u_j; then the same quantiser. Values as in kvq_rotate_quant_append.
+ */
+kvq_status kvq_rotate_quant_append_fwht(const kvq_int4_cache* cache, const float* wk, const void* k, const void* v,
+                                        kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
+                                        float eps, int32_t* dev_err, kvq_stream_t stream);
+
 size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_heads);
 
 /*
@@ -178,6 +202,20 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
                                 const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
                                 void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
                                 kvq_stream_t stream);
+
+/*
+ * kvq_decode_attn_int4_fwht -- kvq_decode_attn_int4 with the FWHT prologue for the queries
+ * (q~ = c FWHT(wq n(q)) in the fp32 order of kvq_rotate_quant_append_fwht) and, when
+ * k_new/v_new are given, for the appended keys. The cache must have been filled with the FWHT
+ * prologue too (kvq_rotate_quant_append_fwht) for the scores to match R's rotation on both sides.
+ *   wq, wk: device float[128], 16-byte aligned (kvq_fold_qk_fwht); wk only read with k_new.
+ * All other arguments, limits and errors as kvq_decode_attn_int4.
+ */
+kvq_status kvq_decode_attn_int4_fwht(const kvq_int4_cache* cache, const float* wq, const float* wk, const void* q,
+                                     kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                     const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                     void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
+                                     kvq_stream_t stream);
 
 /*
  * kvq_fp8_append -- stock FP8 cache write of the sliding-window layers: code =

@@ -55,13 +55,17 @@ def _load():
     L.kvq_build_rotation.argtypes = [u64, i32, vp, vp]
     L.kvq_fold_qk.restype = i32
     L.kvq_fold_qk.argtypes = [vp, vp, vp, i32, vp, vp]
-    L.kvq_rotate_quant_append.restype = i32
-    L.kvq_rotate_quant_append.argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, vp, vp, f32, vp, vp]
+    L.kvq_fold_qk_fwht.restype = i32
+    L.kvq_fold_qk_fwht.argtypes = [vp, vp, vp, i32, vp, vp]
+    for name in ("kvq_rotate_quant_append", "kvq_rotate_quant_append_fwht"):
+        getattr(L, name).restype = i32
+        getattr(L, name).argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, vp, vp, f32, vp, vp]
     L.kvq_decode_workspace_bytes.restype = sz
     L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
-    L.kvq_decode_attn_int4.restype = i32
-    L.kvq_decode_attn_int4.argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, f32,
-                                       f32, vp, vp, sz, vp, vp, vp]
+    for name in ("kvq_decode_attn_int4", "kvq_decode_attn_int4_fwht"):
+        getattr(L, name).restype = i32
+        getattr(L, name).argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, f32,
+                                     f32, vp, vp, sz, vp, vp, vp]
     L.kvq_fp8_append.restype = i32
     L.kvq_fp8_append.argtypes = [ctypes.POINTER(Fp8Ring), vp, vp, i32, i32, vp, vp, f32, f32, vp, vp]
     L.kvq_decode_attn_int4_noalloc.restype = i32
@@ -174,12 +178,26 @@ def alloc_fp8_ring(num_seqs: int, num_kv_heads: int, capacity: int, device="cuda
 
 # ---------------------------------------------------------------- device calls
 
+def kvq_fold_qk_fwht(s, g_q, g_k):
+    """(w_q, w_k) = (s g_q g_k, s) as float32[128] numpy arrays: the multipliers of the FWHT prologue."""
+    s = np.ascontiguousarray(s, np.int8)
+    g_q = np.ascontiguousarray(g_q, np.float32)
+    g_k = np.ascontiguousarray(g_k, np.float32)
+    n = s.shape[0]
+    wq = np.empty(n, np.float32)
+    wk = np.empty(n, np.float32)
+    _check("kvq_fold_qk_fwht", lib.kvq_fold_qk_fwht(s.ctypes.data, g_q.ctypes.data, g_k.ctypes.data, n,
+                                                    wq.ctypes.data, wk.ctypes.data))
+    return wq, wk
+
+
 def kvq_rotate_quant_append(cache: Int4Cache, Mk, k, v, seq_ids, positions, dev_err, eps: float = 1e-6,
-                            stream=None):
+                            stream=None, fwht: bool = False):
+    """fwht=False: Mk is the 128x128 matrix; fwht=True: Mk is the multiplier vector w_k."""
     T = k.shape[0]
-    _check("kvq_rotate_quant_append",
-           lib.kvq_rotate_quant_append(ctypes.byref(cache), _ptr(Mk), _ptr(k), _ptr(v), _dtype_code(k), T,
-                                       _ptr(seq_ids), _ptr(positions), eps, _ptr(dev_err), _stream(stream)))
+    name = "kvq_rotate_quant_append_fwht" if fwht else "kvq_rotate_quant_append"
+    _check(name, getattr(lib, name)(ctypes.byref(cache), _ptr(Mk), _ptr(k), _ptr(v), _dtype_code(k), T,
+                                    _ptr(seq_ids), _ptr(positions), eps, _ptr(dev_err), _stream(stream)))
 
 
 def kvq_decode_workspace_bytes(B: int, S: int, num_q_heads: int, num_kv_heads: int) -> int:
@@ -187,11 +205,13 @@ def kvq_decode_workspace_bytes(B: int, S: int, num_q_heads: int, num_kv_heads: i
 
 
 def kvq_decode_attn_int4(cache: Int4Cache, Mq, Mk, q, ctx_len, out, workspace, dev_err, k_new=None, v_new=None,
-                         sm_scale: float = HEAD_DIM ** -0.5, eps: float = 1e-6, q_rot_out=None, stream=None):
+                         sm_scale: float = HEAD_DIM ** -0.5, eps: float = 1e-6, q_rot_out=None, stream=None,
+                         fwht: bool = False):
+    """fwht=False: Mq, Mk are the folded matrices; fwht=True: the multiplier vectors w_q, w_k."""
     B, S, Hq, _ = q.shape
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check("kvq_decode_attn_int4",
-           lib.kvq_decode_attn_int4(ctypes.byref(cache), _ptr(Mq), _ptr(Mk), _ptr(q), _dtype_code(q), B, S, Hq,
+    name = "kvq_decode_attn_int4_fwht" if fwht else "kvq_decode_attn_int4"
+    _check(name, getattr(lib, name)(ctypes.byref(cache), _ptr(Mq), _ptr(Mk), _ptr(q), _dtype_code(q), B, S, Hq,
                                     _ptr(ctx_len), _ptr(k_new), _ptr(v_new), sm_scale, eps, _ptr(out),
                                     _ptr(workspace), ws_bytes, _ptr(q_rot_out), _ptr(dev_err), _stream(stream)))
 

@@ -97,19 +97,32 @@ kvq_status kvq_fold_qk(const float* R, const float* g_q, const float* g_k, int h
   return KVQ_OK;
 }
 
-kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk, const void* k, const void* v,
-                                   kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
-                                   float eps, int32_t* dev_err, kvq_stream_t stream) {
+kvq_status kvq_fold_qk_fwht(const int8_t* s, const float* g_q, const float* g_k, int head_dim, float* wq_out,
+                            float* wk_out) {
+  if (head_dim != KVQ_HEAD_DIM) return KVQ_ERR_UNSUPPORTED;
+  if (!s || !g_q || !g_k || !wq_out || !wk_out) return KVQ_ERR_INVALID_ARG;
+  for (int i = 0; i < head_dim; ++i) {
+    if (s[i] != 1 && s[i] != -1) return KVQ_ERR_INVALID_ARG;
+    wq_out[i] = (float)((double)s[i] * (double)g_q[i] * (double)g_k[i]);  // exact in fp64, rounded once
+    wk_out[i] = (float)s[i];
+  }
+  return KVQ_OK;
+}
+
+static kvq_status append_impl(const kvq_int4_cache* cache, const float* Mk, const void* k, const void* v,
+                              kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions, float eps,
+                              int32_t* dev_err, kvq_stream_t stream, int fwht) {
   kvq_status st = check_int4_cache(cache);
   if (st != KVQ_OK) return st;
   if (dtype != KVQ_F32 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
   if (T < 0 || (long long)T * cache->num_kv_heads > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
   if (T == 0) return KVQ_OK;
   if (!Mk || !k || !v || !seq_ids || !positions || !dev_err) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(k, 16) || !aligned(v, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(Mk, 16)) return KVQ_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || std::isinf(eps)) return KVQ_ERR_INVALID_ARG;
   kvq::PrepJobs j{};
   j.cache = *cache;
+  j.fwht = fwht;
   j.Mk = Mk;
   j.k = k;
   j.v = v;
@@ -122,17 +135,29 @@ kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk,
   return from_cuda(kvq::launch_prep(j, (cudaStream_t)stream));
 }
 
+kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk, const void* k, const void* v,
+                                   kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
+                                   float eps, int32_t* dev_err, kvq_stream_t stream) {
+  return append_impl(cache, Mk, k, v, dtype, T, seq_ids, positions, eps, dev_err, stream, 0);
+}
+
+kvq_status kvq_rotate_quant_append_fwht(const kvq_int4_cache* cache, const float* wk, const void* k, const void* v,
+                                        kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
+                                        float eps, int32_t* dev_err, kvq_stream_t stream) {
+  return append_impl(cache, wk, k, v, dtype, T, seq_ids, positions, eps, dev_err, stream, 1);
+}
+
 size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_heads) {
   if (B < 1 || B > KVQ_MAX_SEQS || S < 1 || S > 8 || !heads_ok(num_q_heads, num_kv_heads, S)) return 0;
   return kvq::workspace_qrot_bytes(B, S, num_q_heads) +
          kvq::workspace_partials_bytes(B, S, num_q_heads, num_kv_heads);
 }
 
-kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
-                                kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
-                                const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
-                                void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
-                                kvq_stream_t stream) {
+static kvq_status decode_int4_impl(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                   kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                   const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                   void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
+                                   kvq_stream_t stream, int fwht) {
   kvq_status st = check_int4_cache(cache);
   if (st != KVQ_OK) return st;
   if (S < 1 || S > 8 || !heads_ok(num_q_heads, cache->num_kv_heads, S)) return KVQ_ERR_UNSUPPORTED;
@@ -140,8 +165,9 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
   if (dtype != KVQ_F32 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
   if (!Mq || !q || !ctx_len || !out || !workspace || !dev_err) return KVQ_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
-  if (k_new && (!Mk || !aligned(k_new, 16) || !aligned(v_new, 16))) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256)) return KVQ_ERR_INVALID_ARG;
+  if (k_new && (!Mk || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(Mk, 16))) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(Mq, 16))
+    return KVQ_ERR_INVALID_ARG;
   if (q_rot_out && !aligned(q_rot_out, 16)) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale) || !(eps >= 0.0f) || std::isinf(eps)) return KVQ_ERR_INVALID_ARG;
   if (workspace_bytes < kvq_decode_workspace_bytes(B, S, num_q_heads, cache->num_kv_heads))
@@ -154,6 +180,7 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
 
   kvq::PrepJobs j{};
   j.cache = *cache;
+  j.fwht = fwht;
   j.Mk = Mk;
   j.k = k_new;
   j.v = v_new;
@@ -186,6 +213,24 @@ kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, co
   a.partials = partials;
   a.dev_err = dev_err;
   return from_cuda(kvq::launch_attention(a, s));
+}
+
+kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
+                                kvq_stream_t stream) {
+  return decode_int4_impl(cache, Mq, Mk, q, dtype, B, S, num_q_heads, ctx_len, k_new, v_new, sm_scale, eps, out,
+                          workspace, workspace_bytes, q_rot_out, dev_err, stream, 0);
+}
+
+kvq_status kvq_decode_attn_int4_fwht(const kvq_int4_cache* cache, const float* wq, const float* wk, const void* q,
+                                     kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                     const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                     void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
+                                     kvq_stream_t stream) {
+  return decode_int4_impl(cache, wq, wk, q, dtype, B, S, num_q_heads, ctx_len, k_new, v_new, sm_scale, eps, out,
+                          workspace, workspace_bytes, q_rot_out, dev_err, stream, 1);
 }
 
 kvq_status kvq_fp8_append(const kvq_fp8_ring* ring, const void* k, const void* v, kvq_dtype dtype, int T,

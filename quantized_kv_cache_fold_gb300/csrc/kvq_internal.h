@@ -36,6 +36,9 @@ struct PrepJobs {
   float* q_rot_out;  // optional copy
   float eps;
   int32_t* dev_err;
+  // 0: the matrix prologue (Mk, Mq are 128x128 matrices); 1: the FWHT prologue (Mk, Mq are the
+  // 128 multipliers w_k = s, w_q = fp32(s g_q g_k) of kvq_fold_qk_fwht)
+  int fwht;
 };
 
 cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream);

@@ -10,7 +10,8 @@
 //
 // Every floating-point step uses explicit IEEE round-to-nearest intrinsics in the order
 // fixed by the specification in kvq.h, so the codes are bit-identical to a plain CPU
-// evaluation of the same formula.
+// evaluation of the same formula. Two prologue specifications: the 128x128 matrix product
+// (kvq_fold_qk) and the fast Walsh-Hadamard form (kvq_fold_qk_fwht), selected per call.
 
 #include <algorithm>
 
@@ -32,17 +33,48 @@ struct PrepParams {
   int q_jobs;
 };
 
-// y = M n(x). Lane l holds x[4l..4l+3] and returns y[l + 32u], u = 0..3.
-// Ms: shared [128][kMStride] (Ms[j*kMStride + i] = M[j][i]); nbuf: shared float[128] of this warp.
-__device__ __forceinline__ void prologue(const float* __restrict__ Ms, float* nbuf, const float (&x)[4], float eps,
-                                         int lane, float (&y)[4]) {
+// 1 / sqrt(mean(x^2) + eps) of the 128-vector spread over the warp (lane l holds
+// x[4l..4l+3]), in the specified order: per-lane fma chain, xor butterfly 16..1.
+__device__ __forceinline__ float norm_inv(const float (&x)[4], float eps) {
   float t = __fmul_rn(x[0], x[0]);
   t = __fmaf_rn(x[1], x[1], t);
   t = __fmaf_rn(x[2], x[2], t);
   t = __fmaf_rn(x[3], x[3], t);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
-  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, 128.0f), eps)));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, 128.0f), eps)));
+}
+
+// Second specification (FWHT prologue): y = c FWHT(w n(x)), c = fp32(1/sqrt(128)), butterflies
+// (u_i, u_i+h) -> (u_i + u_i+h, u_i - u_i+h) for h = 1, 2, ..., 64. Since R = H diag(s)/sqrt(128)
+// this is R n(x) for w = s and R diag(g_q g_k) n(x) for w = fp32(s g_q g_k). Lane l holds
+// elements 4l..4l+3 of x, w and y: h = 1, 2 inside the lane, h = 4..64 across lanes l ^ h/4.
+__device__ __forceinline__ void prologue_fwht(const float4 w, const float (&x)[4], float eps, int lane,
+                                              float (&y)[4]) {
+  const float inv = norm_inv(x, eps);
+  const float u0 = __fmul_rn(w.x, __fmul_rn(x[0], inv)), u1 = __fmul_rn(w.y, __fmul_rn(x[1], inv));
+  const float u2 = __fmul_rn(w.z, __fmul_rn(x[2], inv)), u3 = __fmul_rn(w.w, __fmul_rn(x[3], inv));
+  const float a0 = __fadd_rn(u0, u1), a1 = __fsub_rn(u0, u1), a2 = __fadd_rn(u2, u3), a3 = __fsub_rn(u2, u3);
+  float v[4] = {__fadd_rn(a0, a2), __fadd_rn(a1, a3), __fsub_rn(a0, a2), __fsub_rn(a1, a3)};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const bool upper = (lane & o) != 0;  // holds u_(i+h); the partner holds u_i
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float pv = __shfl_xor_sync(0xffffffffu, v[e], o);
+      v[e] = upper ? __fsub_rn(pv, v[e]) : __fadd_rn(v[e], pv);
+    }
+  }
+  const float c = __uint_as_float(0x3DB504F3u);  // fp32(1/sqrt(128))
+#pragma unroll
+  for (int e = 0; e < 4; ++e) y[e] = __fmul_rn(c, v[e]);
+}
+
+// y = M n(x). Lane l holds x[4l..4l+3] and returns y[l + 32u], u = 0..3.
+// Ms: shared [128][kMStride] (Ms[j*kMStride + i] = M[j][i]); nbuf: shared float[128] of this warp.
+__device__ __forceinline__ void prologue(const float* __restrict__ Ms, float* nbuf, const float (&x)[4], float eps,
+                                         int lane, float (&y)[4]) {
+  const float inv = norm_inv(x, eps);
   reinterpret_cast<float4*>(nbuf)[lane] =
       make_float4(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv), __fmul_rn(x[2], inv), __fmul_rn(x[3], inv));
   __syncwarp();
@@ -132,7 +164,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       r0a = static_cast<const uint8_t*>(j.q) + (size_t)job0 * rbytes;
     }
   }
-  if (threadIdx.x == 0) prefetch_l2_bulk(M, kD * kD * 4);
+  if (threadIdx.x == 0) prefetch_l2_bulk(M, j.fwht ? kD * 4 : kD * kD * 4);
   if (lane == 0 && r0a) prefetch_l2_bulk(r0a, (uint32_t)rbytes);
   if (lane == 0 && r0b) prefetch_l2_bulk(r0b, (uint32_t)rbytes);
   griddep_wait();
@@ -140,7 +172,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   // the first job's rows into L1 while the matrix is staged in shared memory
   if (r0a) prefetch_l1(r0a + (lane * rbytes) / 32);
   if (r0b) prefetch_l1(r0b + (lane * rbytes) / 32);
-  {
+  // the FWHT prologue needs only this lane's four multipliers; the matrix prologue stages M
+  const float4 w4 = j.fwht ? reinterpret_cast<const float4*>(M)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!j.fwht) {
     // 16 independent 16-byte loads per thread, then the padded (conflict-free) shared stores
     constexpr int kPer = kD * kD / 4 / kPrepThreads;
     float4 v[kPer];
@@ -190,13 +224,21 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       } else {
         float y[4];
-        prologue(Ms, nbuf, x, j.eps, lane, y);  // lane holds y[lane + 32u]
-        const Quant4 q = quantize(y);
         uint8_t* dst = blk + slot * kRec4;
+        Quant4 q;
+        if (j.fwht) {
+          prologue_fwht(w4, x, j.eps, lane, y);  // lane holds y[4 lane + e]: codes 4l..4l+3 = bytes 2l, 2l+1
+          q = quantize(y);
+          *reinterpret_cast<uint16_t*>(dst + 2 * lane) =
+              (uint16_t)((q.c[0] | (q.c[1] << 4)) | ((q.c[2] | (q.c[3] << 4)) << 8));
+        } else {
+          prologue(Ms, nbuf, x, j.eps, lane, y);  // lane holds y[lane + 32u]
+          q = quantize(y);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t hi = __shfl_down_sync(0xffffffffu, q.c[u], 1);
-          if ((lane & 1) == 0) dst[(lane + 32 * u) >> 1] = (uint8_t)(q.c[u] | (hi << 4));
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t hi = __shfl_down_sync(0xffffffffu, q.c[u], 1);
+            if ((lane & 1) == 0) dst[(lane + 32 * u) >> 1] = (uint8_t)(q.c[u] | (hi << 4));
+          }
         }
         if (lane == 0) {
           meta[slot] = q.meta;
@@ -226,6 +268,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       load_row4(j.q, j.q_bf16, (size_t)row, lane, x);
       if (!warp_all_finite(x) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       float y[4];
+      if (j.fwht) {  // lane holds q~[4 lane + e]
+        prologue_fwht(w4, x, j.eps, lane, y);
+        const float4 y4 = make_float4(y[0], y[1], y[2], y[3]);
+        reinterpret_cast<float4*>(j.q_rot + (size_t)row * kD)[lane] = y4;
+        if (j.q_rot_out) reinterpret_cast<float4*>(j.q_rot_out + (size_t)row * kD)[lane] = y4;
+        continue;
+      }
       prologue(Ms, nbuf, x, j.eps, lane, y);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {

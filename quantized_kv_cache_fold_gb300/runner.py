@@ -15,16 +15,17 @@ import numpy as np
 import torch
 
 from . import (HEAD_DIM, PAGE_SIZE, alloc_fp8_ring, alloc_int4_cache, alloc_workspace, kvq_build_rotation,
-               kvq_decode_attn_fp8_swa, kvq_decode_attn_int4, kvq_fold_qk, kvq_rotate_quant_append)
+               kvq_decode_attn_fp8_swa, kvq_decode_attn_int4, kvq_fold_qk, kvq_fold_qk_fwht, kvq_rotate_quant_append)
 
 
 @dataclass
 class Int4Layer:
     tensors: dict
     cache: object
-    Mq: torch.Tensor
-    Mk: torch.Tensor
+    Mq: torch.Tensor  # folded query matrix, or the FWHT multipliers w_q
+    Mk: torch.Tensor  # R, or the FWHT multipliers w_k = s
     R: np.ndarray
+    fwht: bool = False
 
 
 @dataclass
@@ -64,19 +65,29 @@ class DecodeStack:
     def swa_layers(self):
         return [i for i, L in enumerate(self.layers) if isinstance(L, SwaLayer)]
 
-    def set_int4_params(self, l, rot_seed, g_q, g_k, rotate=True):
+    def set_int4_params(self, l, rot_seed, g_q, g_k, rotate=True, prologue="matrix"):
         """Build R from the seed and fold the gains (host), upload M_q and M_k. rotate=False folds
-        R = I instead: the unrotated int4 baseline (M_q = diag(g_q g_k), M_k = I)."""
+        R = I instead: the unrotated int4 baseline (M_q = diag(g_q g_k), M_k = I).
+        prologue="fwht": the same rotation through the fast Walsh-Hadamard prologue (uploads the
+        multipliers w_q = s g_q g_k and w_k = s); set it before filling the layer's cache."""
+        L = self.layers[l]
+        if prologue == "fwht":
+            R, s = kvq_build_rotation(rot_seed)
+            wq, wk = kvq_fold_qk_fwht(s, g_q, g_k)
+            L.R, L.fwht = R, True
+            L.Mq = torch.from_numpy(wq).to(self.device)
+            L.Mk = torch.from_numpy(wk).to(self.device)
+            return
+        assert prologue == "matrix", prologue
         R = kvq_build_rotation(rot_seed)[0] if rotate else np.eye(HEAD_DIM, dtype=np.float32)
         Mq, Mk = kvq_fold_qk(R, g_q, g_k)
-        L = self.layers[l]
-        L.R = R
+        L.R, L.fwht = R, False
         L.Mq = torch.from_numpy(Mq).to(self.device)
         L.Mk = torch.from_numpy(Mk).to(self.device)
 
     def append_int4(self, l, k, v, seq_ids, positions, stream=None):
         L = self.layers[l]
-        kvq_rotate_quant_append(L.cache, L.Mk, k, v, seq_ids, positions, self.dev_err, stream=stream)
+        kvq_rotate_quant_append(L.cache, L.Mk, k, v, seq_ids, positions, self.dev_err, stream=stream, fwht=L.fwht)
 
     def prefill_int4(self, l, ctx, fill, chunk_tokens=16384, bf16=True):
         """Append positions 0..ctx[b]-1 of every sequence; fill(b, pos0, T, k_out, v_out) writes the
@@ -96,7 +107,7 @@ class DecodeStack:
         L = self.layers[l]
         if isinstance(L, Int4Layer):
             kvq_decode_attn_int4(L.cache, L.Mq, L.Mk, q, ctx, out, self.workspace, self.dev_err, k_new=k_new,
-                                 v_new=v_new, q_rot_out=q_rot_out, stream=stream)
+                                 v_new=v_new, q_rot_out=q_rot_out, stream=stream, fwht=L.fwht)
         else:
             kvq_decode_attn_fp8_swa(L.ring, q, ctx, L.window, L.k_scale, L.v_scale, out, self.workspace,
                                     self.dev_err, k_new=k_new, v_new=v_new, stream=stream)

@@ -131,10 +131,15 @@ def device_new_kv(w, layer, S, pos_of_b, which):
 
 # ---------------------------------------------------------------- oracle views
 
-def oracle_layer_params(O, w, layer):
-    """The oracle's own R, M_q, M_k for an int4 layer (from the same seeds)."""
-    _, R32 = O.rotation(synth.rotation_seed(w.seed, layer))
+def oracle_layer_params(O, w, layer, prologue="matrix"):
+    """The oracle's own R, M_q, M_k for an int4 layer (from the same seeds); for the FWHT
+    prologue ("fwht", w_q, w_k)."""
+    seed = synth.rotation_seed(w.seed, layer)
     gq, gk = synth.gains(w.seed, layer)
+    if prologue == "fwht":
+        wq, wk = O.fold_fwht(O.signs(seed, 128), gq, gk)
+        return "fwht", wq, wk
+    _, R32 = O.rotation(seed)
     Mq, Mk = O.fold(R32, gq, gk)
     return R32, Mq, Mk
 
@@ -142,16 +147,18 @@ def oracle_layer_params(O, w, layer):
 def oracle_int4_seq(O, w, layer, b, h, S, ctx_b, params=None):
     """Oracle codes of positions 0..ctx_b+S-1 and attention output of rows 0..S-1 for the G query
     heads of KV head h of sequence b. Returns (codes dict, q~ [S, G, 128], out [S, G, 128])."""
-    R32, Mq, Mk = params if params is not None else oracle_layer_params(O, w, layer)
+    params = params if params is not None else oracle_layer_params(O, w, layer)
+    fwht = isinstance(params[0], str) and params[0] == "fwht"  # ("fwht", w_q, w_k): second prologue specification
+    _, Mq, Mk = params
     Ltot = ctx_b + S
     k = host_rows(synth.kv_rows(w.seed, layer, b, 0, Ltot, w.Hkv, "k", w.bf16), w.bf16)[:, h]
     v = host_rows(synth.kv_rows(w.seed, layer, b, 0, Ltot, w.Hkv, "v", w.bf16), w.bf16)[:, h]
-    y = O.prologue(Mk, k)
+    y = O.prologue_fwht(Mk, k) if fwht else O.prologue(Mk, k)
     kc, ks, ko, kf = O.quantize_int4(y)
     vc, vs, vo, vf = O.quantize_int4(v)
     q = host_rows(synth.q_rows(w.seed, layer, b, ctx_b, S, w.Hq, w.bf16), w.bf16)
     qg = q[:, h * w.G:(h + 1) * w.G].reshape(-1, 128)
-    qt = O.prologue(Mq, qg)
+    qt = O.prologue_fwht(Mq, qg) if fwht else O.prologue(Mq, qg)
     vis = np.repeat(ctx_b + 1 + np.arange(S), w.G)
     out = O.attention_int4(qt, vis, kc, ks, ko, vc, vs, vo, SM)
     codes = {"kc": kc, "ks": ks, "ko": ko, "vc": vc, "vs": vs, "vo": vo, "kflags": kf, "vflags": vf}

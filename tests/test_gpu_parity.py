@@ -19,14 +19,14 @@ from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, Workload, config
 pytestmark = pytest.mark.gpu
 
 
-def build_int4(w, layer, S, page_perm=True, rotate=True):
+def build_int4(w, layer, S, page_perm=True, rotate=True, prologue="matrix"):
     max_pages = w.max_pages()
     perm = None
     if page_perm and w.page_order == "random":
         perm = lambda l, n: synth.page_permutation(w.seed, layer, n)  # noqa: E731
     st = DecodeStack(w.B, w.Hq, w.Hkv, S, max_pages, 1, 1, page_perm=perm)
     gq, gk = synth.gains(w.seed, layer)
-    st.set_int4_params(0, synth.rotation_seed(w.seed, layer), gq, gk, rotate=rotate)
+    st.set_int4_params(0, synth.rotation_seed(w.seed, layer), gq, gk, rotate=rotate, prologue=prologue)
 
     def fill(b, p0, T, kb, vb):
         device_kv(w, layer, b, p0, T, "k", kb[:T])
@@ -48,11 +48,11 @@ def run_int4_step(st, w, layer, S):
     return out.cpu().numpy(), qrot.cpu().numpy()
 
 
-def check_int4(orc, w, layer, S, seqs, heads=None, st=None):
-    st = st or build_int4(w, layer, S)
+def check_int4(orc, w, layer, S, seqs, heads=None, st=None, prologue="matrix"):
+    st = st or build_int4(w, layer, S, prologue=prologue)
     out, qrot = run_int4_step(st, w, layer, S)
     assert st.read_error() == 0, f"device error word {st.read_error():#x}"
-    params = oracle_layer_params(orc, w, layer)
+    params = oracle_layer_params(orc, w, layer, prologue)
     errs = []
     for b in seqs:
         cb = int(w.ctx[b])
@@ -171,6 +171,28 @@ def test_host_errors_raise():
     out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device="cuda")
     with pytest.raises(KvqError):
         st.decode_layer(0, q[:, :, :19].contiguous(), torch.zeros(2, dtype=torch.int32, device="cuda"), out)
+
+
+@pytest.mark.parametrize("S", [1, 5])
+def test_fwht_prologue(orc, S):
+    """The second prologue specification (fast Walsh-Hadamard form): codes, fp16 scale/offset
+    and q~ bit-exact with the oracle's FWHT prologue, attention within tolerance, for single rows
+    and a verify block with its rows appended in the call."""
+    w = Workload("fwht", 28, 3, 20, 4, S, np.array([0, 130, 2047]), True)
+    _, out, _ = check_int4(orc, w, 3, S, range(w.B), prologue="fwht")
+    assert np.isfinite(out).all()
+
+
+def test_fwht_and_matrix_prologues_agree(orc):
+    """Both specifications compute R n(k) and R diag(g_q g_k) n(q): their q~ agree to fp32 rounding."""
+    w = Workload("fwht-vs-matrix", 29, 2, 20, 4, 1, np.array([200, 900]), True)
+    qr = []
+    for prologue in ("matrix", "fwht"):
+        st = build_int4(w, 4, 1, prologue=prologue)
+        _, qrot = run_int4_step(st, w, 4, 1)
+        assert st.read_error() == 0
+        qr.append(qrot)
+    assert np.abs(qr[0] - qr[1]).max() <= 1e-5 * np.abs(qr[0]).max()
 
 
 # ---------------------------------------------------------------- FP8 sliding window
