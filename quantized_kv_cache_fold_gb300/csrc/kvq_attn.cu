@@ -405,12 +405,17 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
       }
     }
 
-    float m[NT][2], l[NT][2], ov[NT][2], acc[NT][8][4];
+    // Softmax state per accumulator row: m = exponent base (-inf until a finite score is seen),
+    // muse = the base used in the exponent (0 while m is -inf), thr = how far a score may exceed
+    // the base before it is moved (scores enter the exponent as s - muse).
+    float m[NT][2], muse[NT][2], thr[NT][2], l[NT][2], ov[NT][2], acc[NT][8][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         m[nt][j] = -INFINITY;
+        muse[nt][j] = 0.0f;
+        thr[nt][j] = -INFINITY;
         l[nt][j] = 0.0f;
         ov[nt][j] = 0.0f;
       }
@@ -516,7 +521,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                  sc[nt][u][c] = fmaf(d[nt][u][c], ka[u][c >> 1], kb[u][c >> 1] * qs[nt][c & 1]);
+                  sc[nt][u][c] = fmaf(d[nt][u][c], ka[u][c >> 1], fmaf(kb[u][c >> 1], qs[nt][c & 1], -muse[nt][c & 1]));
           } else {
 #pragma unroll
             for (int u = 0; u < MTU; ++u) {
@@ -544,7 +549,8 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) sc[nt][u][c] = d[nt][c] * p.score_scale;
+                for (int c = 0; c < 4; ++c)
+                  sc[nt][u][c] = fmaf(d[nt][c], p.score_scale, -muse[nt][c & 1]);
             }
           }
           if (need_mask) {
@@ -571,29 +577,52 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
           }
 
           // ---- online softmax update
-          float muse[NT][2];
+          // Lazy base: scores are already relative to muse. The base moves (to the running
+          // maximum, rescaling l, ov and acc) only when some score of the page exceeds it by
+          // more than 8, so P stays <= 2^8 and most pages skip the cross-lane maximum.
+          {
+            float mx[NT][2];
+            bool need = false;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              float mx = -INFINITY;
+              for (int j = 0; j < 2; ++j) {
+                float v = -INFINITY;
 #pragma unroll
-              for (int u = 0; u < MTU; ++u) mx = fmaxf(mx, fmaxf(sc[nt][u][j], sc[nt][u][2 + j]));
-              mx = warp_max_g(mx);
-              const float mnew = fmaxf(m[nt][j], mx);
-              muse[nt][j] = mnew == -INFINITY ? 0.0f : mnew;
-              const float alpha = fast_exp2(m[nt][j] - muse[nt][j]);
-              m[nt][j] = mnew;
-              if (alpha != 1.0f) {
-                l[nt][j] *= alpha;
-                ov[nt][j] *= alpha;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  acc[nt][i][j] *= alpha;
-                  acc[nt][i][2 + j] *= alpha;
-                }
+                for (int u = 0; u < MTU; ++u) v = fmaxf(v, fmaxf(sc[nt][u][j], sc[nt][u][2 + j]));
+                mx[nt][j] = v;
+                need |= v > thr[nt][j];
               }
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const float mt = warp_max_g(mx[nt][j]);
+                  const float mnew = fmaxf(m[nt][j], muse[nt][j] + mt);
+                  if (mnew != m[nt][j]) {
+                    const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
+                    const float alpha = fast_exp2(m[nt][j] - mu2);
+                    const float delta = muse[nt][j] - mu2;
+                    l[nt][j] *= alpha;
+                    ov[nt][j] *= alpha;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                      acc[nt][i][j] *= alpha;
+                      acc[nt][i][2 + j] *= alpha;
+                    }
+#pragma unroll
+                    for (int u = 0; u < MTU; ++u) {
+                      sc[nt][u][j] += delta;
+                      sc[nt][u][2 + j] += delta;
+                    }
+                    m[nt][j] = mnew;
+                    muse[nt][j] = mu2;
+                    thr[nt][j] = mnew == -INFINITY ? -INFINITY : 8.0f;
+                  }
+                }
             }
+          }
 
           // ---- P and PV
 #pragma unroll
@@ -604,14 +633,14 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
             for (int nt = 0; nt < NT; ++nt) {
               float pr[4];
 #pragma unroll
-              for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[nt][u][c] - muse[nt][c & 1]);
+              for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[nt][u][c]);
               l[nt][0] += pr[0] + pr[2];
               l[nt][1] += pr[1] + pr[3];
               if (FMT == 0) {
                 ov[nt][0] = fmaf(pr[0], vb[u][0], fmaf(pr[2], vb[u][1], ov[nt][0]));
                 ov[nt][1] = fmaf(pr[1], vb[u][0], fmaf(pr[3], vb[u][1], ov[nt][1]));
-                pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0] * va[u][0], pr[1] * va[u][0]));
-                pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2] * va[u][1], pr[3] * va[u][1]));
+                pb[nt][0] = movmatrix_trans(pack_f16x2_sat(pr[0] * va[u][0], pr[1] * va[u][0]));
+                pb[nt][1] = movmatrix_trans(pack_f16x2_sat(pr[2] * va[u][1], pr[3] * va[u][1]));
               } else {
                 pb[nt][0] = movmatrix_trans(pack_f16x2(pr[0], pr[1]));
                 pb[nt][1] = movmatrix_trans(pack_f16x2(pr[2], pr[3]));
@@ -925,7 +954,9 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
       }
     }
 
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f}, ov[2] = {0.0f, 0.0f}, acc[8][4];
+    // lazy exponent base, as in attn_kernel: m, muse, thr per accumulator row
+    float m[2] = {-INFINITY, -INFINITY}, muse[2] = {0.0f, 0.0f}, thr[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.0f, 0.0f}, ov[2] = {0.0f, 0.0f}, acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -973,7 +1004,7 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
             va[u][hh] = mt.z;
             vb[u][hh] = mt.w;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) sc[u][2 * hh + j] = fmaf(d[u][2 * hh + j], mt.x, mt.y * qs[j]);
+            for (int j = 0; j < 2; ++j) sc[u][2 * hh + j] = fmaf(d[u][2 * hh + j], mt.x, fmaf(mt.y, qs[j], -muse[j]));
           }
         if (need_mask) {
 #pragma unroll
@@ -987,25 +1018,42 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
             }
         }
 
-        // ---- online softmax
-        float muse[2];
+        // ---- online softmax (lazy base: moved only when a score exceeds it by more than 8)
+        {
+          float mx[2];
+          bool need = false;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float mx = -INFINITY;
+          for (int j = 0; j < 2; ++j) {
+            float v = -INFINITY;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) mx = fmaxf(mx, fmaxf(sc[u][j], sc[u][2 + j]));
-          mx = warp_max_g(mx);
-          const float mnew = fmaxf(m[j], mx);
-          muse[j] = mnew == -INFINITY ? 0.0f : mnew;
-          const float alpha = fast_exp2(m[j] - muse[j]);
-          m[j] = mnew;
-          if (alpha != 1.0f) {
-            l[j] *= alpha;
-            ov[j] *= alpha;
+            for (int u = 0; u < 4; ++u) v = fmaxf(v, fmaxf(sc[u][j], sc[u][2 + j]));
+            mx[j] = v;
+            need |= v > thr[j];
+          }
+          if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              acc[i][j] *= alpha;
-              acc[i][2 + j] *= alpha;
+            for (int j = 0; j < 2; ++j) {
+              const float mnew = fmaxf(m[j], muse[j] + warp_max_g(mx[j]));
+              if (mnew != m[j]) {
+                const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
+                const float alpha = fast_exp2(m[j] - mu2);
+                const float delta = muse[j] - mu2;
+                l[j] *= alpha;
+                ov[j] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  acc[i][j] *= alpha;
+                  acc[i][2 + j] *= alpha;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  sc[u][j] += delta;
+                  sc[u][2 + j] += delta;
+                }
+                m[j] = mnew;
+                muse[j] = mu2;
+                thr[j] = mnew == -INFINITY ? -INFINITY : 8.0f;
+              }
             }
           }
         }
@@ -1016,13 +1064,13 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
         for (int u = 0; u < 4; ++u) {
           float pr[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[u][c] - muse[c & 1]);
+          for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[u][c]);
           l[0] += pr[0] + pr[2];
           l[1] += pr[1] + pr[3];
           ov[0] = fmaf(pr[0], vb[u][0], fmaf(pr[2], vb[u][1], ov[0]));
           ov[1] = fmaf(pr[1], vb[u][0], fmaf(pr[3], vb[u][1], ov[1]));
-          const uint32_t pb0 = movmatrix_trans(pack_f16x2(pr[0] * va[u][0], pr[1] * va[u][0]));
-          const uint32_t pb1 = movmatrix_trans(pack_f16x2(pr[2] * va[u][1], pr[3] * va[u][1]));
+          const uint32_t pb0 = movmatrix_trans(pack_f16x2_sat(pr[0] * va[u][0], pr[1] * va[u][0]));
+          const uint32_t pb1 = movmatrix_trans(pack_f16x2_sat(pr[2] * va[u][1], pr[3] * va[u][1]));
           const int tok = 16 * u + vtok;
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {

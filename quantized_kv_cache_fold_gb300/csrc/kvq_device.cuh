@@ -207,6 +207,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return d;
 }
 
+// (lo, hi) fp32 -> f16x2, round to nearest even, saturating to +-65504 instead of overflowing.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 // (lo, hi) fp32 -> two e4m3 bytes (lo in the low byte), nearest even, saturating finite.
 __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   uint16_t d;
