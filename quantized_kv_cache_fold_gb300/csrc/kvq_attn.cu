@@ -579,10 +579,20 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
           // ---- online softmax update
           // Lazy base: scores are already relative to muse. The base moves (to the running
           // maximum, rescaling l, ov and acc) only when some score of the page exceeds it by
-          // more than 8, so P stays <= 2^8 and most pages skip the cross-lane maximum.
+          // more than 8, so P stays <= 2^8 and most pages skip the cross-lane maximum. P s_V
+          // enters the PV product in f16, which stays finite for P <= 2^8 while s_V < 255; a page
+          // holding a larger V scale moves the base as soon as any score exceeds it, so that
+          // there P <= 1 and P s_V <= 65504.
           {
             float mx[NT][2];
             bool need = false;
+            bool big = false;
+            if (FMT == 0) {
+              float vmax = 0.0f;
+#pragma unroll
+              for (int u = 0; u < MTU; ++u) vmax = fmaxf(vmax, fmaxf(va[u][0], va[u][1]));
+              big = vmax >= 255.0f;
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -591,7 +601,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
                 for (int u = 0; u < MTU; ++u) v = fmaxf(v, fmaxf(sc[nt][u][j], sc[nt][u][2 + j]));
                 mx[nt][j] = v;
-                need |= v > thr[nt][j];
+                need |= v > (big ? fminf(thr[nt][j], 0.0f) : thr[nt][j]);
               }
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -770,7 +780,7 @@ constexpr int kVBuf = 2 * kPage * kTileRow + kPage * 16;     // K16, V16, meta
 #endif
 // row tiles (8 query rows each) from which the shared-tile kernel is used
 #ifndef KVQ_VERIFY_MIN_TILES
-#define KVQ_VERIFY_MIN_TILES 4
+#define KVQ_VERIFY_MIN_TILES 5
 #endif
 constexpr int kConvWarps = KVQ_VERIFY_CONV;  // 64 / kConvWarps tokens each
 static_assert(64 % (2 * kConvWarps) == 0, "converter warps split the page's tokens in pairs of rows");
@@ -1018,17 +1028,22 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
             }
         }
 
-        // ---- online softmax (lazy base: moved only when a score exceeds it by more than 8)
+        // ---- online softmax (lazy base: moved only when a score exceeds it by more than 8,
+        // or by anything on a page holding a V scale >= 255; see attn_kernel)
         {
           float mx[2];
           bool need = false;
+          float vmax = 0.0f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) vmax = fmaxf(vmax, fmaxf(va[u][0], va[u][1]));
+          const bool big = vmax >= 255.0f;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             float v = -INFINITY;
 #pragma unroll
             for (int u = 0; u < 4; ++u) v = fmaxf(v, fmaxf(sc[u][j], sc[u][2 + j]));
             mx[j] = v;
-            need |= v > thr[j];
+            need |= v > (big ? fminf(thr[j], 0.0f) : thr[j]);
           }
           if (__any_sync(0xffffffffu, need)) {
 #pragma unroll

@@ -37,6 +37,7 @@ ALPHA = np.float32(930.0 / 98.0)
 # stream ids
 S_KEYS, S_VALUES, S_QUERIES, S_GQ, S_GK, S_OUTLIERS, S_CTXLEN, S_PAGEPERM = 1, 2, 3, 4, 5, 6, 7, 8
 S_SWA_K, S_SWA_V, S_SWA_Q, S_ROTSEED = 9, 10, 11, 12
+S_ALIGN = 13
 
 
 def build(verbose: bool = False) -> str:
@@ -173,6 +174,28 @@ def q_rows(seed: int, layer: int, seq: int, pos0: int, S: int, n_q: int, bf16: b
     stream = S_SWA_Q if swa else S_QUERIES
     x = normals(key(seed, stream), q_index(layer, seq, pos0, n_q), S * n_q * HEAD_DIM, None, bf16)
     return x.reshape(S, n_q, HEAD_DIM)
+
+
+def aligned_rows(seed: int, seq: int, L: int, S: int, n_q: int, n_kv: int, theta0: float = 1.4,
+                 v_scale: float = 1.0):
+    """Inputs whose scores climb through the context, for exercising the online softmax.
+
+    Per KV head a direction u_h; the key at position t is cos(a_t) u_h + sin(a_t) |u_h| w_t / |w_t|
+    with a normal draw w_t and a_t = theta0 (1 - t / (L - 1)), so its alignment with u_h rises
+    towards the end. Query rows (S of them per head, the last S positions) are u_h of their KV
+    head (hq // (n_q / n_kv)) plus 0.05 x a normal draw. Values are normal draws x v_scale.
+    Returns (keys [L, n_kv, 128], values [L, n_kv, 128], queries [S, n_q, 128]), float32."""
+    k = key(seed, S_ALIGN)
+    u = normals(k, kv_index(1, seq, 0, n_kv), n_kv * HEAD_DIM).reshape(n_kv, HEAD_DIM).astype(np.float64)
+    w = normals(k, kv_index(0, seq, 0, n_kv), L * n_kv * HEAD_DIM).reshape(L, n_kv, HEAD_DIM).astype(np.float64)
+    a = theta0 * (1.0 - np.arange(L, dtype=np.float64) / max(L - 1, 1))
+    un = np.linalg.norm(u, axis=-1)
+    wn = np.linalg.norm(w, axis=-1, keepdims=True)
+    keys = np.cos(a)[:, None, None] * u[None] + (np.sin(a)[:, None] * un[None])[..., None] * w / wn
+    vals = normals(k, kv_index(2, seq, 0, n_kv), L * n_kv * HEAD_DIM).reshape(L, n_kv, HEAD_DIM) * np.float32(v_scale)
+    noise = normals(k, q_index(3, seq, 0, n_q), S * n_q * HEAD_DIM).reshape(S, n_q, HEAD_DIM).astype(np.float64)
+    qs = u[np.arange(n_q) // (n_q // n_kv)][None] + 0.05 * noise
+    return keys.astype(np.float32), vals.astype(np.float32), qs.astype(np.float32)
 
 
 def context_lengths(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
