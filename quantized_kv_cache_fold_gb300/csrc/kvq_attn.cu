@@ -462,7 +462,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
                 ka[u][hh] = sk * p.score_scale;
                 kb[u][hh] = KVQ_K_BIASED ? ok_ : fmaf(8.0f, sk, ok_);
                 va[u][hh] = sv;
-                vb[u][hh] = fmaf(8.0f, sv, ovv);
+                vb[u][hh] = fmaf(7.5f, sv, ovv);
               }
           }
 
@@ -668,8 +668,8 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
                 for (int ci = 0; ci < 2; ++ci) {
                   uint32_t h0[4], h1[4];
-                  unpack8_centred(rr[2 * ci], h0);
-                  unpack8_centred(rr[2 * ci + 1], h1);
+                  unpack8_v(rr[2 * ci], h0);
+                  unpack8_v(rr[2 * ci + 1], h1);
 #pragma unroll
                   for (int e1 = 0; e1 < 2; ++e1) {
                     const int mtd = 2 * (2 * cc + ci) + e1;
@@ -724,8 +724,13 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int dlo = out_dim<FMT>(i, g), dhi = out_dim<FMT>(i, g + 8);
-          dst[2 + dlo] = (acc[nt][i][j] + ot) * vs;
-          dst[2 + dhi] = (acc[nt][i][2 + j] + ot) * vs;
+          if (FMT == 0) {  // V entered as unpack8_v values: dims of class 2 (i & 1) and 2 (i & 1) + 1
+            dst[2 + dlo] = fmaf(acc[nt][i][j], v_unscale(2 * (i & 1)), ot);
+            dst[2 + dhi] = fmaf(acc[nt][i][2 + j], v_unscale(2 * (i & 1) + 1), ot);
+          } else {
+            dst[2 + dlo] = (acc[nt][i][j] + ot) * vs;
+            dst[2 + dhi] = (acc[nt][i][2 + j] + ot) * vs;
+          }
         }
       }
     }
@@ -886,7 +891,7 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
           uint32_t h[4];
           unpack8_biased(kw[it], h);
           *reinterpret_cast<uint4*>(buf + tok * kTileRow + 16 * (j ^ (tok & 7))) = make_uint4(h[0], h[1], h[2], h[3]);
-          unpack8_centred(vw[it], h);
+          unpack8_v(vw[it], h);
           *reinterpret_cast<uint4*>(buf + kPage * kTileRow + tok * kTileRow + 16 * (j ^ (tok & 7))) =
               make_uint4(h[0], h[1], h[2], h[3]);
         }
@@ -896,7 +901,7 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
           const uint32_t mk = meta[tok], mv = meta[kPage + tok];
           const float sv = h2f_lo(mv);
           reinterpret_cast<float4*>(buf + 2 * kPage * kTileRow)[tok] =
-              make_float4(h2f_lo(mk) * p.score_scale, h2f_hi(mk), sv, fmaf(8.0f, sv, h2f_hi(mv)));
+              make_float4(h2f_lo(mk) * p.score_scale, h2f_hi(mk), sv, fmaf(7.5f, sv, h2f_hi(mv)));
         }
       }
       __syncwarp();
@@ -1114,8 +1119,9 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          dst[2 + tile_dim(2 * i, g)] = acc[i][j] + ot;
-          dst[2 + tile_dim(2 * i + 1, g)] = acc[i][2 + j] + ot;
+          const int d0 = tile_dim(2 * i, g), d1 = tile_dim(2 * i + 1, g);
+          dst[2 + d0] = fmaf(acc[i][j], v_unscale(d0 & 3), ot);  // V tiles hold unpack8_v values
+          dst[2 + d1] = fmaf(acc[i][2 + j], v_unscale(d1 & 3), ot);
         }
       }
     }

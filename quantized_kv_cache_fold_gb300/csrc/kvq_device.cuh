@@ -187,6 +187,37 @@ __device__ __forceinline__ void unpack8_biased(uint32_t x, uint32_t (&h)[4]) {
   h[3] = lop3<0xEA>(x8, 0x00F000F0u, kMagic);
 }
 
+// V code records: each 16-bit element holds the codes c0..c3 of dims 4j..4j+3 of one token in
+// an encoding that converts to exact f16 without f16 arithmetic. Code c is taken as
+// c - 7.5 = +-(e + 1/2), sign = (c < 8), e = c >= 8 ? c - 8 : 7 - c, and read as the f16
+// subnormal +-(2e + 1) 2^(k - 24) = (c - 7.5) 2^(k - 23), for a per-dim k:
+//   dim 4j+0: e in bits 1-3,   sign in bit 15   k = 0, read in place
+//   dim 4j+1: e in bits 4-6,   sign in bit 14   k = 4, read after << 1
+//   dim 4j+2: e in bits 11-13, sign in bit 7    k = 2, read after swapping the two bytes
+//   dim 4j+3: e in bits 8-10,  sign in bit 0    k = 6, read after the swap and << 7
+// The logical codes are what the cache stores; this is only their bit placement.
+__host__ __device__ __forceinline__ uint32_t v_encode4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+  const uint32_t s0 = c0 < 8u, s1 = c1 < 8u, s2 = c2 < 8u, s3 = c3 < 8u;
+  const uint32_t e0 = s0 ? 7u - c0 : c0 - 8u, e1 = s1 ? 7u - c1 : c1 - 8u;
+  const uint32_t e2 = s2 ? 7u - c2 : c2 - 8u, e3 = s3 ? 7u - c3 : c3 - 8u;
+  return (e0 << 1) | (s0 << 15) | (e1 << 4) | (s1 << 14) | (e2 << 11) | (s2 << 7) | (e3 << 8) | s3;
+}
+// Factor that takes dim 4j+i of a PV product over unpack8_v values back to c - 7.5 units: 2^(23 - k_i).
+__device__ __forceinline__ float v_unscale(int i) {
+  return i == 0 ? 8388608.0f : i == 1 ? 524288.0f : i == 2 ? 2097152.0f : 131072.0f;
+}
+
+// Two 16-bit V elements (two tokens, or dims 4j..4j+3 and 4j+4..4j+7 of one token) -> four f16x2:
+// h[i] = dim 4j+i of the low element and of the high element, (c - 7.5) 2^(k_i - 23).
+__device__ __forceinline__ void unpack8_v(uint32_t x, uint32_t (&h)[4]) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, 0x2301;" : "=r"(r) : "r"(x));  // bytes swapped within each half
+  h[0] = lop3<0xEA>(x, 0x800E800Eu, 0x00010001u);
+  h[1] = lop3<0xEA>(x << 1, 0x80E080E0u, 0x00100010u);
+  h[2] = lop3<0xEA>(r, 0x80388038u, 0x00040004u);
+  h[3] = lop3<0xEA>(r << 7, 0x83808380u, 0x00400040u);
+}
+
 // Two e4m3 bytes (low byte first) -> f16x2 (exact: e4m3 is a subset of f16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t d;

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       } else {
         const Quant4 q = quantize(x);  // lane holds elements 4l..4l+3
-        const uint32_t two = (q.c[0] | (q.c[1] << 4)) | ((q.c[2] | (q.c[3] << 4)) << 8);
+        const uint32_t two = v_encode4(q.c[0], q.c[1], q.c[2], q.c[3]);
         const int chunk = (lane >> 3) ^ ((slot >> 1) & 3);
         *reinterpret_cast<uint16_t*>(blk + kPage * kRec4 + slot * kRec4 + chunk * 16 + ((2 * lane) & 15)) =
             (uint16_t)two;

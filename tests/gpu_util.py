@@ -46,6 +46,20 @@ def _nibbles(rec):
     return out
 
 
+def _v_codes(rec):
+    """[..., 64] bytes of V records (chunk swizzle undone) -> [..., 128] codes. Each 16-bit element
+    (little endian) holds dims 4l..4l+3 as (e, sign) fields: dim 0 e bits 1-3 / sign 15, dim 1
+    4-6 / 14, dim 2 11-13 / 7, dim 3 8-10 / 0; code = sign ? 7 - e : 8 + e."""
+    u = rec.astype(np.uint16).reshape(rec.shape[:-1] + (32, 2))
+    u = (u[..., 0] | (u[..., 1] << 8)).astype(np.int64)
+    out = np.empty(rec.shape[:-1] + (32, 4), np.uint8)
+    for i, (eb, sb) in enumerate(((1, 15), (4, 14), (11, 7), (8, 0))):
+        e = (u >> eb) & 7
+        sg = (u >> sb) & 1
+        out[..., i] = np.where(sg == 1, 7 - e, 8 + e)
+    return out.reshape(rec.shape[:-1] + (128,))
+
+
 def unpack_int4(tensors, b, h, L):
     """Logical K/V codes and fp16 scale/offset bits of positions 0..L-1 of sequence b, head h."""
     bt = tensors["block_table"][b].cpu().numpy()
@@ -68,7 +82,7 @@ def unpack_int4(tensors, b, h, L):
         vlog[:, c * 16:(c + 1) * 16] = np.take_along_axis(vc, idx, axis=1)
     return {
         "kc": _nibbles(kc), "ks": (km & 0xFFFF).astype(np.uint16), "ko": (km >> 16).astype(np.uint16),
-        "vc": _nibbles(vlog), "vs": (vm & 0xFFFF).astype(np.uint16), "vo": (vm >> 16).astype(np.uint16),
+        "vc": _v_codes(vlog), "vs": (vm & 0xFFFF).astype(np.uint16), "vo": (vm >> 16).astype(np.uint16),
     }
 
 
