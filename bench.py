@@ -288,6 +288,74 @@ def run_64k(device, steps=30, warmup=3):
             "session_layer_steps_per_s": round(w.B / t, 1), "algorithmic_bytes": by}
 
 
+def run_verify(device, steps=30, warmup=3):
+    """The speculative-verify workload: 64 sequences at 16,384 context, 20/4 heads, S = 1, 4 and 8
+    query rows per sequence with the S new K/V rows rotated, quantised and appended inside the
+    call (at the same positions every repetition), one int4 layer. S = 8 (40 rows per KV head) is
+    timed with both many-row kernels (the mma.sync shared-tile kernel, the default, and the
+    tcgen05 variant selected by KVQ_MANY_ROWS_KERNEL)."""
+    import os
+
+    import torch
+
+    import synth
+    from quantized_kv_cache_fold_gb300.runner import DecodeStack
+    from synth.workloads import config
+
+    w = config(4)
+    stream = torch.cuda.current_stream().cuda_stream
+    perm = lambda l, n: synth.page_permutation(w.seed, l, n)  # noqa: E731
+    Smax = 8
+    st = DecodeStack(w.B, w.Hq, w.Hkv, Smax, w.max_pages() + 1, 1, 1, page_perm=perm, device=device)
+    gq, gk = synth.gains(w.seed, 0)
+    st.set_int4_params(0, synth.rotation_seed(w.seed, 0), gq, gk)
+
+    def fill(b, p0, T, kb, vb):
+        synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "k", True, kb.data_ptr(), stream)
+        synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "v", True, vb.data_ptr(), stream)
+
+    st.prefill_int4(0, w.ctx, fill, chunk_tokens=32768)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).to(device)
+    rows = []
+    for S, kernel in ((1, None), (4, None), (8, "tile"), (8, "tcgen05")):
+        q = torch.empty((w.B, S, w.Hq, 128), dtype=torch.bfloat16, device=device)
+        kn = torch.empty((w.B, S, w.Hkv, 128), dtype=torch.bfloat16, device=device)
+        vn = torch.empty_like(kn)
+        for t, key in ((q, synth.S_QUERIES), (kn, synth.S_KEYS), (vn, synth.S_VALUES)):
+            synth.normals_device(synth.key(w.seed + 2000 + S, key), 0, t.numel(), t.data_ptr(), None, True, stream)
+        out = torch.empty((w.B, S, w.Hq, 128), dtype=torch.float32, device=device)
+        old = os.environ.get("KVQ_MANY_ROWS_KERNEL")
+        if kernel:
+            os.environ["KVQ_MANY_ROWS_KERNEL"] = kernel
+        try:
+            for _ in range(warmup):
+                st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(min(steps, 30))]
+            for e0, e1 in evs:
+                e0.record()
+                st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)
+                e1.record()
+            torch.cuda.synchronize()
+        finally:
+            if kernel:
+                if old is None:
+                    del os.environ["KVQ_MANY_ROWS_KERNEL"]
+                else:
+                    os.environ["KVQ_MANY_ROWS_KERNEL"] = old
+        assert st.read_error() == 0
+        t = statistics.median([e0.elapsed_time(e1) for e0, e1 in evs]) * 1e-3
+        by = int((w.ctx + S).sum()) * w.Hkv * 136
+        rows.append({"S": S, "rows_per_kv_head": S * w.G, "many_row_kernel": kernel or "-",
+                     "int4_call_us": round(t * 1e6, 1), "hbm_gbs": round(by / t / 1e9, 1),
+                     "query_rows_per_s": round(w.B * S / t, 1)})
+    del st
+    torch.cuda.empty_cache()
+    return {"workload": "speculative verify: 64 sequences x 16,384 context, 20/4 heads, new rows appended in the "
+                        "call, one int4 layer, random page order", "points": rows}
+
+
 def run_swa(device, steps=30, warmup=3):
     """The 40 FP8 window-513 layers of the 256k step alone (8 sequences x 4 KV heads, 576-slot
     rings, one query row, appended row inside the call), steps captured in one CUDA graph. A
@@ -853,10 +921,11 @@ def main():
     ap.add_argument("--prologue", default="matrix", choices=["matrix", "fwht"],
                     help="Q/K prologue of the int4 layers: the folded 128x128 matrices (default) or the "
                          "fast Walsh-Hadamard form (second codec specification)")
-    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity"],
+    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity", "verify"],
                     help="run only the 64k single-layer int4 point, only the 40 window layers of the 256k "
-                         "step (small cases for profiling), the A/B of full-layer formats (ab), or the "
-                         "capacity and throughput sweep of a fixed KV pool (capacity)")
+                         "step (small cases for profiling), the A/B of full-layer formats (ab), the "
+                         "capacity and throughput sweep of a fixed KV pool (capacity), or the speculative "
+                         "verify workload with both many-row kernels (verify)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -873,6 +942,10 @@ def main():
         import torch
         torch.cuda.set_device(local)
         print(json.dumps(run_ab(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+    elif args.only == "verify":
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_verify(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
     elif args.only == "swa":
         import torch
         torch.cuda.set_device(local)

@@ -26,6 +26,9 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -784,6 +787,11 @@ constexpr int kVBuf = 2 * kPage * kTileRow + kPage * 16;     // K16, V16, meta
 #define KVQ_VERIFY_CONV 2
 #endif
 // row tiles (8 query rows each) from which the shared-tile kernel is used
+// many-row calls through the tcgen05 kernel (1) or the shared-tile mma.sync kernel (0) unless
+// the environment variable KVQ_MANY_ROWS_KERNEL names one ("tcgen05" or "tile")
+#ifndef KVQ_VERIFY_TC
+#define KVQ_VERIFY_TC 0
+#endif
 #ifndef KVQ_VERIFY_MIN_TILES
 #define KVQ_VERIFY_MIN_TILES 5
 #endif
@@ -1130,6 +1138,580 @@ __global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kern
   }
 }
 
+// ------------------------------------------------------------ many query rows: tcgen05 variant
+// The shared-tile kernel above is bound by shared-memory reads: every 8-row tile warp reads the
+// page's f16 tiles through ldmatrix. Here the two contractions run on the asynchronous tensor
+// cores (tcgen05.mma, accumulators in tensor memory), so each tile is read once per product for
+// all query rows. Work unit: up to two pages (128 tokens) of one segment.
+//
+//   warp 0       producer: page-head blocks into kTcStages int4 stages (produce_pages)
+//   warps 1-2    converters: K codes -> K^ (unpack8_biased values), V codes -> V^ (unpack8_v
+//                values), per-token fp32 (s_K * score scale, o_K, s_V, o_V + 7.5 s_V); K^ and
+//                V^ token-major, 128-byte rows of 64 dims, 128-byte swizzle, dims in the
+//                unpacked order 8w + {0, 4, 1, 5, 2, 6, 3, 7}
+//   warp 3       MMA: S = K^ Q'^T into tensor memory (M = 128 tokens, N = rows rounded up to
+//                16, K = 128 dims, K-major operands); O += V^T P (M = 128 dims, N = rows,
+//                K = 128 tokens; both operands token-major, i.e. MN-major)
+//   warps 4-15   softmax: thread = token (tensor-memory lane 32 (warp % 4) + lane), rows split
+//                in three groups of 16 between warps w, w + 4 and w + 8; lazy exponent base as in
+//                attn_kernel; P s_V written token-major (f16) for the PV product
+//
+// Q' is the query with the high-nibble dims divided by 16 (K^ holds 1024 + c and 1024 + 16c);
+// the bias 1024 sum(Q') of each row is subtracted from S in fp32. Every wait is bounded; the
+// softmax warps take every decision that steers their named barriers through barrier
+// reductions, so they always meet at the same barriers.
+constexpr int kTcStages = 4;
+constexpr int kTcConv = 2;
+constexpr int kTcSoft = 12;
+constexpr int kTcThreads = (1 + kTcConv + 1 + kTcSoft) * 32;
+constexpr int kTcHalf = 16;  // rows per softmax thread (three row groups)
+constexpr int kTcMaxRows = 48;
+
+struct TcLayout {  // offsets from the 1024-byte aligned start of dynamic shared memory
+  size_t kt, vt, pt, qt, meta, stages, bars, valid, vvalid, flags, taddr, rowc, rowst, ovrow, rowm, red, pre, total;
+  __host__ __device__ explicit TcLayout(int B) {
+    kt = 0;                     // [2][2 dim-atoms][128 tokens][128 B]
+    vt = kt + 2 * 32768;        // [2][2 dim-atoms][128 tokens][128 B]
+    pt = vt + 2 * 32768;        // [2][128 tokens][128 B] (rows 0..63)
+    qt = pt + 2 * 16384;        // [2 dim-atoms][48 rows][128 B]
+    meta = qt + 2 * 6144;       // [2][128] float4
+    stages = meta + 2 * 2048;   // kTcStages int4 stages
+    bars = stages + (size_t)kTcStages * kStage4;
+    valid = bars + 8 * 32;
+    vvalid = valid + 4 * kTcStages;  // [2][2]
+    flags = vvalid + 16;
+    taddr = flags + 32;
+    rowc = align_up(taddr + 16, 16);     // [48] float4: -bias, qs, -muse, thr
+    rowst = rowc + 16 * kTcMaxRows;      // [48] m
+    ovrow = rowst + 4 * kTcMaxRows;      // [48] offset sums of the finished segment
+    rowm = ovrow + 4 * kTcMaxRows;       // [12][16] per-warp row maxima
+    red = rowm + 4 * kTcSoft * kTcHalf;  // [12][16][2] per-warp l, ov sums
+    pre = red + 8 * kTcSoft * kTcHalf;
+    total = pre + 4 * (size_t)(B + 1);
+  }
+};
+
+// Unit iterator shared by all roles: consecutive pairs of pages within each segment of the
+// CTA's range.
+struct TcUnits {
+  const AttnParams& p;
+  const int* pre;
+  long long seg_start, seg_end, p1;
+  int b, h, lp0, np, j0, kseg, sidx;
+  __device__ TcUnits(const AttnParams& p_, const int* pre_, long long p0, long long p1_)
+      : p(p_), pre(pre_), seg_start(p0), seg_end(p0), p1(p1_), b(0), h(0), lp0(0), np(0), j0(0), kseg(0), sidx(-1) {}
+  // advance to the next unit; false at the end. first = the unit starts a segment.
+  __device__ bool next(bool& first) {
+    j0 += 2;
+    first = false;
+    if (sidx < 0 || seg_start + j0 >= seg_end) {
+      if (sidx >= 0) {
+        kseg += (int)(seg_end - seg_start);
+        seg_start = seg_end;
+      }
+      if (seg_start >= p1) return false;
+      decode_page(pre, p.B, p.Hkv, seg_start, b, h, lp0, np);
+      seg_end = min(p1, seg_start + (np - lp0));
+      j0 = 0;
+      ++sidx;
+      first = true;
+    }
+    return true;
+  }
+  __device__ int npg() const { return (int)min(2LL, seg_end - seg_start - j0); }
+  __device__ int k0() const { return kseg + j0; }   // CTA page index of the unit's first page
+  __device__ int lp() const { return lp0 + j0; }    // sequence page of the unit's first page
+  __device__ bool last() const { return seg_start + j0 + 2 >= seg_end; }  // last unit of its segment
+};
+
+__device__ __forceinline__ int tc_chunk(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
+__device__ __forceinline__ int tc_dim(int m) {  // dim at position m of a unpacked 8-dim group
+  return 8 * (m >> 3) + ((m & 1) ? 4 : 0) + ((m & 7) >> 1);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const TcLayout L(p.B);
+  uint8_t* stages = smem + L.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  // Buffers of unit u: K^, V^, meta, S (tensor memory) and P, all u % 2.
+  uint64_t* full = bars;             // [4]
+  uint64_t* empty = bars + 4;        // [4]
+  uint64_t* tready = bars + 8;       // [2] unit converted -> MMA / softmax
+  uint64_t* tfree = bars + 10;       // [2] PV(u) done -> buffers free
+  uint64_t* sfull = bars + 12;       // [2] QK(u) done
+  uint64_t* sfree = bars + 14;       // [2] S of unit u read
+  uint64_t* pready = bars + 16;      // [2] P of unit u written
+  uint64_t* qready = bars + 18;      // Q' of the next segment written
+  uint64_t* ofree = bars + 19;       // O of the finished segment read
+  uint64_t* fin = bars + 20;         // final MMA completion
+  volatile int* valid = reinterpret_cast<volatile int*>(smem + L.valid);
+  volatile int* vvalid = reinterpret_cast<volatile int*>(smem + L.vvalid);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + L.taddr);
+  float4* rowc = reinterpret_cast<float4*>(smem + L.rowc);
+  float* rowst = reinterpret_cast<float*>(smem + L.rowst);
+  float* ovrow = reinterpret_cast<float*>(smem + L.ovrow);
+  float* rowm = reinterpret_cast<float*>(smem + L.rowm);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  int* pre = reinterpret_cast<int*>(smem + L.pre);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  griddep_wait();
+  griddep_launch_dependents();
+  build_prefix(p, 0, pre, flags);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTcConv);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tready[b], kTcConv);
+      mbar_init(&tfree[b], 1);
+      mbar_init(&sfull[b], 1);
+      mbar_init(&sfree[b], kTcSoft);
+      mbar_init(&pready[b], kTcSoft);
+    }
+    mbar_init(qready, 1);
+    mbar_init(ofree, 1);
+    mbar_init(fin, 1);
+  }
+  // V^ tiles start finite (a one-page unit multiplies the other page's rows by P = 0)
+  for (int i = threadIdx.x; i < 2 * 32768 / 16; i += kTcThreads)
+    reinterpret_cast<uint4*>(smem + L.vt)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < 2 * 16384 / 16; i += kTcThreads)
+    reinterpret_cast<uint4*>(smem + L.pt)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < 2 * 6144 / 16; i += kTcThreads)
+    reinterpret_cast<uint4*>(smem + L.qt)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_barrier_init();
+  fence_proxy_async_shared();
+  if (warp == 3) tmem_alloc_256(taddr_s);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *taddr_s;
+
+  if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
+  const long long P = (long long)p.Hkv * pre[p.B];
+  const int n_eff = (int)min((long long)p.n_cta, P);
+  const bool active = (int)blockIdx.x < n_eff;
+  const long long p0 = active ? (long long)blockIdx.x * P / n_eff : 0;
+  const long long p1 = active ? (long long)(blockIdx.x + 1) * P / n_eff : 0;
+  const int R = p.R, G = p.G;
+  const int NP = (R + 15) & ~15;
+  const uint32_t idesc_qk = umma_idesc_f16(NP, false, false);
+  const uint32_t idesc_pv = umma_idesc_f16(NP, true, true);
+
+  // ------------------------------------------------------------ producer
+  if (warp == 0) {
+    if (active) produce_pages<0>(p, pre, stages, full, empty, valid, flags, kTcStages, p0, p1, lane);
+    return;
+  }
+
+  // ------------------------------------------------------------ converters
+  if (warp <= kTcConv) {
+    const int cw = warp - 1;
+    TcUnits U(p, pre, p0, p1);
+    bool first;
+    for (int u = 0; active && U.next(first); ++u) {
+      const int b = u & 1;
+      bool ok = u < 2 || __all_sync(0xffffffffu, mbar_wait_bounded(&tfree[b], (uint32_t)((u >> 1) - 1) & 1u));
+      uint8_t* kt = smem + L.kt + b * 32768;
+      uint8_t* vt = smem + L.vt + b * 32768;
+      float4* meta = reinterpret_cast<float4*>(smem + L.meta + b * 2048);
+      for (int jj = 0; ok && jj < U.npg(); ++jj) {
+        const int k = U.k0() + jj, s = k % kTcStages;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(k / kTcStages) & 1u));
+        if (!ok) break;
+        const uint8_t* st4 = stages + (size_t)s * kStage4;
+        const int vpage = valid[s];
+        if (cw == 0 && lane == 0) vvalid[2 * b + jj] = vpage;
+        if (vpage) {
+          const int w = lane & 15;
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int tt = 32 * cw + 2 * it + (lane >> 4);  // token of the page
+            const int slot = 64 * jj + tt;                  // token of the unit
+            const uint32_t kw = *reinterpret_cast<const uint32_t*>(st4 + tt * kRec4 + 4 * w);
+            const uint32_t vw = *reinterpret_cast<const uint32_t*>(st4 + kPage * kRec4 + tt * kRec4 +
+                                                                 16 * ((w >> 2) ^ ((tt >> 1) & 3)) + 4 * (w & 3));
+            uint32_t hk[4], hv[4];
+            unpack8_biased(kw, hk);
+            unpack8_v(vw, hv);
+            const int off = (w >> 3) * 16384 + tc_chunk(slot, w & 7);
+            *reinterpret_cast<uint4*>(kt + off) = make_uint4(hk[0], hk[1], hk[2], hk[3]);
+            *reinterpret_cast<uint4*>(vt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          }
+          const int tt = 32 * cw + lane;
+          const uint32_t* mw = reinterpret_cast<const uint32_t*>(st4 + 2 * kPage * kRec4);
+          const uint32_t mk = mw[tt], mv = mw[kPage + tt];
+          const float sv = h2f_lo(mv);
+          meta[64 * jj + tt] = make_float4(h2f_lo(mk) * p.score_scale, h2f_hi(mk), sv, fmaf(7.5f, sv, h2f_hi(mv)));
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      if (!ok) {
+        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+        flags[0] = 1;
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tready[b]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ MMA warp
+  if (warp == 3) {
+    if (lane == 0 && active) {
+      // Polls the readiness of the next QK (tiles converted, its S buffer read, Q' of a new
+      // segment written) and of the oldest PV (P written, O of the previous segment read) and
+      // issues whichever is ready, so neither waits behind the other.
+      TcUnits Uq(p, pre, p0, p1), Up(p, pre, p0, p1);
+      bool fq = false, fp = false;
+      bool qmore = Uq.next(fq), pmore = Up.next(fp);
+      int vq = 0, vp = 0;  // next unit to get its QK / its PV
+      bool ok = true;
+      uint64_t t_idle = 0;
+      uint32_t idle = 0;
+      while (pmore) {
+        bool progressed = false;
+        if (qmore) {
+          const int b = vq & 1;
+          if (mbar_test(&tready[b], (uint32_t)(vq >> 1) & 1u) &&
+              (vq < 2 || mbar_test(&sfree[b], (uint32_t)((vq >> 1) - 1) & 1u)) &&
+              (!fq || mbar_test(qready, (uint32_t)Uq.sidx & 1u))) {
+            tc_fence_after();
+            const uint32_t kt = smem_addr(smem + L.kt + b * 32768), qt = smem_addr(smem + L.qt);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_f16(tmem + 64 * b, umma_sdesc(kt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                       umma_sdesc(qt + (kk >> 2) * 6144 + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
+            umma_commit(&sfull[b]);
+            ++vq;
+            qmore = Uq.next(fq);
+            progressed = true;
+          }
+        }
+        if (vp < vq) {
+          const int b = vp & 1;
+          if (mbar_test(&pready[b], (uint32_t)(vp >> 1) & 1u) &&
+              (!fp || Up.sidx == 0 || mbar_test(ofree, (uint32_t)(Up.sidx - 1) & 1u))) {
+            tc_fence_after();
+            const uint32_t vt = smem_addr(smem + L.vt + b * 32768), pt = smem_addr(smem + L.pt + b * 16384);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_f16(tmem + 128, umma_sdesc(vt + kk * 2048, 16384, 1024), umma_sdesc(pt + kk * 2048, 16384, 1024),
+                       idesc_pv, (fp && kk == 0) ? 0u : 1u);
+            umma_commit(&tfree[b]);
+            ++vp;
+            pmore = Up.next(fp);
+            progressed = true;
+          }
+        }
+        if (progressed) {  // the clock is read only every 1024 idle polls (it is slow to read)
+          idle = 0;
+          t_idle = 0;
+        } else if ((++idle & 1023u) == 0) {
+          if (t_idle == 0) {
+            t_idle = globaltimer();
+          } else if (globaltimer() - t_idle > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
+        }
+      }
+      if (!ok) {
+        set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+        flags[0] = 1;
+      }
+      umma_commit(fin);  // every MMA issued above has completed once this arrives
+      if (!mbar_wait_bounded(fin, 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(3, 32 + kTcSoft * 32);
+    tc_fence_after();
+    tmem_dealloc_256(tmem);
+    return;
+  }
+
+  // ------------------------------------------------------------ softmax warps
+  const int sw = warp - 4, q = sw & 3, rh = sw >> 2;
+  const int tok = 32 * q + lane;                  // token of the unit = tensor-memory lane
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int nsoft = kTcSoft * 32;
+  const int tid = threadIdx.x - 4 * 32;           // 0..255
+  float l[kTcHalf], ov[kTcHalf];
+#pragma unroll
+  for (int j = 0; j < kTcHalf; ++j) l[j] = ov[j] = 0.0f;
+
+  // Q' tile and per-row constants of the segment of sequence bq, KV head hq
+  auto load_segment = [&](int bq, int hq) {
+    for (int e = tid; e < kTcMaxRows * 16; e += nsoft) {  // 16 threads per row, one 8-dim chunk each
+      const int r = e >> 4, w = e & 15;
+      float qv[8];
+      if (r < R) {
+        const float* qrow = p.q_rot + (((size_t)bq * p.S + r / G) * p.Hq + hq * G + r % G) * kD + 8 * w;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) qv[m] = qrow[tc_dim(m) - 8 * (m >> 3)];
+      } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) qv[m] = 0.0f;
+      }
+      uint32_t hq4[4];
+      float part = 0.0f, bsum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float hs = (i & 1) ? 0.0625f : 1.0f;  // positions 2, 3, 6, 7 meet high nibbles
+        hq4[i] = pack_f16x2(qv[2 * i] * hs, qv[2 * i + 1] * hs);
+        bsum += h2f_lo(hq4[i]) + h2f_hi(hq4[i]);
+        part += qv[2 * i] + qv[2 * i + 1];
+      }
+      *reinterpret_cast<uint4*>(smem + L.qt + (w >> 3) * 6144 + tc_chunk(r, w & 7)) =
+          make_uint4(hq4[0], hq4[1], hq4[2], hq4[3]);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        part += __shfl_xor_sync(0xffffffffu, part, o);
+        bsum += __shfl_xor_sync(0xffffffffu, bsum, o);
+      }
+      if (w == 0) {
+        rowc[r] = make_float4(-1024.0f * bsum, part * p.score_scale, 0.0f, -INFINITY);
+        rowst[r] = -INFINITY;
+      }
+    }
+    fence_proxy_async_shared();
+  };
+
+  TcUnits U(p, pre, p0, p1);
+  bool first = false;
+  bool more = active && U.next(first);
+  bool err = false;
+  if (more) load_segment(U.b, U.h);
+  err = named_barrier_or(2, nsoft, false);
+  if (more && tid == 0) mbar_arrive(qready);
+  int ctxb = 0;
+  bool pend = false;  // a failed wait of the previous step, reported at the next barrier
+  for (int v = 0; more && !err; ++v) {
+    const int b = v & 1;
+    const uint32_t rb = (uint32_t)(v >> 1) & 1u;
+    if (first) {
+      bool bad = false;
+      ctxb = eff_ctx(p, U.b, bad, 0);
+    }
+    bool ok = mbar_wait_bounded(&tready[b], rb) && mbar_wait_bounded(&sfull[b], rb);
+    float d[kTcHalf];
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kTcHalf / 8; ++c) {
+        float t8[8];
+        tmem_ld8(tmem + lane_base + 64 * b + kTcHalf * rh + 8 * c, t8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d[8 * c + i] = t8[i];
+      }
+      tmem_wait_ld();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sfree[b]);
+
+    // ---- scores of this token for rows kTcHalf * rh + j (causal limits only on a unit that
+    // reaches past the context)
+    const int npg = U.npg(), jj = tok >> 6;
+    const bool tvalid = ok && jj < npg && vvalid[2 * b + jj] != 0;
+    const int pos = (U.lp() + jj) * kPage + (tok & 63);
+    const bool unit_mask = (U.lp() + npg) * kPage - 1 > ctxb;
+    const float4 mt = tvalid ? reinterpret_cast<const float4*>(smem + L.meta + b * 2048)[tok]
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const bool big = mt.z >= 255.0f;
+    bool need = false;
+#pragma unroll
+    for (int j = 0; j < kTcHalf; ++j) {
+      const int r = kTcHalf * rh + j;
+      float sc = -INFINITY;
+      if (r < R && tvalid && (!unit_mask || pos <= ctxb + r / G)) {
+        const float4 c = rowc[r];
+        sc = fmaf(d[j] + c.x, mt.x, fmaf(mt.y, c.y, c.z));
+        need |= sc > (big ? fminf(c.w, 0.0f) : c.w);
+      }
+      d[j] = sc;
+    }
+    if (named_barrier_or(2, nsoft, need || !ok || pend)) {
+      err = named_barrier_or(2, nsoft, !ok || pend);
+      if (err) break;
+      // ---- rare: move the base of the rows that need it (per-row maximum over the 128 tokens)
+#pragma unroll
+      for (int j = 0; j < kTcHalf; ++j) {
+        float mx = d[j];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) rowm[sw * kTcHalf + j] = mx;
+      }
+      named_barrier(2, nsoft);
+      bool resc = false;
+      float alpha[kTcHalf];
+#pragma unroll
+      for (int j = 0; j < kTcHalf; ++j) {
+        const int r = kTcHalf * rh + j;
+        alpha[j] = 1.0f;
+        if (r >= R) continue;
+        float mt4 = rowm[(4 * rh) * kTcHalf + j];
+        for (int qq = 1; qq < 4; ++qq) mt4 = fmaxf(mt4, rowm[(4 * rh + qq) * kTcHalf + j]);
+        const float4 c = rowc[r];
+        const float mold = rowst[r], muse = -c.z;
+        const float mnew = fmaxf(mold, muse + mt4);
+        if (mnew != mold) {
+          const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
+          alpha[j] = fast_exp2(mold - mu2);
+          d[j] += muse - mu2;
+          l[j] *= alpha[j];
+          ov[j] *= alpha[j];
+          resc = true;
+        }
+      }
+      // O rows of this warp's tensor-memory lanes, columns of its row half (not on a
+      // segment's first unit: O starts from zero there)
+      const bool any_resc = named_barrier_or(2, nsoft, resc);
+      if (any_resc && !first) {
+        const bool okp = mbar_wait_bounded(&tfree[b ^ 1], (uint32_t)((v - 1) >> 1) & 1u);
+        if (okp) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < kTcHalf / 8; ++c) {
+            float t8[8];
+            tmem_ld8(tmem + lane_base + 128 + kTcHalf * rh + 8 * c, t8);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] *= alpha[8 * c + i];
+            tmem_st8(tmem + lane_base + 128 + kTcHalf * rh + 8 * c, t8);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        err = named_barrier_or(2, nsoft, !okp);
+        if (err) break;
+      }
+      if (q == 0 && lane < kTcHalf) {  // one writer per row publishes the new base
+        const int r = kTcHalf * rh + lane;
+        if (r < R) {
+          float mt4 = rowm[(4 * rh) * kTcHalf + lane];
+          for (int qq = 1; qq < 4; ++qq) mt4 = fmaxf(mt4, rowm[(4 * rh + qq) * kTcHalf + lane]);
+          const float4 c = rowc[r];
+          const float mold = rowst[r];
+          const float mnew = fmaxf(mold, -c.z + mt4);
+          if (mnew != mold) {
+            rowst[r] = mnew;
+            rowc[r] = make_float4(c.x, c.y, mnew == -INFINITY ? 0.0f : -mnew, mnew == -INFINITY ? -INFINITY : 8.0f);
+          }
+        }
+      }
+      named_barrier(2, nsoft);
+    }
+
+    // ---- P and P s_V (f16, token-major) for the PV product
+    uint32_t pk[kTcHalf / 2];
+#pragma unroll
+    for (int j = 0; j < kTcHalf; j += 2) {
+      const float p0v = fast_exp2(d[j]), p1v = fast_exp2(d[j + 1]);
+      l[j] += p0v;
+      l[j + 1] += p1v;
+      ov[j] = fmaf(p0v, mt.w, ov[j]);
+      ov[j + 1] = fmaf(p1v, mt.w, ov[j + 1]);
+      pk[j / 2] = pack_f16x2_sat(p0v * mt.z, p1v * mt.z);
+    }
+    ok = v < 2 || mbar_wait_bounded(&tfree[b], (uint32_t)((v >> 1) - 1) & 1u);
+    if (ok) {
+      uint8_t* pt = smem + L.pt + b * 16384;
+#pragma unroll
+      for (int c = 0; c < kTcHalf / 8; ++c)
+        *reinterpret_cast<uint4*>(pt + tc_chunk(tok, (kTcHalf / 8) * rh + c)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_shared();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pready[b]);
+    pend = !ok;
+
+    if (U.last()) {
+      // ---- segment end: token sums per row, next segment's Q', then O -> CTA partial
+      const int bs = U.b, hs = U.h, seg = bs * p.Hkv + hs;
+#pragma unroll
+      for (int j = 0; j < kTcHalf; ++j) {
+        float lt = l[j], ot = ov[j];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          lt += __shfl_xor_sync(0xffffffffu, lt, o);
+          ot += __shfl_xor_sync(0xffffffffu, ot, o);
+        }
+        if (lane == 0) {
+          red[(sw * kTcHalf + j) * 2] = lt;
+          red[(sw * kTcHalf + j) * 2 + 1] = ot;
+        }
+        l[j] = ov[j] = 0.0f;
+      }
+      err = named_barrier_or(2, nsoft, pend);
+      if (err) break;
+      pend = false;
+      if (q == 0 && lane < kTcHalf && kTcHalf * rh + lane < R) {
+        const int r = kTcHalf * rh + lane;
+        float lt = 0.0f, ot = 0.0f;
+        for (int qq = 0; qq < 4; ++qq) {
+          lt += red[((4 * rh + qq) * kTcHalf + lane) * 2];
+          ot += red[((4 * rh + qq) * kTcHalf + lane) * 2 + 1];
+        }
+        float* dst = p.partials + ((size_t)(blockIdx.x + seg) * R + r) * kPartialStride;
+        dst[0] = rowst[r];
+        dst[1] = lt;
+        ovrow[r] = ot;
+      }
+      named_barrier(2, nsoft);
+      bool f2 = false;
+      more = U.next(f2);
+      if (more) load_segment(U.b, U.h);
+      named_barrier(2, nsoft);
+      if (more && tid == 0) mbar_arrive(qready);
+      // O of the finished segment (lane = dim position, columns = rows of this half)
+      ok = mbar_wait_bounded(&tfree[b], rb);
+      if (ok) {
+        tc_fence_after();
+        float o[kTcHalf];
+#pragma unroll
+        for (int c = 0; c < kTcHalf / 8; ++c) {
+          float t8[8];
+          tmem_ld8(tmem + lane_base + 128 + kTcHalf * rh + 8 * c, t8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[8 * c + i] = t8[i];
+        }
+        tmem_wait_ld();
+        const int m = tok, dim = tc_dim(m);
+        const float us = v_unscale(dim & 3);
+#pragma unroll
+        for (int j = 0; j < kTcHalf; ++j) {
+          const int r = kTcHalf * rh + j;
+          if (r < R)
+            p.partials[((size_t)(blockIdx.x + seg) * R + r) * kPartialStride + 2 + dim] = fmaf(o[j], us, ovrow[r]);
+        }
+      }
+      tc_fence_before();
+      err = named_barrier_or(2, nsoft, !ok);
+      if (!err && more && tid == 0) mbar_arrive(ofree);
+      first = f2;
+    } else {
+      more = U.next(first);
+    }
+  }
+  if (err && tid == 0) {
+    set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+    flags[0] = 1;
+  }
+  tc_fence_before();
+  named_barrier(3, 32 + kTcSoft * 32);
+}
+
 // One block per (segment, query row): merges the segment's CTA partials and normalises.
 template <int FMT>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
@@ -1274,6 +1856,49 @@ cudaError_t launch_verify(AttnParams& p, int T, long long p_max, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
 }
 
+// int4 with many query rows through the tcgen05 kernel, then the same combine.
+cudaError_t launch_tc(AttnParams& p, long long p_max, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+  if (dc.sm == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    dc.sm = n > 0 ? n : 1;
+  }
+  const size_t smem = TcLayout(p.B).total + 1024;  // + alignment of the tile atoms
+  static bool attr_set[64] = {false};
+  cudaError_t e = cudaSuccess;
+  if (!attr_set[(dev >= 0 && dev < 64) ? dev : 0]) {
+    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set[(dev >= 0 && dev < 64) ? dev : 0] = true;
+  }
+  long long grid = std::min<long long>((long long)dc.sm, kMaxCtas);  // one CTA per SM
+  grid = std::max<long long>(1, std::min(grid, p_max));
+  p.n_cta = (int)grid;
+  p.ntg = 1;
+  p.nkg = 1;
+  p.nstages = kTcStages;
+  p.rows_pad = kTcMaxRows;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
+}
+
 }  // namespace
 
 size_t workspace_qrot_bytes(int B, int S, int Hq) { return align_up((size_t)B * S * Hq * kD * 4, 256); }
@@ -1315,7 +1940,11 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p_max = (long long)p.Hkv * p.B * (p.cap / kPage);
   }
   const int ntiles = (p.R + 7) / 8;
-  if (job.fmt == 0 && ntiles >= KVQ_VERIFY_MIN_TILES) return launch_verify(p, ntiles, p_max, stream);
+  if (job.fmt == 0 && ntiles >= KVQ_VERIFY_MIN_TILES) {
+    const char* sel = getenv("KVQ_MANY_ROWS_KERNEL");
+    const bool tc = sel ? strcmp(sel, "tcgen05") == 0 : KVQ_VERIFY_TC != 0;
+    return tc ? launch_tc(p, p_max, stream) : launch_verify(p, ntiles, p_max, stream);
+  }
   int NT;
   if (ntiles <= 3) {
     NT = ntiles;

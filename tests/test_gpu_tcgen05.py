@@ -1,0 +1,45 @@
+"""The tcgen05 many-row attention kernel, on the GPU through the C ABI.
+
+"Serving Kolibri-1 with a 4-bit KV cache", section "What we do": one decode kernel family serves
+1..8 query rows per sequence so that verify blocks reuse each KV byte. Calls with more than 32
+rows per KV head have two implementations; KVQ_MANY_ROWS_KERNEL=tcgen05 selects the one whose
+QK^T and PV products run as tcgen05.mma with accumulators in tensor memory. These cases repeat
+the many-row parity checks through it: codes bit-exact, outputs within the tolerance of the
+oracle's attention over the same codes, on the synthetic verify workload (S = 7 and 8, GQA 5,
+ragged contexts, random page order) and on the climbing-score inputs that move the softmax base
+repeatedly and put V scales above 255.
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+from test_gpu_parity import check_int4
+from test_gpu_softmax_base import test_climbing_scores_match_oracle
+from synth.workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def tcgen05_kernel():
+    old = os.environ.get("KVQ_MANY_ROWS_KERNEL")
+    os.environ["KVQ_MANY_ROWS_KERNEL"] = "tcgen05"
+    yield
+    if old is None:
+        del os.environ["KVQ_MANY_ROWS_KERNEL"]
+    else:
+        os.environ["KVQ_MANY_ROWS_KERNEL"] = old
+
+
+@pytest.mark.parametrize("S", [7, 8])
+def test_tcgen05_verify_rows(orc, tcgen05_kernel, S):
+    # 3 sequences with ragged contexts (page tails, several CTAs per segment), random page order
+    w = Workload("tc", 19, 3, 20, 4, S, np.array([1000, 2345, 777]), True, page_order="random")
+    check_int4(orc, w, 0, S, seqs=range(w.B))
+
+
+@pytest.mark.parametrize("v_scale", [1.0, 3000.0])
+def test_tcgen05_climbing_scores(orc, tcgen05_kernel, v_scale):
+    test_climbing_scores_match_oracle(orc, 8, v_scale)
