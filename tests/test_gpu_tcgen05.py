@@ -43,3 +43,12 @@ def test_tcgen05_verify_rows(orc, tcgen05_kernel, S):
 @pytest.mark.parametrize("v_scale", [1.0, 3000.0])
 def test_tcgen05_climbing_scores(orc, tcgen05_kernel, v_scale):
     test_climbing_scores_match_oracle(orc, 8, v_scale)
+
+
+def test_tcgen05_config4_verify_full_size(orc, tcgen05_kernel):
+    # the speculative-verify workload at its full size (64 x 16,384, S = 8), sampled sequences
+    from synth.workloads import config
+    w = config(4)
+    w.S = 8
+    _, _, errs = check_int4(orc, w, 0, 8, [0, 37, 63])
+    print("tcgen05 config4 S=8 worst max-abs %.2e rel-L2 %.2e" % (max(e[0] for e in errs), max(e[1] for e in errs)))
