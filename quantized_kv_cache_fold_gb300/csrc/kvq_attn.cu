@@ -28,6 +28,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -1747,6 +1748,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
 struct DevCache {
   int sm = 0;
   bool vattr = false;  // many-row kernel: shared-memory attribute set, occupancy cache
+  bool tattr = false;  // tcgen05 many-row kernel: shared-memory attribute set
   size_t vocc_smem = 0;
   int vocc_threads = 0, vocc = 0;
   bool attr[2][4] = {{false}};
@@ -1755,34 +1757,39 @@ struct DevCache {
   int occ[2][4] = {{0}};
 };
 DevCache g_dev[64];
+std::mutex g_dev_mu;  // guards g_dev (launch-configuration caches shared by host threads)
 
 template <int FMT, int NT>
 cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_max, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
-  if (dc.sm == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    dc.sm = n > 0 ? n : 1;
-  }
-  if (!dc.attr[FMT][NT]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_kernel<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e != cudaSuccess) return e;
-    dc.attr[FMT][NT] = true;
-  }
   cudaError_t e = cudaSuccess;
-  if (dc.occ_smem[FMT][NT] != smem || dc.occ_threads[FMT][NT] != threads) {
-    int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<FMT, NT>, threads, smem);
-    if (e != cudaSuccess) return e;
-    dc.occ[FMT][NT] = std::max(o, 1);
-    dc.occ_smem[FMT][NT] = smem;
-    dc.occ_threads[FMT][NT] = threads;
+  int occ = 1, sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+    if (dc.sm == 0) {
+      int n = 0;
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      dc.sm = n > 0 ? n : 1;
+    }
+    if (!dc.attr[FMT][NT]) {
+      e = cudaFuncSetAttribute(attn_kernel<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+      if (e != cudaSuccess) return e;
+      dc.attr[FMT][NT] = true;
+    }
+    if (dc.occ_smem[FMT][NT] != smem || dc.occ_threads[FMT][NT] != threads) {
+      int o = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_kernel<FMT, NT>, threads, smem);
+      if (e != cudaSuccess) return e;
+      dc.occ[FMT][NT] = std::max(o, 1);
+      dc.occ_smem[FMT][NT] = smem;
+      dc.occ_threads[FMT][NT] = threads;
+    }
+    occ = dc.occ[FMT][NT];
+    sm = dc.sm;
   }
-  const int occ = dc.occ[FMT][NT];
-  long long grid = std::min<long long>((long long)dc.sm * occ, kMaxCtas);
+  long long grid = std::min<long long>((long long)sm * occ, kMaxCtas);
   grid = std::max<long long>(1, std::min(grid, p_max));
   p.n_cta = (int)grid;
   // both grids may start while the previous one on the stream finishes (each waits for it
@@ -1809,12 +1816,6 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
 cudaError_t launch_verify(AttnParams& p, int T, long long p_max, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
-  if (dc.sm == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    dc.sm = n > 0 ? n : 1;
-  }
   p.ntg = T;
   p.nkg = 1;
   p.nstages = kVStages;
@@ -1822,20 +1823,32 @@ cudaError_t launch_verify(AttnParams& p, int T, long long p_max, cudaStream_t st
   const size_t smem = VerifyLayout(p.B).total;
   const int threads = (1 + kConvWarps + T) * 32;
   cudaError_t e = cudaSuccess;
-  if (!dc.vattr) {
-    e = cudaFuncSetAttribute(attn_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e != cudaSuccess) return e;
-    dc.vattr = true;
+  int occ = 1, sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+    if (dc.sm == 0) {
+      int n = 0;
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      dc.sm = n > 0 ? n : 1;
+    }
+    if (!dc.vattr) {
+      e = cudaFuncSetAttribute(attn_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+      if (e != cudaSuccess) return e;
+      dc.vattr = true;
+    }
+    if (dc.vocc_smem != smem || dc.vocc_threads != threads) {
+      int o = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_verify_kernel, threads, smem);
+      if (e != cudaSuccess) return e;
+      dc.vocc = std::max(o, 1);
+      dc.vocc_smem = smem;
+      dc.vocc_threads = threads;
+    }
+    occ = dc.vocc;
+    sm = dc.sm;
   }
-  if (dc.vocc_smem != smem || dc.vocc_threads != threads) {
-    int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_verify_kernel, threads, smem);
-    if (e != cudaSuccess) return e;
-    dc.vocc = std::max(o, 1);
-    dc.vocc_smem = smem;
-    dc.vocc_threads = threads;
-  }
-  long long grid = std::min<long long>((long long)dc.sm * dc.vocc, kMaxCtas);
+  long long grid = std::min<long long>((long long)sm * occ, kMaxCtas);
   grid = std::max<long long>(1, std::min(grid, p_max));
   p.n_cta = (int)grid;
   cudaLaunchAttribute attr[1];
@@ -1860,21 +1873,25 @@ cudaError_t launch_verify(AttnParams& p, int T, long long p_max, cudaStream_t st
 cudaError_t launch_tc(AttnParams& p, long long p_max, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
-  if (dc.sm == 0) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    dc.sm = n > 0 ? n : 1;
-  }
   const size_t smem = TcLayout(p.B).total + 1024;  // + alignment of the tile atoms
-  static bool attr_set[64] = {false};
   cudaError_t e = cudaSuccess;
-  if (!attr_set[(dev >= 0 && dev < 64) ? dev : 0]) {
-    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set[(dev >= 0 && dev < 64) ? dev : 0] = true;
+  int sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+    if (dc.sm == 0) {
+      int n = 0;
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      dc.sm = n > 0 ? n : 1;
+    }
+    if (!dc.tattr) {
+      e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) return e;
+      dc.tattr = true;
+    }
+    sm = dc.sm;
   }
-  long long grid = std::min<long long>((long long)dc.sm, kMaxCtas);  // one CTA per SM
+  long long grid = std::min<long long>((long long)sm, kMaxCtas);  // one CTA per SM
   grid = std::max<long long>(1, std::min(grid, p_max));
   p.n_cta = (int)grid;
   p.ntg = 1;

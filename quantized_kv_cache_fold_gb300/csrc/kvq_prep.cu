@@ -15,6 +15,8 @@
 
 #include <algorithm>
 
+#include <mutex>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -320,17 +322,21 @@ __global__ void fp8_append_kernel(const Fp8AppendJob j) {
   }
 }
 
+std::mutex g_prep_mu;  // guards the per-device caches below
+int g_sm_count[64] = {0};
+bool g_prep_attr[64] = {false};
+
 int sm_count() {
-  static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] == 0) {
+  std::lock_guard<std::mutex> lock(g_prep_mu);
+  if (g_sm_count[dev] == 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
+    g_sm_count[dev] = n > 0 ? n : 1;
   }
-  return cached[dev];
+  return g_sm_count[dev];
 }
 
 }  // namespace
@@ -344,13 +350,15 @@ cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
   const int cap = 2 * sm_count();
   p.kv_blocks = std::min((p.kv_jobs + kPrepWarps - 1) / kPrepWarps, cap);
   const int q_blocks = std::min((p.q_jobs + kPrepWarps - 1) / kPrepWarps, cap);
-  static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  {
+    std::lock_guard<std::mutex> lock(g_prep_mu);
+    if (dev < 0 || dev >= 64 || !g_prep_attr[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) g_prep_attr[dev] = true;
+    }
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(p.kv_blocks + q_blocks), 1, 1);

@@ -35,6 +35,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <mutex>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -556,17 +558,21 @@ struct SwaDevCache {
   bool attr[4] = {false};
 };
 SwaDevCache g_swa_dev[64];
+std::mutex g_swa_mu;  // guards g_swa_dev
 
 template <int NT>
 cudaError_t launch_swa_t(const SwaParams& p, size_t smem, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  SwaDevCache& dc = g_swa_dev[(dev >= 0 && dev < 64) ? dev : 0];
-  if (!dc.attr[NT]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(swa_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
-    if (e != cudaSuccess) return e;
-    dc.attr[NT] = true;
+  {
+    std::lock_guard<std::mutex> lock(g_swa_mu);
+    SwaDevCache& dc = g_swa_dev[(dev >= 0 && dev < 64) ? dev : 0];
+    if (!dc.attr[NT]) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(swa_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
+      if (e != cudaSuccess) return e;
+      dc.attr[NT] = true;
+    }
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)((long long)p.B * p.Hkv * p.cs), 1, 1);
