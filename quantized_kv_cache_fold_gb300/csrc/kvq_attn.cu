@@ -15,13 +15,17 @@
 // into a ring of shared-memory stages with bulk asynchronous copies (TMA engine) signalled
 // on mbarriers; consumer warps are arranged as token groups x tile groups. A tile is 8
 // query rows (rows = S x G query heads of the KV head, row n = r*G + g). Per page a warp:
-//   QK^T on tensor cores: A = 16 tokens x 16 dims of centred codes (c - 8) in f16,
-//        B = 16 dims x 8 query rows of q~ in f16, fp32 accumulate (mma.m16n8k16);
-//   score = log2(e)*sm_scale*(s_K*dot + (o_K + 8 s_K)*sum(q~)) -- scale and offset per token;
-//   online softmax with warp-shuffle max, exp2;
-//   PV on tensor cores: A = 16 dims x 16 tokens of centred V codes (ldmatrix.trans),
-//        B = 16 tokens x 8 rows of p*s_V in f16 (movmatrix transposes the QK accumulator),
-//        plus sum_j p_j (o_V + 8 s_V) added per row.
+//   QK^T on tensor cores (mma.m16n8k16, fp32 accumulate): A = 16 tokens x 16 dims of K codes
+//        read as f16 1024 + c (low nibbles) or 1024 + 16c (high nibbles, whose query values
+//        are divided by 16), B = 16 dims x 8 query rows of q~ in f16; the accumulator starts at
+//        -1024 sum(q~ fragment), so it holds sum q~ c exactly up to fp32 rounding;
+//   score = log2(e)*sm_scale*(s_K*dot + o_K*sum(q~)) -- scale and offset per token;
+//   online softmax with exp2 against a lazily moved base (moved only when a score passes it
+//        by more than 8, or by anything on pages with a V scale of 255 or more);
+//   PV on tensor cores: A = 16 dims x 16 tokens of V codes read as f16 subnormals
+//        (c - 7.5) 2^(k - 23), B = 16 tokens x 8 rows of p*s_V in f16 (movmatrix transposes
+//        the QK accumulator), plus
+//        sum_j p_j (o_V + 7.5 s_V) added per row; the partial undoes 2^(k - 23) per dim.
 
 #include <algorithm>
 #include <cmath>
@@ -104,9 +108,10 @@ struct SmemLayout {
 };
 
 // Context length of sequence b as used by every kernel of one call (clamped into the
-// cache; `bad` reports a clamp).
+// cache; `bad` reports a clamp). Read at L2 (ld.global.cg): combine_kernel reads it before
+// waiting for the previous grid, so no line an SM's L1 kept from an earlier call may serve it.
 __device__ __forceinline__ int eff_ctx(const AttnParams& p, int b, bool& bad, int fmt) {
-  int c = p.ctx[b];
+  int c = __ldcg(p.ctx + b);
   if (fmt == 0) {
     const int cap = p.max_pages * kPage - p.S;
     if (c < 0 || c > cap) {
@@ -770,9 +775,9 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 //
 //   warp 0          producer: page-head blocks into kVStages int4 stages (produce_pages)
 //   kConvWarps      converters: K codes -> f16 biased (1024 + c / 1024 + 16c, see
-//                   unpack8_biased), V codes -> f16 centred (c - 8), per-token scale/offset ->
-//                   fp32, into one of kVBufs tile buffers; each converts an equal share of the
-//                   64 tokens
+//                   unpack8_biased), V codes -> f16 subnormals (c - 7.5) 2^(k - 23) (see
+//                   unpack8_v), per-token scale/offset -> fp32, into one of kVBufs tile
+//                   buffers; each converts an equal share of the 64 tokens
 //   T tile warps    one per 8 query rows: QK^T, online softmax and PV on tensor
 //                   cores over every page of the CTA's range, partial per segment and row
 //
@@ -1718,9 +1723,12 @@ template <int FMT>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
   volatile int* flags = cpre + p.B + 1;
+  // The previous grid is the same call's attention kernel. It triggers this launch only after
+  // its own wait, so every grid before it has completed, and it writes nothing but the partials
+  // and the error word: the context lengths (read at L2, see eff_ctx) are taken before waiting.
+  build_prefix(p, FMT, cpre, flags);
   griddep_wait();
   griddep_launch_dependents();
-  build_prefix(p, FMT, cpre, flags);
   __syncthreads();
   const int R = p.R;
   const int seg = blockIdx.x / R, row = blockIdx.x - (blockIdx.x / R) * R;
@@ -1731,15 +1739,46 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   const long long first_pg = (long long)p.Hkv * cpre[b] + (long long)h * np;
   const int c0 = (int)cta_of(first_pg, P, n_eff), c1 = (int)cta_of(first_pg + np - 1, P, n_eff);
   const int d = threadIdx.x;
-  float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.partials[((size_t)(c + seg) * R + row) * kPartialStride]);
-  const float Mu = M == -INFINITY ? 0.0f : M;
-  float lsum = 0.0f, a = 0.0f;
-  for (int c = c0; c <= c1; ++c) {
-    const float* src = p.partials + ((size_t)(c + seg) * R + row) * kPartialStride;
-    const float w = fast_exp2(src[0] - Mu);
-    lsum += w * src[1];
-    a += w * src[2 + d];
+  // chunks of up to 8 partials: all loads of a chunk are issued before any is used; the chunk
+  // is merged with log-sum-exp weights against its own maximum, then folded into the total
+  float M = -INFINITY, lsum = 0.0f, a = 0.0f;
+  for (int cb = c0; cb <= c1; cb += 8) {
+    float mv[8], lv[8], av[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (cb + k <= c1) {
+        const float* src = p.partials + ((size_t)(cb + k + seg) * R + row) * kPartialStride;
+        mv[k] = src[0];
+        lv[k] = src[1];
+        av[k] = src[2 + d];
+      } else {
+        mv[k] = -INFINITY;
+        lv[k] = 0.0f;
+        av[k] = 0.0f;
+      }
+    }
+    float Mc = mv[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) Mc = fmaxf(Mc, mv[k]);
+    if (Mc == -INFINITY) continue;  // nothing visible in this chunk
+    float lc = 0.0f, ac = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = fast_exp2(mv[k] - Mc);
+      lc += w * lv[k];
+      ac += w * av[k];
+    }
+    if (M == -INFINITY) {
+      M = Mc;
+      lsum = lc;
+      a = ac;
+    } else {
+      const float Mn = fmaxf(M, Mc);
+      const float so = fast_exp2(M - Mn), sc = fast_exp2(Mc - Mn);
+      lsum = lsum * so + lc * sc;
+      a = a * so + ac * sc;
+      M = Mn;
+    }
   }
   const int r = row / p.G, gi = row - (row / p.G) * p.G;
   p.out[(((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + d] = a / lsum;
