@@ -311,17 +311,20 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   }
   __syncwarp();
 
-  int c0 = p.pos0[b];
-  if (c0 < 0) {
-    if (rank == 0 && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
-    c0 = 0;
+  // Every load below is issued before any result is used: the first position, the query rows
+  // and the first appended key/value row (S = 1 decode appends one; its owner is known only
+  // once the position is, so every warp loads it). No atomic sits between them, so the loads
+  // need not wait for a branch on the position.
+  const int c0raw = p.pos0[b];
+  float xnew[2][4];  // appended row r = 0: key, value
+  if (p.k_new != nullptr) {
+    const size_t row0 = (size_t)b * p.S * p.Hkv + h;
+    load_row4(p.k_new, p.bf16, row0, lane, xnew[0]);
+    load_row4(p.v_new, p.bf16, row0, lane, xnew[1]);
   }
-  const int p_last = c0 + p.S - 1;  // newest position after the append
-  const int slot_last = p_last % p.cap;
 
-  // ---- query fragments (B operand, 8 rows per tile) and per-row window limits
+  // ---- query fragments (B operand, 8 rows per tile)
   uint32_t qf[NT][8][2];
-  int lim_lo[NT][2], lim_hi[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int tile = tg * NT + nt;
@@ -363,9 +366,23 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       qf[nt][ks][0] = pack_f16x2(qv[4 * ks], qv[4 * ks + 1]);
       qf[nt][ks][1] = pack_f16x2(qv[4 * ks + 2], qv[4 * ks + 3]);
     }
+  }
+
+  int c0 = c0raw;
+  if (c0 < 0) {
+    if (rank == 0 && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
+    c0 = 0;
+  }
+  const int p_last = c0 + p.S - 1;  // newest position after the append
+  const int slot_last = p_last % p.cap;
+
+  // ---- per-row window limits
+  int lim_lo[NT][2], lim_hi[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
-      const int nC = 8 * tile + 2 * t + jj;
+      const int nC = 8 * (tg * NT + nt) + 2 * t + jj;
       const int r = nC < p.R ? nC / p.G : 0;
       lim_hi[nt][jj] = c0 + r;
       lim_lo[nt][jj] = max(0, c0 + r - p.window + 1);
@@ -387,7 +404,12 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         float x[4];
-        load_row4(which ? p.v_new : p.k_new, p.bf16, row, lane, x);
+        if (r == 0) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = xnew[which][e];
+        } else {
+          load_row4(which ? p.v_new : p.k_new, p.bf16, row, lane, x);
+        }
         if (!warp_all_finite(x)) {
           if (lane == 0 && tg == 0) set_err(p.dev_err, KVQ_DEVERR_NONFINITE);
           continue;
@@ -477,7 +499,7 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   // other CTAs push that into CTA 0, which merges the cluster and writes the output.
   const uint32_t bar0 = map_cluster(smem_addr(recv_bar), 0);
   const uint32_t recv0 = map_cluster(smem_addr(recv), 0);
-  if (rank == 0 && !mbar_wait_bounded(recv_bar, 0) && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+  bool received = false;  // CTA 0: the other CTAs' pushes have landed (waited after the own merge)
   for (int e = threadIdx.x; e < p.R * 16; e += blockDim.x) {
     const int row = e >> 4, c8 = e & 15;
     const int tgr = (row >> 3) / NT;  // tile group holding this row
@@ -516,7 +538,12 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       st_async_f32x4(dst + 32 + 32 * c8, make_float4(a[4], a[5], a[6], a[7]), bar0);
       continue;
     }
-    // CTA 0: fold in the other CTAs' partials (relative to their own maxima)
+    // CTA 0: fold in the other CTAs' partials (relative to their own maxima). Threads with an
+    // item wait for the pushes, so the CTA outlives the copies into its shared memory.
+    if (!received) {
+      if (!mbar_wait_bounded(recv_bar, 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+      received = true;
+    }
     float mr[kMaxCluster];
     float Mc = M;
 #pragma unroll
