@@ -21,6 +21,13 @@
  *    saturate, a bounded wait that gave up) are OR-ed into *dev_err as KVQ_DEVERR_* bits;
  *    the affected token-heads or pages are skipped. Kernels never trap and never spin
  *    without a time limit. The caller reads *dev_err after synchronising.
+ *  - Kernels are launched with programmatic stream serialisation, so a call's first kernel
+ *    may start while the previous kernel on the stream is still running. Until that kernel
+ *    has completed it reads none of the call's inputs except the folded prologue weights
+ *    (Mq, Mk and their FWHT multipliers), which the int4 calls stage on chip first. Those
+ *    must be complete when the call is made: written by a host copy, by an ordinary kernel,
+ *    or by a kernel that allows dependent launch only after writing them. Within a call each
+ *    kernel waits for the one before it before reading anything that kernel writes.
  *  - Fixed geometry: head_dim 128, 64 tokens per page.
  *  - Thread-safe: no mutable global state beyond per-device attribute caches.
  */

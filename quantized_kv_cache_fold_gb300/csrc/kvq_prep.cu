@@ -150,8 +150,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   const PrepJobs& j = p.j;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
-  // may overlap the previous grid on the stream: only L2 prefetches (the matrix, and the rows of
-  // this warp's first job) before the wait
+  // May overlap the previous grid on the stream. Before the wait: L2 prefetches of this warp's
+  // first rows, and the folded weights (M, or the FWHT multipliers), which are complete before
+  // the call (kvq.h) and are staged into shared memory now.
   const size_t rbytes = (size_t)kD * ((kv_role ? j.kv_bf16 : j.q_bf16) ? 2 : 4);
   const int job0 = kv_role ? (int)blockIdx.x * kPrepWarps + warp
                            : ((int)blockIdx.x - p.kv_blocks) * kPrepWarps + warp;
@@ -166,14 +167,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       r0a = static_cast<const uint8_t*>(j.q) + (size_t)job0 * rbytes;
     }
   }
-  if (threadIdx.x == 0) prefetch_l2_bulk(M, j.fwht ? kD * 4 : kD * kD * 4);
   if (lane == 0 && r0a) prefetch_l2_bulk(r0a, (uint32_t)rbytes);
   if (lane == 0 && r0b) prefetch_l2_bulk(r0b, (uint32_t)rbytes);
-  griddep_wait();
-  griddep_launch_dependents();
-  // the first job's rows into L1 while the matrix is staged in shared memory
-  if (r0a) prefetch_l1(r0a + (lane * rbytes) / 32);
-  if (r0b) prefetch_l1(r0b + (lane * rbytes) / 32);
   // the FWHT prologue needs only this lane's four multipliers; the matrix prologue stages M
   const float4 w4 = j.fwht ? reinterpret_cast<const float4*>(M)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   if (!j.fwht) {
@@ -193,6 +188,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
     }
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int Hkv = j.cache.num_kv_heads;
   if (kv_role) {
@@ -220,8 +217,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       uint32_t* meta = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kRec4);
       const size_t row = (size_t)tok * Hkv + h;
 
-      float x[4];
+      float x[4], xv[4];  // key and value rows, loaded together
       load_row4(j.k, j.kv_bf16, row, lane, x);
+      load_row4(j.v, j.kv_bf16, row, lane, xv);
       if (!warp_all_finite(x)) {
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       } else {
@@ -248,11 +246,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         }
       }
 
-      load_row4(j.v, j.kv_bf16, row, lane, x);
-      if (!warp_all_finite(x)) {
+      if (!warp_all_finite(xv)) {
         if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
       } else {
-        const Quant4 q = quantize(x);  // lane holds elements 4l..4l+3
+        const Quant4 q = quantize(xv);  // lane holds elements 4l..4l+3
         const uint32_t two = v_encode4(q.c[0], q.c[1], q.c[2], q.c[3]);
         const int chunk = (lane >> 3) ^ ((slot >> 1) & 3);
         *reinterpret_cast<uint16_t*>(blk + kPage * kRec4 + slot * kRec4 + chunk * 16 + ((2 * lane) & 15)) =
