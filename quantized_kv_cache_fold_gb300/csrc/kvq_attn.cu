@@ -46,7 +46,7 @@ namespace {
 #define KVQ_TOKEN_GROUPS 4
 #endif
 #ifndef KVQ_STAGES_INT4
-#define KVQ_STAGES_INT4 8
+#define KVQ_STAGES_INT4 12
 #endif
 // K codes enter QK^T as 1024+c (no per-element bias subtraction); see unpack8_biased.
 #ifndef KVQ_K_BIASED
@@ -91,6 +91,10 @@ struct AttnParams {
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Per-lane online-softmax state of one 8-row tile as the token groups exchange it at a
+// segment end: m and l and ov of the lane's two rows, then its 32 accumulator values.
+constexpr int kMergeFloats = 6 + 32;
+
 // Shared-memory layout, identical on host (sizing) and device.
 struct SmemLayout {
   size_t stages, full, empty, valid, pre, flags, red, total;
@@ -103,7 +107,8 @@ struct SmemLayout {
     pre = valid + 4 * nstages;
     flags = pre + 4 * (B + 1);
     red = align_up(flags + 16, 16);
-    total = red + (size_t)nkg * rows_pad * kPartialStride * 4;
+    // one merge slot per tile group: kMergeFloats floats per lane per 8-row tile (lane-major)
+    total = red + (size_t)(rows_pad / 8) * kMergeFloats * 32 * 4;
   }
 };
 
@@ -715,54 +720,83 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // ---- segment end: reduce this warp's partial, merge token groups, write the CTA partial
+    // ---- segment end: the token groups' states are merged pairwise, lane by lane (every token
+    // group of a tile group holds the same rows and dims in the same fragment positions), from
+    // the last token group down to group 0 through one shared slot per tile group; group 0 then
+    // reduces l and the offset term over its lanes and writes the CTA partial.
+    float* mslot = red + (size_t)tg * NT * kMergeFloats * 32;
+    for (int kk = p.nkg - 1; kk >= 1; --kk) {
+      if (kg == kk) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int tile = tg * NT + nt;
+        for (int nt = 0; nt < NT; ++nt) {
+          float* q = mslot + (size_t)nt * kMergeFloats * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float lt = warp_sum_g(l[nt][j]);
-        const float ot = warp_sum_g(ov[nt][j]);
-        const int row = 8 * tile + 2 * t + j;
-        float* dst = red + ((size_t)kg * p.rows_pad + row) * kPartialStride;
-        if (g == 0) {
-          dst[0] = m[nt][j];
-          dst[1] = lt;
+          for (int j = 0; j < 2; ++j) {
+            q[32 * j] = m[nt][j];
+            q[32 * (2 + j)] = l[nt][j];
+            q[32 * (4 + j)] = ov[nt][j];
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) q[32 * (6 + 4 * i + c)] = acc[nt][i][c];
         }
-        const float vs = FMT == 0 ? 1.0f : p.v_scale;
+      }
+      named_barrier(1, nwc * 32);
+      if (kg == kk - 1) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int dlo = out_dim<FMT>(i, g), dhi = out_dim<FMT>(i, g + 8);
-          if (FMT == 0) {  // V entered as unpack8_v values: dims of class 2 (i & 1) and 2 (i & 1) + 1
-            dst[2 + dlo] = fmaf(acc[nt][i][j], v_unscale(2 * (i & 1)), ot);
-            dst[2 + dhi] = fmaf(acc[nt][i][2 + j], v_unscale(2 * (i & 1) + 1), ot);
-          } else {
-            dst[2 + dlo] = (acc[nt][i][j] + ot) * vs;
-            dst[2 + dhi] = (acc[nt][i][2 + j] + ot) * vs;
+        for (int nt = 0; nt < NT; ++nt) {
+          const float* q = mslot + (size_t)nt * kMergeFloats * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float mo = q[32 * j];
+            const float mn = fmaxf(m[nt][j], mo);
+            const float mu = mn == -INFINITY ? 0.0f : mn;
+            const float a = fast_exp2(m[nt][j] - mu), bo = fast_exp2(mo - mu);
+            l[nt][j] = fmaf(l[nt][j], a, q[32 * (2 + j)] * bo);
+            ov[nt][j] = fmaf(ov[nt][j], a, q[32 * (4 + j)] * bo);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc[nt][i][j] = fmaf(acc[nt][i][j], a, q[32 * (6 + 4 * i + j)] * bo);
+              acc[nt][i][2 + j] = fmaf(acc[nt][i][2 + j], a, q[32 * (6 + 4 * i + 2 + j)] * bo);
+            }
+            m[nt][j] = mn;
+          }
+        }
+      }
+      named_barrier(1, nwc * 32);
+    }
+    if (kg == 0) {
+      float* dstp = p.partials + ((size_t)(blockIdx.x + seg) * R) * kPartialStride;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int tile = tg * NT + nt;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float lt = warp_sum_g(l[nt][j]);
+          const float ot = warp_sum_g(ov[nt][j]);
+          const int row = 8 * tile + 2 * t + j;
+          if (row >= R) continue;
+          float* dst = dstp + (size_t)row * kPartialStride;
+          if (g == 0) {
+            dst[0] = m[nt][j];
+            dst[1] = lt;
+          }
+          const float vs = FMT == 0 ? 1.0f : p.v_scale;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int dlo = out_dim<FMT>(i, g), dhi = out_dim<FMT>(i, g + 8);
+            if (FMT == 0) {  // V entered as unpack8_v values: dims of class 2 (i & 1) and 2 (i & 1) + 1
+              dst[2 + dlo] = fmaf(acc[nt][i][j], v_unscale(2 * (i & 1)), ot);
+              dst[2 + dhi] = fmaf(acc[nt][i][2 + j], v_unscale(2 * (i & 1) + 1), ot);
+            } else {
+              dst[2 + dlo] = (acc[nt][i][j] + ot) * vs;
+              dst[2 + dhi] = (acc[nt][i][2 + j] + ot) * vs;
+            }
           }
         }
       }
     }
-    named_barrier(1, nwc * 32);
-    float* dstp = p.partials + ((size_t)(blockIdx.x + seg) * R) * kPartialStride;
-    for (int e = threadIdx.x; e < R * kPartialStride; e += nwc * 32) {
-      const int row = e / kPartialStride, c = e - row * kPartialStride;
-      float M = -INFINITY;
-      for (int kk = 0; kk < p.nkg; ++kk) M = fmaxf(M, red[((size_t)kk * p.rows_pad + row) * kPartialStride]);
-      float v;
-      if (c == 0) {
-        v = M;
-      } else {
-        const float Mu = M == -INFINITY ? 0.0f : M;
-        v = 0.0f;
-        for (int kk = 0; kk < p.nkg; ++kk) {
-          const float* src = red + ((size_t)kk * p.rows_pad + row) * kPartialStride;
-          v += fast_exp2(src[0] - Mu) * src[c];
-        }
-      }
-      dstp[e] = v;
-    }
-    named_barrier(1, nwc * 32);
     seg_start = seg_end;
   }
 
