@@ -97,18 +97,18 @@ constexpr int kMergeFloats = 6 + 32;
 
 // Shared-memory layout, identical on host (sizing) and device.
 struct SmemLayout {
-  size_t stages, full, empty, valid, pre, flags, red, total;
+  size_t stages, full, empty, valid, red, pre, flags, total;
   __host__ __device__ SmemLayout(int fmt, int nstages, int B, int nkg, int rows_pad) {
     const size_t stage = fmt == 0 ? kStage4 : kStage8;
     stages = 0;
     full = align_up(stages + nstages * stage, 16);
     empty = full + 8 * nstages;
     valid = empty + 8 * nstages;
-    pre = valid + 4 * nstages;
-    flags = pre + 4 * (B + 1);
-    red = align_up(flags + 16, 16);
+    red = align_up(valid + 4 * nstages, 16);
     // one merge slot per tile group: kMergeFloats floats per lane per 8-row tile (lane-major)
-    total = red + (size_t)(rows_pad / 8) * kMergeFloats * 32 * 4;
+    pre = align_up(red + (size_t)(rows_pad / 8) * kMergeFloats * 32 * 4, 128);
+    flags = pre + 4 * (B + 1);
+    total = align_up(flags + 16, 16);
   }
 };
 
