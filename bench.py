@@ -292,8 +292,8 @@ def run_verify(device, steps=30, warmup=3):
     """The speculative-verify workload: 64 sequences at 16,384 context, 20/4 heads, S = 1, 4 and 8
     query rows per sequence with the S new K/V rows rotated, quantised and appended inside the
     call (at the same positions every repetition), one int4 layer. S = 8 (40 rows per KV head) is
-    timed with both many-row kernels (the mma.sync shared-tile kernel, the default, and the
-    tcgen05 variant selected by KVQ_MANY_ROWS_KERNEL)."""
+    timed with the default split-K kernel and with the two kernels KVQ_MANY_ROWS_KERNEL selects
+    for many rows (the mma.sync shared-tile kernel and the tcgen05 variant)."""
     import os
 
     import torch
@@ -317,7 +317,7 @@ def run_verify(device, steps=30, warmup=3):
     st.prefill_int4(0, w.ctx, fill, chunk_tokens=32768)
     ctx = torch.from_numpy(w.ctx.astype(np.int32)).to(device)
     rows = []
-    for S, kernel in ((1, None), (4, None), (8, "tile"), (8, "tcgen05")):
+    for S, kernel in ((1, None), (4, None), (8, None), (8, "tile"), (8, "tcgen05")):
         q = torch.empty((w.B, S, w.Hq, 128), dtype=torch.bfloat16, device=device)
         kn = torch.empty((w.B, S, w.Hkv, 128), dtype=torch.bfloat16, device=device)
         vn = torch.empty_like(kn)
@@ -347,7 +347,7 @@ def run_verify(device, steps=30, warmup=3):
         assert st.read_error() == 0
         t = statistics.median([e0.elapsed_time(e1) for e0, e1 in evs]) * 1e-3
         by = int((w.ctx + S).sum()) * w.Hkv * 136
-        rows.append({"S": S, "rows_per_kv_head": S * w.G, "many_row_kernel": kernel or "-",
+        rows.append({"S": S, "rows_per_kv_head": S * w.G, "many_row_kernel": kernel or "split",
                      "int4_call_us": round(t * 1e6, 1), "hbm_gbs": round(by / t / 1e9, 1),
                      "query_rows_per_s": round(w.B * S / t, 1)})
     del st

@@ -55,6 +55,22 @@ namespace {
 #ifndef KVQ_INT4_MAXREG
 #define KVQ_INT4_MAXREG 168
 #endif
+// int4 split kernel with 2 or 3 row tiles in one warp (one CTA per SM: about 250 registers a
+// thread): 7 token groups, so 8 warps, two per SM sub-partition (4 -> 7: 300 -> 248 us at S = 2
+// on the 64k workload), and 14 stages.
+#ifndef KVQ_TILES3_TOKEN_GROUPS
+#define KVQ_TILES3_TOKEN_GROUPS 7
+#endif
+#ifndef KVQ_TILES3_STAGES
+#define KVQ_TILES3_STAGES 14
+#endif
+// 4 to 6 row tiles: two tile groups of up to 3 tiles, 3 token groups (7 warps), 6 stages.
+#ifndef KVQ_TILES6_TOKEN_GROUPS
+#define KVQ_TILES6_TOKEN_GROUPS 3
+#endif
+#ifndef KVQ_TILES6_STAGES
+#define KVQ_TILES6_STAGES 6
+#endif
 // A consumer warp takes pages kg, kg + nkg, ... and page k lands in stage k mod nstages with
 // phase parity (k / nstages) & 1. Parity only tells adjacent phases apart, so every stage
 // must belong to one consumer warp (nstages a multiple of nkg); otherwise a warp running
@@ -826,12 +842,10 @@ constexpr int kVBuf = 2 * kPage * kTileRow + kPage * 16;     // K16, V16, meta
 #ifndef KVQ_VERIFY_CONV
 #define KVQ_VERIFY_CONV 2
 #endif
-// row tiles (8 query rows each) from which the shared-tile kernel is used
-// many-row calls through the tcgen05 kernel (1) or the shared-tile mma.sync kernel (0) unless
-// the environment variable KVQ_MANY_ROWS_KERNEL names one ("tcgen05" or "tile")
-#ifndef KVQ_VERIFY_TC
-#define KVQ_VERIFY_TC 0
-#endif
+// Row tiles (8 query rows each) from which the environment variable KVQ_MANY_ROWS_KERNEL may
+// select this shared-tile kernel ("tile") or the tcgen05 kernel ("tcgen05") instead of the split
+// kernel, which is the default for every call (faster at 5 and 6 tiles as well: 516 against
+// 560 us at S = 8, GQA 5, 64 x 16,384).
 #ifndef KVQ_VERIFY_MIN_TILES
 #define KVQ_VERIFY_MIN_TILES 5
 #endif
@@ -2032,20 +2046,20 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
   const int ntiles = (p.R + 7) / 8;
   if (job.fmt == 0 && ntiles >= KVQ_VERIFY_MIN_TILES) {
     const char* sel = getenv("KVQ_MANY_ROWS_KERNEL");
-    const bool tc = sel ? strcmp(sel, "tcgen05") == 0 : KVQ_VERIFY_TC != 0;
-    return tc ? launch_tc(p, p_max, stream) : launch_verify(p, ntiles, p_max, stream);
+    if (sel && strcmp(sel, "tcgen05") == 0) return launch_tc(p, p_max, stream);
+    if (sel && strcmp(sel, "tile") == 0) return launch_verify(p, ntiles, p_max, stream);
   }
   int NT;
   if (ntiles <= 3) {
     NT = ntiles;
     p.ntg = 1;
-    p.nkg = NT == 1 ? KVQ_TOKEN_GROUPS : 4;
-    p.nstages = NT == 1 ? KVQ_STAGES_INT4 : 8;
+    p.nkg = NT == 1 ? KVQ_TOKEN_GROUPS : (job.fmt == 0 ? KVQ_TILES3_TOKEN_GROUPS : 4);
+    p.nstages = NT == 1 ? KVQ_STAGES_INT4 : (job.fmt == 0 ? KVQ_TILES3_STAGES : 8);
   } else {
     NT = (ntiles + 1) / 2;
     p.ntg = 2;
-    p.nkg = 2;
-    p.nstages = 4;
+    p.nkg = job.fmt == 0 ? KVQ_TILES6_TOKEN_GROUPS : 2;
+    p.nstages = job.fmt == 0 ? KVQ_TILES6_STAGES : 4;
   }
   if (job.fmt == 1) {  // window rings too large for one cluster per (sequence, KV head)
     p.nkg = NT == 1 ? 4 : 2;
