@@ -835,11 +835,7 @@ def run_kvq(args, rank, world, local):
             "metric": METRIC, "value": round(value, 2), "unit": "session-steps/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u4", "data": "synthetic",
-            "config": {"workload": "decode step at 256k: 8 sequences x 262,144 context, 50 layers "
-                                   "(10 rotated int4 + 40 FP8 window 513), 20/4 heads x 128, bf16 inputs, 1 query row",
-                       "prologue": args.prologue,
-                       "global_batch": 8 * world, "seq_len": int(bench_ctx0()), "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (11.4 GB of int4 cache read per step)"},
+            "config": step_config(args, world),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(frac, 4), "traffic": attn_traffic(int(np.mean(call_bytes))),
                          "traffic_how": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the attention kernel "
@@ -863,6 +859,15 @@ def run_kvq(args, rank, world, local):
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
+
+
+def step_config(args, world):
+    """The `config` of both arms' JSON line: the 256k decode step."""
+    return {"workload": "decode step at 256k: 8 sequences x 262,144 context, 50 layers "
+                        "(10 rotated int4 + 40 FP8 window 513), 20/4 heads x 128, bf16 inputs, 1 query row",
+            "prologue": args.prologue,
+            "global_batch": 8 * world, "seq_len": int(bench_ctx0()), "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (11.4 GB of int4 cache read per step)"}
 
 
 def bench_ctx0():
@@ -904,7 +909,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_sample * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": "decode step at 256k (oracle sample)", "global_batch": 8, "seq_len": L - 1},
+            "config": step_config(args, world),
             "cpu_baseline": {"value": round(value, 5), "unit": "session-steps/s", "cores": O.threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 5), "unit": "session-steps/s", "h2d_bytes_per_step": 0,
