@@ -265,6 +265,23 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
                                    kvq_stream_t stream);
 
 /*
+ * kvq_fp8_swa_plan -- the launch shape kvq_decode_attn_fp8_swa takes for these sizes on the
+ * calling thread's current device; no launch, nothing allocated (reads device attributes and
+ * the kernel's occupancy, cached per device).
+ *   out[0]: CTAs per (sequence, KV head): the cluster size of the one-launch path, which
+ *           appends and attends in one kernel and merges on chip; 1 also for the
+ *           one-CTA-per-pair shape taken when the call has at least as many (sequence, KV head)
+ *           pairs as the device has SMs; 0 where the one-launch path does not fit (rings
+ *           beyond one cluster; 40 or more query rows per KV head with fewer pairs than SMs),
+ *           which takes a separate append, the split-K kernel and its combine pass.
+ *   out[1]: unit streams (warps per query-tile group) per CTA; out[2]: copy stages per stream;
+ *   out[3]: 32-slot ring units per stream (the largest; 0 with out[0] = 0).
+ * Returns KVQ_ERR_INVALID_ARG / KVQ_ERR_UNSUPPORTED under the same conditions on these
+ * arguments as kvq_decode_attn_fp8_swa (capacity a positive multiple of 64).
+ */
+kvq_status kvq_fp8_swa_plan(int capacity, int B, int S, int num_q_heads, int num_kv_heads, int32_t out[4]);
+
+/*
  * kvq_decode_attn_int4_noalloc -- the same computation as kvq_decode_attn_int4 for callers
  * that cannot allocate device memory at decode time (an engine that hands all free GPU
  * memory to its KV pool at start-up, a thread that must not touch the device allocator, an

@@ -62,6 +62,8 @@ def _load():
         getattr(L, name).argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, vp, vp, f32, vp, vp]
     L.kvq_decode_workspace_bytes.restype = sz
     L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.kvq_fp8_swa_plan.restype = i32
+    L.kvq_fp8_swa_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
     for name in ("kvq_decode_attn_int4", "kvq_decode_attn_int4_fwht"):
         getattr(L, name).restype = i32
         getattr(L, name).argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, f32,
@@ -202,6 +204,13 @@ def kvq_rotate_quant_append(cache: Int4Cache, Mk, k, v, seq_ids, positions, dev_
 
 def kvq_decode_workspace_bytes(B: int, S: int, num_q_heads: int, num_kv_heads: int) -> int:
     return int(lib.kvq_decode_workspace_bytes(B, S, num_q_heads, num_kv_heads))
+
+
+def kvq_fp8_swa_plan(capacity: int, B: int, S: int, num_q_heads: int, num_kv_heads: int) -> tuple:
+    """(CTAs per pair or 0 for the split-K path, streams per CTA, stages, units per stream)."""
+    out = (ctypes.c_int32 * 4)()
+    _check("kvq_fp8_swa_plan", lib.kvq_fp8_swa_plan(capacity, B, S, num_q_heads, num_kv_heads, out))
+    return tuple(int(x) for x in out)
 
 
 def kvq_decode_attn_int4(cache: Int4Cache, Mq, Mk, q, ctx_len, out, workspace, dev_err, k_new=None, v_new=None,

@@ -233,6 +233,17 @@ kvq_status kvq_decode_attn_int4_fwht(const kvq_int4_cache* cache, const float* w
                           workspace, workspace_bytes, q_rot_out, dev_err, stream, 1);
 }
 
+kvq_status kvq_fp8_swa_plan(int capacity, int B, int S, int num_q_heads, int num_kv_heads, int32_t out[4]) {
+  if (!out) return KVQ_ERR_INVALID_ARG;
+  if (capacity < KVQ_PAGE_SIZE || capacity % KVQ_PAGE_SIZE || num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;
+  if (S < 1 || S > 8 || !heads_ok(num_q_heads, num_kv_heads, S)) return KVQ_ERR_UNSUPPORTED;
+  if (B < 1 || B > KVQ_MAX_SEQS) return KVQ_ERR_INVALID_ARG;
+  int shape[4];
+  kvq::swa_plan_shape(capacity, B, S, num_q_heads, num_kv_heads, shape);
+  for (int i = 0; i < 4; ++i) out[i] = shape[i];
+  return KVQ_OK;
+}
+
 kvq_status kvq_fp8_append(const kvq_fp8_ring* ring, const void* k, const void* v, kvq_dtype dtype, int T,
                           const int32_t* seq_ids, const int32_t* positions, float k_scale, float v_scale,
                           int32_t* dev_err, kvq_stream_t stream) {
@@ -282,7 +293,7 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
   cudaStream_t s = (cudaStream_t)stream;
   // Rings that one cluster per (sequence, KV head) covers: one launch that appends the new
   // rows and attends. Larger rings: a separate append, then the split-K path and its combine.
-  const bool cluster = kvq::swa_cluster_path(ring->capacity, S, num_q_heads, ring->num_kv_heads);
+  const bool cluster = kvq::swa_cluster_path(ring->capacity, B, S, num_q_heads, ring->num_kv_heads);
   if (k_new && !cluster) {
     kvq::Fp8AppendJob j{};
     j.ring = *ring;

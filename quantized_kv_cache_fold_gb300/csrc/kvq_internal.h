@@ -82,10 +82,12 @@ struct AttnJob {
 cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream);
 
 // FP8 window attention with one thread-block cluster per (sequence, KV head), appending
-// job.k_new / job.v_new itself. swa_cluster_path() says whether a ring of this capacity and
-// these head counts takes it; larger rings go through launch_attention (fmt 1) after a
-// separate append.
-bool swa_cluster_path(int capacity, int S, int Hq, int Hkv);
+// job.k_new / job.v_new itself. swa_cluster_path() says whether a ring of this capacity, with
+// this batch and these head counts, takes it; larger rings go through launch_attention (fmt 1)
+// after a separate append.
+bool swa_cluster_path(int capacity, int B, int S, int Hq, int Hkv);
+// The chosen shape: CTAs per pair (0: split-K path), streams per CTA, stages, units per stream.
+void swa_plan_shape(int capacity, int B, int S, int Hq, int Hkv, int out[4]);
 cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream);
 
 // Workspace layout shared by the API and the launchers.

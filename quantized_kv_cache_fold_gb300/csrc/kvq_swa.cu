@@ -9,7 +9,10 @@
 // A window is a few hundred positions: far too little work to spread over a whole grid and
 // merge through global memory, and far too much latency for one SM to pull and process alone.
 // Here the ring is cut into 32-slot units spread over the warps of one cluster (at most 8
-// CTAs), and the partial softmax states are merged on chip:
+// CTAs), and the partial softmax states are merged on chip. With many (sequence, KV head)
+// pairs (at least one per SM) the pairs themselves fill the GPU: then each pair gets one CTA
+// (a cluster of one) whose few unit streams take several units each in turn, as many streams
+// as still let the whole grid be resident at once, and there is nothing to push:
 //
 //   warp (unit stream w, tile group tg): streams the units u = w, w + NS, w + 2 NS, ...
 //     (NS = streams in the cluster) through its own one- or two-stage shared-memory buffer,
@@ -47,6 +50,10 @@ namespace {
 #ifndef KVQ_SWA_STREAMS
 #define KVQ_SWA_STREAMS 6
 #endif
+// Stages per unit stream in the one-CTA-per-pair plan.
+#ifndef KVQ_SWA_BATCH_STAGES
+#define KVQ_SWA_BATCH_STAGES 2
+#endif
 
 constexpr int kBlk = 2 * kPage * kRec8;  // 16384 bytes per 64-slot ring block (K half, V half)
 constexpr int kUnit = 32;                // slots per work unit
@@ -57,6 +64,7 @@ constexpr int kPushBytes = 8 + 4 * kD;   // bytes pushed per query row: (m, l) a
 constexpr int kMaxCluster = 8;
 constexpr int kMaxStreams = 8;           // unit streams per CTA (merge loops are unrolled to this)
 constexpr int kMaxUnitsPerStream = 4;    // beyond this the split-K path with a combine pass is used
+constexpr int kMaxUnitsBatched = 18;     // one-CTA-per-pair plan: a 576-slot ring through one stream
 constexpr size_t kSmemCap = 200 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -77,21 +85,24 @@ struct SwaParams {
 
 struct SwaPlan {
   int NT, ntg, nws, cs, nst, rows_pad, ups;
+  bool batched;  // one CTA per pair, streams of up to kMaxUnitsBatched units
   size_t smem;
 };
 
 // Shared memory: stages [warp][nst][kStg], the warps' copy barriers [warp][nst] and the
-// receive barrier, partials [warp][NT*8][132], the receive area [cs][rows_pad][132].
+// receive barrier, partials [warp][NT*8][132], the receive area [cs - 1][rows_pad][132] (CTA 0
+// of the cluster receives from ranks 1 .. cs - 1).
 struct SwaSmem {
   size_t bars, part, recv, total;
   __host__ __device__ SwaSmem(int nw, int nst, int NT, int cs, int rows_pad) {
     bars = (size_t)nw * nst * kStg;
     part = (bars + 8 * ((size_t)nw * nst + 1) + 15) / 16 * 16;
     recv = part + (size_t)nw * NT * 8 * kRedStride * 4;
-    total = recv + (size_t)cs * rows_pad * kRedStride * 4;
+    total = recv + (size_t)(cs - 1) * rows_pad * kRedStride * 4;
   }
 };
 
+// Cluster plan: the ring's units over the warps of one cluster per (sequence, KV head).
 SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
   SwaPlan pl{};
   const int nunits = cap / kUnit;
@@ -105,8 +116,8 @@ SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
     pl.ntg = 2;
   }
   pl.rows_pad = pl.ntg * pl.NT * 8;
-  for (int nws = std::min(KVQ_SWA_STREAMS, kMaxStreams); nws >= 1; --nws) {
-    if (nws * pl.ntg * 32 > 256) continue;
+  const int nws_max = std::min(std::min(KVQ_SWA_STREAMS, kMaxStreams), 256 / (32 * pl.ntg));
+  for (int nws = nws_max; nws >= 1; --nws) {
     pl.nws = nws;
     pl.cs = std::min(kMaxCluster, (nunits + nws - 1) / nws);
     const int ns = pl.cs * nws;
@@ -116,7 +127,7 @@ SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
       if (pl.smem <= kSmemCap) return pl;
     }
   }
-  pl.smem = 0;  // does not fit (cannot happen for rows_pad <= 48)
+  pl.smem = 0;  // does not fit (40 or more query rows per KV head): the split-K path
   return pl;
 }
 
@@ -532,7 +543,7 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       a[7] = fmaf(wgt, v1.w, a[7]);
     }
     if (rank != 0) {
-      const uint32_t dst = recv0 + 4u * (uint32_t)((rank * p.rows_pad + row) * kRedStride);
+      const uint32_t dst = recv0 + 4u * (uint32_t)(((rank - 1) * p.rows_pad + row) * kRedStride);
       if (c8 == 0) st_async_f32x2(dst, M, lsum, bar0);
       st_async_f32x4(dst + 16 + 32 * c8, make_float4(a[0], a[1], a[2], a[3]), bar0);
       st_async_f32x4(dst + 32 + 32 * c8, make_float4(a[4], a[5], a[6], a[7]), bar0);
@@ -548,7 +559,7 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     float Mc = M;
 #pragma unroll
     for (int rr = 1; rr < kMaxCluster; ++rr) {
-      mr[rr] = rr < p.cs ? recv[(rr * p.rows_pad + row) * kRedStride] : -INFINITY;
+      mr[rr] = rr < p.cs ? recv[((rr - 1) * p.rows_pad + row) * kRedStride] : -INFINITY;
       Mc = fmaxf(Mc, mr[rr]);
     }
     const float Mcu = Mc == -INFINITY ? 0.0f : Mc;
@@ -559,7 +570,7 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
 #pragma unroll
     for (int rr = 1; rr < kMaxCluster; ++rr) {
       if (rr >= p.cs) break;
-      const float* sr = recv + (rr * p.rows_pad + row) * kRedStride;
+      const float* sr = recv + ((rr - 1) * p.rows_pad + row) * kRedStride;
       const float wgt = fast_exp2(mr[rr] - Mcu);
       const float4 v0 = reinterpret_cast<const float4*>(sr + 4)[2 * c8];
       const float4 v1 = reinterpret_cast<const float4*>(sr + 4)[2 * c8 + 1];
@@ -583,9 +594,23 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
 
 struct SwaDevCache {
   bool attr[4] = {false};
+  int sm = 0;
+  int occ[4][3][kMaxStreams + 1][KVQ_SWA_BATCH_STAGES + 1] = {};  // resident CTAs per SM by [NT][ntg][nws][nst]
 };
 SwaDevCache g_swa_dev[64];
 std::mutex g_swa_mu;  // guards g_swa_dev
+
+SwaDevCache& dev_cache(int dev) { return g_swa_dev[(dev >= 0 && dev < 64) ? dev : 0]; }
+
+// Call with g_swa_mu held: allow the kernel its dynamic shared memory (once per device).
+template <int NT>
+cudaError_t ensure_attr(SwaDevCache& dc) {
+  if (dc.attr[NT]) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(swa_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
+  if (e == cudaSuccess) dc.attr[NT] = true;
+  return e;
+}
 
 template <int NT>
 cudaError_t launch_swa_t(const SwaParams& p, size_t smem, cudaStream_t stream) {
@@ -593,13 +618,8 @@ cudaError_t launch_swa_t(const SwaParams& p, size_t smem, cudaStream_t stream) {
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(g_swa_mu);
-    SwaDevCache& dc = g_swa_dev[(dev >= 0 && dev < 64) ? dev : 0];
-    if (!dc.attr[NT]) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(swa_cluster_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
-      if (e != cudaSuccess) return e;
-      dc.attr[NT] = true;
-    }
+    const cudaError_t e = ensure_attr<NT>(dev_cache(dev));
+    if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)((long long)p.B * p.Hkv * p.cs), 1, 1);
@@ -619,15 +639,110 @@ cudaError_t launch_swa_t(const SwaParams& p, size_t smem, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, swa_cluster_kernel<NT>, p);
 }
 
+template <int NT>
+int occupancy_t(int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swa_cluster_kernel<NT>, threads, smem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+struct DeviceShape {
+  int dev, sm;
+};
+
+// Current device and its SM count (sm = 0 if it cannot be read: then only the cluster plans apply).
+DeviceShape device_shape() {
+  DeviceShape d{0, 0};
+  if (cudaGetDevice(&d.dev) != cudaSuccess) return d;
+  std::lock_guard<std::mutex> lock(g_swa_mu);
+  SwaDevCache& dc = dev_cache(d.dev);
+  if (dc.sm == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d.dev) != cudaSuccess) return d;
+    dc.sm = n;
+  }
+  d.sm = dc.sm;
+  return d;
+}
+
+// Resident one-CTA-per-pair CTAs per SM for this plan shape (0 if unknown).
+int ctas_per_sm(int dev, const SwaPlan& pl) {
+  std::lock_guard<std::mutex> lock(g_swa_mu);
+  SwaDevCache& dc = dev_cache(dev);
+  int& o = dc.occ[pl.NT][pl.ntg][pl.nws][pl.nst];
+  if (o == 0) {
+    const int threads = pl.nws * pl.ntg * 32;
+    cudaError_t e;
+    switch (pl.NT) {
+      case 1: e = ensure_attr<1>(dc); o = e == cudaSuccess ? occupancy_t<1>(threads, pl.smem) : 0; break;
+      case 2: e = ensure_attr<2>(dc); o = e == cudaSuccess ? occupancy_t<2>(threads, pl.smem) : 0; break;
+      default: e = ensure_attr<3>(dc); o = e == cudaSuccess ? occupancy_t<3>(threads, pl.smem) : 0; break;
+    }
+  }
+  return o;
+}
+
+// The plan for a call. With at least as many (sequence, KV head) pairs as SMs the pairs fill
+// the GPU unsplit: one CTA per pair, its units over nws streams. The grid then runs in
+// ceil(pairs / (SMs x resident CTAs)) rounds of up to ceil(units / nws) units per stream; nws
+// takes the fewest rounds, then the fewest units per stream (a later round of CTAs costs more
+// than longer streams in one), then the fewest streams. With fewer pairs the cluster plan.
+SwaPlan choose_plan(int cap, int B, int S, int Hq, int Hkv) {
+  const SwaPlan cl = make_plan(cap, S, Hq, Hkv);
+  const long long pairs = (long long)B * Hkv;
+  const DeviceShape d = device_shape();
+  if (d.sm <= 0 || pairs < d.sm) return cl;
+  const int nunits = cap / kUnit;
+  const int nws_max = std::min(std::min(KVQ_SWA_STREAMS, kMaxStreams), 256 / (32 * cl.ntg));
+  SwaPlan best{};
+  long long best_cost = -1;
+  for (int nws = 1; nws <= nws_max; ++nws) {
+    SwaPlan pl = cl;
+    pl.nws = nws;
+    pl.cs = 1;
+    pl.ups = (nunits + nws - 1) / nws;
+    if (pl.ups > kMaxUnitsBatched) continue;
+    pl.batched = true;
+    pl.smem = 0;
+    for (pl.nst = std::min(KVQ_SWA_BATCH_STAGES, pl.ups); pl.nst >= 1; --pl.nst) {
+      const size_t bytes = SwaSmem(nws * pl.ntg, pl.nst, pl.NT, 1, pl.rows_pad).total;
+      if (bytes <= kSmemCap) {
+        pl.smem = bytes;
+        break;
+      }
+    }
+    if (pl.smem == 0) continue;
+    const int occ = ctas_per_sm(d.dev, pl);
+    if (occ <= 0) continue;
+    const long long slots = (long long)d.sm * occ;
+    const long long cost = (pairs + slots - 1) / slots * 1000 + pl.ups;
+    if (best_cost < 0 || cost < best_cost) {
+      best = pl;
+      best_cost = cost;
+    }
+  }
+  return best_cost < 0 ? cl : best;
+}
+
 }  // namespace
 
-bool swa_cluster_path(int capacity, int S, int Hq, int Hkv) {
-  const SwaPlan pl = make_plan(capacity, S, Hq, Hkv);
-  return pl.smem != 0 && pl.ups <= kMaxUnitsPerStream;
+bool swa_cluster_path(int capacity, int B, int S, int Hq, int Hkv) {
+  const SwaPlan pl = choose_plan(capacity, B, S, Hq, Hkv);
+  return pl.smem != 0 && (pl.batched || pl.ups <= kMaxUnitsPerStream);
+}
+
+void swa_plan_shape(int capacity, int B, int S, int Hq, int Hkv, int out[4]) {
+  const SwaPlan pl = choose_plan(capacity, B, S, Hq, Hkv);
+  const bool cluster = pl.smem != 0 && (pl.batched || pl.ups <= kMaxUnitsPerStream);
+  out[0] = cluster ? pl.cs : 0;
+  out[1] = cluster ? pl.nws : 0;
+  out[2] = cluster ? pl.nst : 0;
+  out[3] = cluster ? pl.ups : 0;
 }
 
 cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream) {
-  const SwaPlan pl = make_plan(job.ring.capacity, job.S, job.Hq, job.Hkv);
+  const SwaPlan pl = choose_plan(job.ring.capacity, job.B, job.S, job.Hq, job.Hkv);
   SwaParams p{};
   p.ring = job.ring.data;
   p.cap = job.ring.capacity;

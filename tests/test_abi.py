@@ -95,6 +95,13 @@ def test_host_validation_rejects_before_launch():
     bad_ring = kvq.Fp8Ring(0x10000, 4, 4, 500, 128)
     assert f(ctypes.byref(bad_ring), 0x80000, 1, 2, 1, 20, 0x90000, 400, None, None, 0.01, 0.01, 0.088, 0xA0000,
              0xB0000, 1 << 30, 0xC0000, None) == 1  # capacity not a multiple of 64
+    shape = (ctypes.c_int32 * 4)()
+    plan = kvq.lib.kvq_fp8_swa_plan
+    assert plan(500, 8, 1, 20, 4, shape) == 1       # capacity not a multiple of 64
+    assert plan(576, 8, 9, 20, 4, shape) == 2       # more than 8 rows
+    assert plan(576, 8, 1, 21, 4, shape) == 2       # query heads not a multiple of KV heads
+    assert plan(576, 0, 1, 20, 4, shape) == 1
+    assert plan(576, 8, 1, 20, 4, None) == 1
     assert kvq.lib.kvq_build_rotation(1, 64, None, 0x1000) == 2
     assert kvq.lib.kvq_rotate_quant_append(ctypes.byref(c), 0x1000, 0x2000, 0x3000, 1, 0, None, None, 1e-6, None,
                                            None) == 0  # T == 0 is a no-op

@@ -12,7 +12,7 @@ import torch
 import synth
 from gpu_util import (assert_close, device_kv, device_new_kv, device_q, oracle_int4_seq, oracle_layer_params,
                       oracle_swa_seq, unpack_fp8, unpack_int4)
-from quantized_kv_cache_fold_gb300 import DEVERR_NONFINITE, DEVERR_PAGE, DEVERR_POS, KvqError
+from quantized_kv_cache_fold_gb300 import DEVERR_NONFINITE, DEVERR_PAGE, DEVERR_POS, KvqError, kvq_fp8_swa_plan
 from quantized_kv_cache_fold_gb300.runner import DecodeStack
 from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, Workload, config
 
@@ -215,7 +215,9 @@ def build_swa(w, layer, S, cap=576, window=513):
     return st
 
 
-def check_swa(orc, w, layer, S, window=513, cap=576):
+def check_swa(orc, w, layer, S, window=513, cap=576, sample=None):
+    """Window layer of the call against the oracle: every sequence, or the sequences in
+    `sample` (all outputs still checked to be finite)."""
     st = build_swa(w, layer, S, cap, window)
     ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
     q = device_q(w, layer, S, w.ctx, swa=True)
@@ -226,7 +228,8 @@ def check_swa(orc, w, layer, S, window=513, cap=576):
     torch.cuda.synchronize()
     assert st.read_error() == 0, f"device error word {st.read_error():#x}"
     out = out.cpu().numpy()
-    for b in range(w.B):
+    assert np.isfinite(out).all()
+    for b in (range(w.B) if sample is None else sample):
         for h in range(w.Hkv):
             kc, vc, positions, ref = oracle_swa_seq(orc, w, layer, b, h, S, int(w.ctx[b]), window)
             gk, gv = unpack_fp8(st.layers[0].tensors, b, h, positions)
@@ -263,10 +266,39 @@ def test_swa_large_ring_general_path(orc):
 
 
 def test_swa_many_sequences(orc):
-    """40 sequences x 4 KV heads: 160 clusters of 5 CTAs, more CTAs than SMs."""
+    """40 sequences x 4 KV heads: 160 clusters of 3 CTAs, more CTAs than SMs."""
     ctx = (np.arange(40) * 97 % 1500).astype(np.int64)
     w = Workload("swa-many", 26, len(ctx), 20, 4, 1, ctx, True)
     check_swa(orc, w, 4, 1)
+
+
+ONE_CTA_PER_PAIR = [(420, 1), (300, 1), (160, 1), (110, 1), (55, 1), (200, 4), (120, 8)]
+
+
+def test_swa_plan_shapes():
+    """Window launch shapes: a cluster of several CTAs per (sequence, KV head) for few pairs,
+    one CTA per pair once there are as many pairs as SMs (with different stream counts over
+    the batches below), the split-K path for a ring beyond one cluster."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = {(B, S): kvq_fp8_swa_plan(576, B, S, 20, 4) for B, S in ONE_CTA_PER_PAIR}
+    for (B, S), (cs, nws, nst, ups) in shapes.items():
+        assert (cs == 1) == (4 * B >= sms), (B, S, cs)
+        assert nws >= 1 and 1 <= nst <= ups and nws * ups >= 18
+    if sms <= 220:
+        assert len({sh[1] for sh in shapes.values() if sh[0] == 1}) >= 3
+    assert kvq_fp8_swa_plan(576, 8, 1, 20, 4)[0] > 1
+    assert kvq_fp8_swa_plan(8192, 2, 2, 20, 4) == (0, 0, 0, 0)
+
+
+@pytest.mark.parametrize("B,S", ONE_CTA_PER_PAIR)
+def test_swa_one_cta_per_pair(orc, B, S):
+    """Batches whose (sequence, KV head) pairs fill the GPU unsplit (on 152 SMs): one CTA per
+    pair, its 18 ring units over one to a few streams of several units each (ragged when the
+    count does not divide 18; S = 8 with two tile groups). Contexts from 0 to 2999: early
+    rings, full windows, wrap-around. Every seventh sequence and the last against the oracle."""
+    ctx = (np.arange(B) * 389 % 3000).astype(np.int64)
+    w = Workload(f"swa-pairs{B}x{S}", 28, B, 20, 4, S, ctx, True)
+    check_swa(orc, w, 6, S, sample=sorted(set(range(0, B, 7)) | {B - 1}))
 
 
 def test_swa_nonfinite_row_and_bad_position_flagged(orc):
