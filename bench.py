@@ -356,19 +356,22 @@ def run_verify(device, steps=30, warmup=3):
                         "call, one int4 layer, random page order", "points": rows}
 
 
-def run_swa(device, steps=30, warmup=3):
+def run_swa(device, steps=30, warmup=3, sequences=None, layers=None):
     """The 40 FP8 window-513 layers of the 256k step alone (8 sequences x 4 KV heads, 576-slot
     rings, one query row, appended row inside the call), steps captured in one CUDA graph. A
-    small case (a few hundred MB) for profiling the window kernel."""
+    small case (a few hundred MB) for profiling the window kernel. `sequences` replaces the 8
+    sequences by that many, each at the 256k position (the large-batch launch shape); `layers`
+    replaces the 40 layers (a smaller device footprint for profiling)."""
     import torch
 
     import synth
-    from quantized_kv_cache_fold_gb300 import kvq_fp8_append
+    from quantized_kv_cache_fold_gb300 import kvq_fp8_append, kvq_fp8_swa_plan
     from quantized_kv_cache_fold_gb300.runner import DecodeStack
     from synth.workloads import SWA_K_SCALE, SWA_V_SCALE, config
 
     w = config(5)
-    B, S, nL = w.B, 1, w.swa_layers
+    ctx_all = w.ctx if sequences is None else np.full(sequences, int(w.ctx[0]), np.int64)
+    B, S, nL = len(ctx_all), 1, (w.swa_layers if layers is None else layers)
     st = DecodeStack(B, w.Hq, w.Hkv, S, 1, n_layers=nL, full_every=nL + 1, ring_capacity=w.ring_capacity,
                      window=w.window, swa_k_scale=SWA_K_SCALE, swa_v_scale=SWA_V_SCALE, device=device)
     stream = torch.cuda.current_stream().cuda_stream
@@ -376,7 +379,7 @@ def run_swa(device, steps=30, warmup=3):
     for l in range(nL):
         L = st.layers[l]
         for b in range(B):
-            P = int(w.ctx[b])
+            P = int(ctx_all[b])
             k = torch.empty((cap, w.Hkv, 128), dtype=torch.bfloat16, device=device)
             v = torch.empty_like(k)
             synth.kv_rows_device(w.seed, l, b, P - cap, cap, w.Hkv, "swa_k", True, k.data_ptr(), stream)
@@ -390,7 +393,7 @@ def run_swa(device, steps=30, warmup=3):
     vn = torch.empty_like(kn)
     for buf, sid in ((q, synth.S_QUERIES), (kn, synth.S_KEYS), (vn, synth.S_VALUES)):
         synth.normals_device(synth.key(w.seed + 1000, sid), 0, buf.numel(), buf.data_ptr(), None, True, stream)
-    pos0 = (torch.from_numpy(w.ctx.astype(np.int32)).to(device)[None, :] +
+    pos0 = (torch.from_numpy(ctx_all.astype(np.int32)).to(device)[None, :] +
             torch.arange(total, dtype=torch.int32, device=device)[:, None]).contiguous()
     out = torch.empty((nL, B, S, w.Hq, 128), dtype=torch.float32, device=device)
 
@@ -416,11 +419,13 @@ def run_swa(device, steps=30, warmup=3):
     torch.cuda.synchronize()
     assert st.read_error() == 0, f"device error word {st.read_error():#x}"
     us = e0.elapsed_time(e1) * 1e3 / (steps * nL)
-    by = int(np.minimum(w.ctx + 1, w.window).sum()) * w.Hkv * 256
+    by = int(np.minimum(ctx_all + 1, w.window).sum()) * w.Hkv * 256
     return {"workload": f"{nL} FP8 window-{w.window} layers of the 256k step: {B} sequences x {w.Hkv} KV heads, "
                         f"{cap}-slot rings, 1 query row, appended row in the call",
-            "window_layer_us": round(us, 2), "bytes_per_layer": by, "layers_per_step": nL,
-            "window_us_per_step": round(us * nL, 1)}
+            "window_layer_us": round(us, 2), "bytes_per_layer": by, "hbm_gbs": round(by / us / 1e3, 1),
+            "layers_per_step": nL, "window_us_per_step": round(us * nL, 1),
+            "launch_shape": dict(zip(("ctas_per_pair", "streams_per_cta", "stages", "units_per_stream"),
+                                     kvq_fp8_swa_plan(cap, B, S, w.Hq, w.Hkv)))}
 
 
 def run_ab(device, steps=30, warmup=3):
@@ -926,6 +931,9 @@ def main():
     ap.add_argument("--prologue", default="matrix", choices=["matrix", "fwht"],
                     help="Q/K prologue of the int4 layers: the folded 128x128 matrices (default) or the "
                          "fast Walsh-Hadamard form (second codec specification)")
+    ap.add_argument("--sequences", type=int, default=None,
+                    help="--only swa: this many sequences instead of the 256k step's 8")
+    ap.add_argument("--layers", type=int, default=None, help="--only swa: this many window layers instead of 40")
     ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity", "verify"],
                     help="run only the 64k single-layer int4 point, only the 40 window layers of the 256k "
                          "step (small cases for profiling), the A/B of full-layer formats (ab), the "
@@ -954,7 +962,8 @@ def main():
     elif args.only == "swa":
         import torch
         torch.cuda.set_device(local)
-        print(json.dumps(run_swa(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+        print(json.dumps(run_swa(f"cuda:{local}", steps=args.steps, warmup=args.warmup, sequences=args.sequences,
+                                 layers=args.layers)), flush=True)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
