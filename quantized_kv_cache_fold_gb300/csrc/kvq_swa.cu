@@ -23,6 +23,7 @@
 //     it into the landed copy, so the appended rows are attended in the same launch;
 //     QK^T and PV on tensor cores (mma.m16n8k16, e4m3 -> f16 exactly), online softmax in
 //     exp2 form, query rows masked outside [max(0, p_r - window + 1), p_r];
+//   a lone stream in a cluster of one normalises its rows and stores them; otherwise
 //   partial (m, l, acc[128]) per stream and query row -> shared memory;
 //   each CTA merges its streams per (row, 8 dims) with log-sum-exp weights and pushes the
 //   result into CTA 0 of the cluster with asynchronous remote stores (st.async) that complete
@@ -94,10 +95,12 @@ struct SwaPlan {
 // of the cluster receives from ranks 1 .. cs - 1).
 struct SwaSmem {
   size_t bars, part, recv, total;
-  __host__ __device__ SwaSmem(int nw, int nst, int NT, int cs, int rows_pad) {
+  // direct: one unit stream per tile group in a cluster of one; each warp's rows are complete
+  // and go straight to the output, so there are no partials.
+  __host__ __device__ SwaSmem(int nw, int nst, int NT, int cs, int rows_pad, bool direct) {
     bars = (size_t)nw * nst * kStg;
     part = (bars + 8 * ((size_t)nw * nst + 1) + 15) / 16 * 16;
-    recv = part + (size_t)nw * NT * 8 * kRedStride * 4;
+    recv = part + (direct ? 0 : (size_t)nw * NT * 8 * kRedStride * 4);
     total = recv + (size_t)(cs - 1) * rows_pad * kRedStride * 4;
   }
 };
@@ -123,7 +126,7 @@ SwaPlan make_plan(int cap, int S, int Hq, int Hkv) {
     const int ns = pl.cs * nws;
     pl.ups = (nunits + ns - 1) / ns;
     for (pl.nst = std::min(2, pl.ups); pl.nst >= 1; --pl.nst) {
-      pl.smem = SwaSmem(nws * pl.ntg, pl.nst, pl.NT, pl.cs, pl.rows_pad).total;
+      pl.smem = SwaSmem(nws * pl.ntg, pl.nst, pl.NT, pl.cs, pl.rows_pad, nws == 1 && pl.cs == 1).total;
       if (pl.smem <= kSmemCap) return pl;
     }
   }
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   const int b = pair / p.Hkv, h = pair - (pair / p.Hkv) * p.Hkv;
   const int stream = rank * p.nws + ws, nstream = p.cs * p.nws;
   const int nu = stream < p.nunits ? (p.nunits - 1 - stream) / nstream + 1 : 0;  // units of this stream
-  const SwaSmem L(nw, p.nst, NT, p.cs, p.rows_pad);
+  const SwaSmem L(nw, p.nst, NT, p.cs, p.rows_pad, p.nws == 1 && p.cs == 1);
   uint8_t* wst = smem + (size_t)warp * p.nst * kStg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* wfull = bars + warp * p.nst;
@@ -482,6 +485,30 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   if (done < nu && lane == 0) {  // gave up: let the copies still in flight land before leaving
     for (int i = done; i < min(nu, done + p.nst); ++i)
       if (!mbar_wait_bounded(&wfull[i % p.nst], (uint32_t)(i / p.nst) & 1u)) break;
+  }
+
+  if (p.nws == 1 && p.cs == 1) {
+    // ---- the only stream of this tile group: its rows are complete; normalise and store them
+    // (lane: dims 16 i + 2 g and 16 i + 2 g + 1 of rows 2 t and 2 t + 1 of each tile)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const float lt = warp_sum_g(l[nt][jj]);
+        const int row = (tg * NT + nt) * 8 + 2 * t + jj;
+        if (row < p.R) {
+          const float inv = 1.0f / lt;
+          const int r = row / p.G, gi = row - (row / p.G) * p.G;
+          float* dst = p.out + (((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + 2 * g;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float2*>(dst + 16 * i) =
+                make_float2(acc[nt][i][jj] * p.v_scale * inv, acc[nt][i][2 + jj] * p.v_scale * inv);
+        }
+      }
+    }
+    cluster_wait();
+    return;
   }
 
   // ---- this stream's partial for its tile group's rows
@@ -706,7 +733,7 @@ SwaPlan choose_plan(int cap, int B, int S, int Hq, int Hkv) {
     pl.batched = true;
     pl.smem = 0;
     for (pl.nst = std::min(KVQ_SWA_BATCH_STAGES, pl.ups); pl.nst >= 1; --pl.nst) {
-      const size_t bytes = SwaSmem(nws * pl.ntg, pl.nst, pl.NT, 1, pl.rows_pad).total;
+      const size_t bytes = SwaSmem(nws * pl.ntg, pl.nst, pl.NT, 1, pl.rows_pad, nws == 1).total;
       if (bytes <= kSmemCap) {
         pl.smem = bytes;
         break;
