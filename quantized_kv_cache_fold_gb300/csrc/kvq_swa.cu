@@ -55,6 +55,7 @@ namespace {
 #ifndef KVQ_SWA_BATCH_STAGES
 #define KVQ_SWA_BATCH_STAGES 2
 #endif
+static_assert(KVQ_SWA_BATCH_STAGES >= 1 && KVQ_SWA_BATCH_STAGES <= 2, "a unit stream tracks at most two stages");
 
 constexpr int kBlk = 2 * kPage * kRec8;  // 16384 bytes per 64-slot ring block (K half, V half)
 constexpr int kUnit = 32;                // slots per work unit
@@ -294,8 +295,8 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     }
     fence_barrier_init();
     fence_proxy_async_shared();
-    if (tg == 0)
-      for (int i = 0; i < nu; ++i) {
+    if (tg == 0)  // the units copied first (all of a cluster plan's; a long stream's head)
+      for (int i = 0; i < min(nu, 2 * p.nst); ++i) {
         const int u = stream + i * nstream;
         const uint8_t* blk = seg + (size_t)(u >> 1) * kBlk + (u & 1) * kHalf;
         prefetch_l2_bulk(blk, kHalf);
@@ -451,16 +452,25 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       for (int c = 0; c < 4; ++c) acc[nt][i][c] = 0.0f;
   }
 
-  int done = 0;  // units consumed
-  for (int i = 0; i < nu; ++i) {
-    const int s = i % p.nst;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&wfull[s], (uint32_t)(i / p.nst) & 1u));
+  // Units are consumed in the order they were issued. The first min(nst, nu) are the stream's
+  // first units, copied before the position was known; each refill takes the stream's next unit
+  // that holds a position of the rows' windows [max(0, c0 - window + 1), p_last] and skips units
+  // wholly outside them (the ring's slots beyond the window, and slots not yet written). A unit
+  // holding an appended row is never skipped.
+  const int span = p_last - max(0, c0 - p.window + 1);
+  int issued = min(p.nst, nu);  // units issued so far (warp-uniform)
+  int next_i = issued;          // the stream's next unit index to consider for a refill
+  int su0 = stream, su1 = stream + nstream;  // unit held by stage 0 / 1 (nst <= 2)
+  int done = 0;                 // units consumed
+  for (int k = 0; k < issued; ++k) {
+    const int s = k % p.nst;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&wfull[s], (uint32_t)(k / p.nst) & 1u));
     if (!ok) {
       if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
       break;
     }
     uint8_t* st = wst + (size_t)s * kStg;
-    const int u = stream + i * nstream;
+    const int u = s == 0 ? su0 : su1;
     if (have) {
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
@@ -475,16 +485,31 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       __syncwarp();
     }
     attend_unit<NT>(st, u, p_last, slot_last, p.cap, p.score_scale, qf, lim_lo, lim_hi, m, l, acc, lane);
-    done = i + 1;
+    done = k + 1;
     __syncwarp();
-    if (lane == 0 && i + p.nst < nu) {  // refill this stage with the stream's unit i + nst
-      fence_proxy_async_shared();
-      load_unit(st, seg, u + p.nst * nstream, &wfull[s], policy_evict_first());
+    // refill this stage with the stream's next unit that holds a window position: the unit's
+    // slot nearest behind slot_last is d slots back (0 if it holds slot_last)
+    for (; next_i < nu; ++next_i) {
+      const int un = stream + next_i * nstream;
+      const int first = un * kUnit, last = first + kUnit - 1;
+      const int d = (slot_last >= first && slot_last <= last) ? 0 : (slot_last - last + p.cap) % p.cap;
+      if (d <= span) break;
+    }
+    if (next_i < nu) {
+      const int un = stream + next_i * nstream;
+      if (lane == 0) {
+        fence_proxy_async_shared();
+        load_unit(st, seg, un, &wfull[s], policy_evict_first());
+      }
+      if (s == 0) su0 = un;
+      else su1 = un;
+      ++next_i;
+      ++issued;
     }
   }
-  if (done < nu && lane == 0) {  // gave up: let the copies still in flight land before leaving
-    for (int i = done; i < min(nu, done + p.nst); ++i)
-      if (!mbar_wait_bounded(&wfull[i % p.nst], (uint32_t)(i / p.nst) & 1u)) break;
+  if (done < issued && lane == 0) {  // gave up: let the copies still in flight land before leaving
+    for (int k = done; k < min(issued, done + p.nst); ++k)
+      if (!mbar_wait_bounded(&wfull[k % p.nst], (uint32_t)(k / p.nst) & 1u)) break;
   }
 
   if (p.nws == 1 && p.cs == 1) {

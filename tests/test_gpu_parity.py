@@ -301,6 +301,41 @@ def test_swa_one_cta_per_pair(orc, B, S):
     check_swa(orc, w, 6, S, sample=sorted(set(range(0, B, 7)) | {B - 1}))
 
 
+def test_swa_nonfinite_row_one_cta_per_pair(orc):
+    """The error paths with one CTA per (sequence, KV head) and a lone stream storing its rows
+    directly (300 sequences on 152 SMs): a NaN in one appended window key is flagged, that row
+    is neither stored nor attended and the other pairs stay exact; a negative position is
+    flagged and clamped."""
+    B = 300
+    ctx = (np.arange(B) * 389 % 3000).astype(np.int64)
+    w = Workload("swa-err-pairs", 29, B, 20, 4, 1, ctx, True)
+    st = build_swa(w, 7, 1)
+    assert kvq_fp8_swa_plan(576, B, 1, 20, 4)[0] == 1
+    dev_ctx = torch.from_numpy(w.ctx.astype(np.int32)).cuda()
+    q = device_q(w, 7, 1, w.ctx, swa=True)
+    k_new = device_new_kv(w, 7, 1, w.ctx, "swa_k")
+    v_new = device_new_kv(w, 7, 1, w.ctx, "swa_v")
+    k_new[7, 0, 2, 5] = float("nan")
+    out = torch.empty((B, 1, w.Hq, 128), dtype=torch.float32, device="cuda")
+    st.decode_layer(0, q, dev_ctx, out, k_new=k_new, v_new=v_new)
+    torch.cuda.synchronize()
+    assert st.read_error() == DEVERR_NONFINITE
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    for b, h in [(0, 0), (7, 0), (7, 1), (7, 3), (8, 2), (150, 1), (299, 3)]:
+        kc, vc, positions, ref = oracle_swa_seq(orc, w, 7, b, h, 1, int(w.ctx[b]), 513)
+        gk, gv = unpack_fp8(st.layers[0].tensors, b, h, positions)
+        assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+        assert_close(got[b, :, h * w.G:(h + 1) * w.G], ref, f"swa seq {b} head {h}")
+    st.dev_err.zero_()
+    bad = dev_ctx.clone()
+    bad[3] = -5
+    st.decode_layer(0, q, bad, out)
+    torch.cuda.synchronize()
+    assert st.read_error() == DEVERR_POS
+    assert np.isfinite(out.cpu().numpy()).all()
+
+
 def test_swa_nonfinite_row_and_bad_position_flagged(orc):
     """A NaN in one appended window key is flagged and that row is neither stored nor attended;
     the other (sequence, KV head) pairs stay exact. A negative position is flagged and clamped."""
