@@ -737,8 +737,8 @@ int ctas_per_sm(int dev, const SwaPlan& pl) {
 
 // The plan for a call. With at least as many (sequence, KV head) pairs as SMs the pairs fill
 // the GPU unsplit: one CTA per pair, its units over nws streams. The grid then runs in
-// ceil(pairs / (SMs x resident CTAs)) rounds of up to ceil(units / nws) units per stream; nws
-// takes the fewest rounds, then the fewest units per stream (a later round of CTAs costs more
+// ceil(pairs / (SMs x resident CTAs)) waves of up to ceil(units / nws) units per stream; nws
+// takes the fewest waves, then the fewest units per stream (a later wave of CTAs costs more
 // than longer streams in one), then the fewest streams. With fewer pairs the cluster plan.
 SwaPlan choose_plan(int cap, int B, int S, int Hq, int Hkv) {
   const SwaPlan cl = make_plan(cap, S, Hq, Hkv);
