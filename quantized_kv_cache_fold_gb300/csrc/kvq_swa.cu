@@ -11,8 +11,8 @@
 // Here the ring is cut into 32-slot units spread over the warps of one cluster (at most 8
 // CTAs), and the partial softmax states are merged on chip. With many (sequence, KV head)
 // pairs (at least one per SM) the pairs themselves fill the GPU: then each pair gets one CTA
-// (a cluster of one) whose few unit streams take several units each in turn, as many streams
-// as still let the whole grid be resident at once, and there is nothing to push:
+// (a cluster of one) whose few unit streams take several units each in turn (as many streams
+// as keep the grid in its fewest waves of resident CTAs), and there is nothing to push:
 //
 //   warp (unit stream w, tile group tg): streams the units u = w, w + NS, w + 2 NS, ...
 //     (NS = streams in the cluster) through its own one- or two-stage shared-memory buffer,
