@@ -11,7 +11,9 @@ Functions and what pins them (tests/test_oracle_pins.py):
   fold                          (M_q n(q)).(M_k n(k)) == (g_q n(q)).(g_k n(k))
   prologue                      fp32 spec vs an fp64 evaluation (error bound), scale invariance
   quantize_int4                 |y^ - y| <= s/2 bound, ramp and tie hand cases, constant vector
-  fp16 / e4m3 converters        numpy float16 and torch float8_e4m3fn, nextafter for RD/RU
+  fp16 / e4m3 converters        numpy/torch float16 and torch float8_e4m3fn, nextafter for RD/RU,
+                                over all 2^32 fp32 inputs (tests/test_oracle_converters.py)
+  channel_ratio                 a hand-worked matrix with an exact ratio (tests/golden/channel_ratio.txt)
   attention_int4 / fp8 / f64    L=1, equal keys, dominant key, 2-token closed form, permutation
   claim_errors                  ordering claims of the page; its percentages stay unpinned
 """
@@ -56,6 +58,7 @@ def _bind(L):
     L.orc_prologue_fwht.argtypes = [vp, vp, i64, f32, vp, i32]
     L.orc_quantize_int4.argtypes = [vp, i64, vp, vp, vp, vp, i32]
     L.orc_dequant_int4.argtypes = [vp, vp, vp, i64, vp]
+    L.orc_convert_range.argtypes = [ctypes.c_uint32, i64, vp, vp, vp, vp, i32]
     L.orc_fp16_round_bits.argtypes = [f32, i32]
     L.orc_fp16_round_bits.restype = ctypes.c_uint16
     L.orc_fp16_value.argtypes = [ctypes.c_uint16]
@@ -174,6 +177,17 @@ class Oracle:
     def fp16_round_bits(self, x: float, direction: int) -> int:
         """direction 0 nearest-even, -1 toward -inf, +1 toward +inf."""
         return int(self.L.orc_fp16_round_bits(float(x), int(direction)))
+
+    def convert_range(self, first: int, n: int):
+        """(rn, rd, ru, e4) of the n fp32 bit patterns first, first+1, ...: fp16 bits rounded to
+        nearest-even, toward -inf and toward +inf, and the saturating e4m3 code."""
+        rn = np.empty(n, np.uint16)
+        rd = np.empty(n, np.uint16)
+        ru = np.empty(n, np.uint16)
+        e4 = np.empty(n, np.uint8)
+        self.L.orc_convert_range(first & 0xFFFFFFFF, n, rn.ctypes.data, rd.ctypes.data, ru.ctypes.data,
+                                 e4.ctypes.data, self.threads)
+        return rn, rd, ru, e4
 
     def fp16_value(self, h: int) -> float:
         return float(self.L.orc_fp16_value(int(h)))

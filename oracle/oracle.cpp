@@ -448,6 +448,24 @@ void orc_dequant_int4(const uint8_t* codes, const uint16_t* sbits, const uint16_
 }
 
 uint16_t orc_fp16_round_bits(float x, int dir) { return fp16_bits(fp16_round(x, dir)); }
+
+// The converters above over n consecutive fp32 bit patterns first, first+1, ... (wrapping
+// at 2^32), for the exhaustive pins: fp16 bits rounded to nearest-even (rn), toward -inf
+// (rd), toward +inf (ru), and the saturating e4m3 code (e4). Any output may be NULL.
+void orc_convert_range(uint32_t first, int64_t n, uint16_t* rn, uint16_t* rd, uint16_t* ru, uint8_t* e4,
+                       int threads) {
+  for_range(n, threads, [&](int64_t a, int64_t b) {
+    for (int64_t i = a; i < b; ++i) {
+      const uint32_t bits = first + (uint32_t)i;
+      float x;
+      std::memcpy(&x, &bits, sizeof(x));
+      if (rn) rn[i] = fp16_bits(fp16_round(x, 0));
+      if (rd) rd[i] = fp16_bits(fp16_round(x, -1));
+      if (ru) ru[i] = fp16_bits(fp16_round(x, +1));
+      if (e4) e4[i] = e4m3_encode(x);
+    }
+  });
+}
 double orc_fp16_value(uint16_t h) { return fp16_value(h); }
 uint8_t orc_e4m3_encode(float x) { return e4m3_encode(x); }
 double orc_e4m3_value(uint8_t c) { return e4m3_value(c); }
@@ -518,7 +536,12 @@ void orc_attention_f64(const double* q, int64_t nrows, const double* K, const do
 double orc_channel_ratio(const double* keys, int64_t n, int d) {
   std::vector<double> m(d, 0.0);
   for (int64_t t = 0; t < n; ++t)
-    for (int c = 0; c < d; ++c) m[c] += std::fabs(keys[t * d + c]);
+    for (int c = 0; c < d; ++c) {
+      const double k = keys[t * d + c];
+      m[c] += MUT(17) ? k * k : std::fabs(k);  // MUT(17): root-mean-square per channel
+    }
+  if (MUT(17))
+    for (int c = 0; c < d; ++c) m[c] = std::sqrt(m[c]);
   double mx = 0.0, mean = 0.0;
   for (int c = 0; c < d; ++c) {
     mx = std::max(mx, m[c]);

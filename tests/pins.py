@@ -387,6 +387,25 @@ def check_attention_fp8(O):
 
 # ------------------------------------------------------------------ claims of the page
 
+def check_channel_ratio(O):
+    """Section "What we do": the largest key channel against the average one. The hand-worked
+    matrix of tests/golden/channel_ratio.txt has the exact ratio 8/3; the statistic ignores signs,
+    the order of tokens and channels and a common scale, and is 1 for a single channel."""
+    lines = _golden_lines("channel_ratio.txt")
+    rows = [[float(v) for v in ln.split()] for ln in lines if not ln.startswith("ratio")]
+    num, den = (int(v) for v in [ln for ln in lines if ln.startswith("ratio")][0].split()[1].split("/"))
+    k = np.array(rows, np.float64)
+    assert abs(O.channel_ratio(k) - num / den) < 1e-12, ("hand-worked ratio", O.channel_ratio(k))
+    rng = _rng(12)
+    x = rng.standard_normal((33, 16))
+    x[:, 5] *= 6.0
+    r = O.channel_ratio(x)
+    assert abs(O.channel_ratio(-x) - r) < 1e-12
+    assert abs(O.channel_ratio(x[rng.permutation(33)][:, rng.permutation(16)]) - r) < 1e-12
+    assert abs(O.channel_ratio(0.25 * x) - r) < 1e-12
+    assert abs(O.channel_ratio(x[:, :1]) - 1.0) < 1e-15
+
+
 def check_claims(O):
     """Section "What we do": rotation lowers the max/mean key channel ratio (<= 2.2 after),
     and 4-bit keys move attention less with the rotation; FP8 keys move it least."""
@@ -408,5 +427,6 @@ ALL_CHECKS = [
     check_hadamard, check_signs, check_rotation, check_fold, check_prologue, check_prologue_fwht,
     check_quantizer_cases,
     check_quantizer_bounds, check_quantizer_flags, check_fp16_converter, check_e4m3_converter,
-    check_attention_closed_forms, check_attention_structure, check_attention_fp8, check_claims,
+    check_attention_closed_forms, check_attention_structure, check_attention_fp8, check_channel_ratio,
+    check_claims,
 ]

@@ -31,6 +31,7 @@ MUTATIONS = {
     14: "FWHT prologue without the 1/sqrt(128) scale",
     15: "FWHT query multipliers without the signs",
     16: "softmax without max subtraction",
+    17: "key channel statistic as root-mean-square instead of mean |k|",
 }
 
 
