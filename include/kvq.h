@@ -164,7 +164,8 @@ kvq_status kvq_fold_qk_fwht(const int8_t* s, const float* g_q, const float* g_k,
  *   lanes l=0..31 hold x[4l..4l+3]; t_l = fma(x3,x3,fma(x2,x2,fma(x1,x1,x0*x0)));
  *   t_l <- t_l + t_(l^o) for o = 16,8,4,2,1; inv = 1/sqrt(t/128 + eps); n = x*inv;
  *   y_j = fma chain over i=0..127 of M[j][i]*n_i;
- *   o = fp16 toward -inf of min(y) (+0 for a zero); s = fp16 toward +inf of (max(y)-o)/15;
+ *   o = fp16 toward -inf of min(y); s = fp16 toward +inf of (max(y)-o)/15 (a zero o or s is
+ *   stored as +0; an o below -65504 or an s above 65504 saturates there, KVQ_DEVERR_RANGE);
  *   code_i = 0 if s == 0 else clamp(round_half_even((y_i - o)/s), 0, 15).
  * Values use the same quantiser on the raw row. T == 0 is a no-op.
  */
@@ -172,11 +173,6 @@ kvq_status kvq_rotate_quant_append(const kvq_int4_cache* cache, const float* Mk,
                                    kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
                                    float eps, int32_t* dev_err, kvq_stream_t stream);
 
-/*
- * Bytes of device workspace needed by kvq_decode_attn_int4 / kvq_decode_attn_fp8_swa for
- * B sequences, S query rows each, num_q_heads query heads over num_kv_heads KV heads.
- * Returns 0 for arguments no call would accept.
- */
 /*
  * kvq_rotate_quant_append_fwht -- kvq_rotate_quant_append with the second prologue
  * specification: y = c FWHT(wk n(k)), c = fp32(1/sqrt(128)) (R n(k) up to rounding).
@@ -189,6 +185,11 @@ kvq_status kvq_rotate_quant_append_fwht(const kvq_int4_cache* cache, const float
                                         kvq_dtype dtype, int T, const int32_t* seq_ids, const int32_t* positions,
                                         float eps, int32_t* dev_err, kvq_stream_t stream);
 
+/*
+ * Bytes of device workspace needed by kvq_decode_attn_int4 / kvq_decode_attn_fp8_swa for
+ * B sequences, S query rows each, num_q_heads query heads over num_kv_heads KV heads.
+ * Returns 0 for arguments no call would accept.
+ */
 size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_heads);
 
 /*
@@ -288,14 +289,20 @@ kvq_status kvq_fp8_swa_plan(int capacity, int B, int S, int num_q_heads, int num
  * environment where cudaMalloc or a framework allocator is unavailable). The paper has no
  * counterpart: this is a packaging variant of the workspace handling only.
  * The workspace comes from a fixed scratch array inside this library's device image, of
- * KVQ_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds that much until the
- * process exits. The call allocates nothing; the caller still passes every input and output.
- *   - Arguments and results are those of kvq_decode_attn_int4 without (workspace,
- *     workspace_bytes).
- *   - Requests whose workspace (kvq_decode_workspace_bytes) exceeds the scratch return
- *     KVQ_ERR_SCRATCH_TOO_SMALL and launch nothing.
- *   - The first call on each device looks up the scratch's device address (with that
- *     device current); make that first call before any stream capture.
+ * KVQ_NOALLOC_SCRATCH_BYTES. The call allocates nothing; the caller still passes every input
+ * and output.
+ *   - Arguments, checks and results are those of kvq_decode_attn_int4 without (workspace,
+ *     workspace_bytes): the same status for the same bad argument.
+ *   - Requests with valid arguments whose workspace (kvq_decode_workspace_bytes) exceeds the
+ *     scratch return KVQ_ERR_SCRATCH_TOO_SMALL and launch nothing.
+ *   - When the memory is taken: under lazy module loading (the CUDA default) the first call on
+ *     a device loads the module holding the array, and so allocates its 16 MiB there, while
+ *     looking up its device address (with that device current); under eager loading the
+ *     library's load does. The device keeps it until the process exits. Make the first call on
+ *     each device before reserving the memory pool the engine hands out, and before any
+ *     stream capture.
+ *   - Every call looks the address up again (cheap once loaded), so calls stay valid across a
+ *     cudaDeviceReset.
  *   - All calls on a device share the one scratch array, which keeps the last call's
  *     contents (no call needs it zeroed). Calls whose execution overlaps on the GPU race on
  *     it: serialise them (one stream, or explicit ordering between streams and threads).

@@ -256,7 +256,7 @@ bool all_finite(const float* x, int n) {
 // token and head. fp32 specification:
 //   mn = min y, mx = max y
 //   o = fp16_down(mn)  (-0 stored as +0)
-//   s = fp16_up((mx - o) / 15)
+//   s = fp16_up((mx - o) / 15)  (-0 stored as +0)
 //   c_i = 0 if s == 0, else clamp(round_half_even((y_i - o) / s), 0, 15)
 // Flags: 1 = non-finite input (record not produced), 2 = fp16 range saturated.
 int quantize_one(const float* y, uint8_t* codes, uint16_t* sbits, uint16_t* obits) {
@@ -280,6 +280,7 @@ int quantize_one(const float* y, uint8_t* codes, uint16_t* sbits, uint16_t* obit
     sd = kHalfMax;
     flags |= 2;
   }
+  if (sd == 0.0) sd = 0.0;  // canonical +0 (a row of zeros whose largest element is -0)
   float s = (float)sd;
   for (int i = 0; i < 128; ++i) {
     if (s == 0.0f) {

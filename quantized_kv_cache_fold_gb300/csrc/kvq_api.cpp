@@ -153,23 +153,41 @@ size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_head
          kvq::workspace_partials_bytes(B, S, num_q_heads, num_kv_heads);
 }
 
-static kvq_status decode_int4_impl(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
-                                   kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
-                                   const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
-                                   void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
-                                   kvq_stream_t stream, int fwht) {
+}  // extern "C"
+
+namespace kvq {
+
+kvq_status check_decode_int4_args(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                  kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                  const void* k_new, const void* v_new, float sm_scale, float eps, const float* out,
+                                  const float* q_rot_out, const int32_t* dev_err) {
   kvq_status st = check_int4_cache(cache);
   if (st != KVQ_OK) return st;
   if (S < 1 || S > 8 || !heads_ok(num_q_heads, cache->num_kv_heads, S)) return KVQ_ERR_UNSUPPORTED;
   if (B < 1 || B > KVQ_MAX_SEQS || B > cache->num_seqs) return KVQ_ERR_INVALID_ARG;
   if (dtype != KVQ_F32 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
-  if (!Mq || !q || !ctx_len || !out || !workspace || !dev_err) return KVQ_ERR_INVALID_ARG;
+  if (!Mq || !q || !ctx_len || !out || !dev_err) return KVQ_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
   if (k_new && (!Mk || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(Mk, 16))) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(Mq, 16))
-    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(Mq, 16)) return KVQ_ERR_INVALID_ARG;
   if (q_rot_out && !aligned(q_rot_out, 16)) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale) || !(eps >= 0.0f) || std::isinf(eps)) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+}  // namespace kvq
+
+extern "C" {
+
+static kvq_status decode_int4_impl(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                   kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                   const void* k_new, const void* v_new, float sm_scale, float eps, float* out,
+                                   void* workspace, size_t workspace_bytes, float* q_rot_out, int32_t* dev_err,
+                                   kvq_stream_t stream, int fwht) {
+  kvq_status st = kvq::check_decode_int4_args(cache, Mq, Mk, q, dtype, B, S, num_q_heads, ctx_len, k_new, v_new,
+                                              sm_scale, eps, out, q_rot_out, dev_err);
+  if (st != KVQ_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return KVQ_ERR_INVALID_ARG;
   if (workspace_bytes < kvq_decode_workspace_bytes(B, S, num_q_heads, cache->num_kv_heads))
     return KVQ_ERR_INVALID_ARG;
 

@@ -91,6 +91,13 @@ void swa_plan_shape(int capacity, int B, int S, int Hq, int Hkv, int out[4]);
 cudaError_t launch_swa_cluster(const AttnJob& job, cudaStream_t stream);
 
 // Workspace layout shared by the API and the launchers.
+// Host-side argument checks of kvq_decode_attn_int4 other than the workspace (status as that
+// call returns it); shared with the allocation-free entry point.
+kvq_status check_decode_int4_args(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
+                                  kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,
+                                  const void* k_new, const void* v_new, float sm_scale, float eps, const float* out,
+                                  const float* q_rot_out, const int32_t* dev_err);
+
 size_t workspace_qrot_bytes(int B, int S, int Hq);
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv);
 

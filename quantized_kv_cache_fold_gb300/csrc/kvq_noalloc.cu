@@ -4,8 +4,15 @@
 // GPU memory for its KV pool up front, a host process whose allocator must not be touched
 // from the decode thread, or code running where cudaMalloc (or a framework allocator) is
 // not allowed. This entry point takes the attention workspace from a fixed scratch array
-// that lives in this library's device image instead of from the caller. Every GPU that
-// loads the library holds the array (KVQ_NOALLOC_SCRATCH_BYTES) until the process exits.
+// that lives in this library's device image instead of from the caller.
+//
+// When the array is allocated: this file is its own CUDA module. Under lazy module loading
+// (CUDA_MODULE_LOADING=LAZY, the default) the module, and with it the array's
+// KVQ_NOALLOC_SCRATCH_BYTES of device memory, is loaded on a device by the first call of this
+// entry point there (its cudaGetSymbolAddress); under eager loading, when the library's
+// modules load. Either way the device holds the array until the process exits (or the device
+// is reset). So make the first call on each device before reserving the memory pool the
+// engine hands out, and before any stream capture.
 //
 // The array is shared by every call on a device and keeps the last call's contents. The
 // workspace needs no zeroing: each call writes every part of it before reading it. Calls
@@ -13,9 +20,11 @@
 // threads) race on the array; the caller serialises them.
 //
 // In host code the array's name is only a host-side stand-in for the device symbol, never
-// a device address: the device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached. That set-up happens in the
-// first call on each device, so make the first call before any stream capture.
+// a device address. The first call on a device, with that device current, looks the device
+// address up with cudaGetSymbolAddress under a lock (that set-up loads the module). Every
+// later call repeats the lookup, which is cheap once the module is loaded, so a
+// cudaDeviceReset between calls (after which the array may sit elsewhere) cannot leave a
+// stale address behind.
 
 #include <cuda_runtime.h>
 
@@ -23,25 +32,28 @@
 #include <mutex>
 
 #include "kvq.h"
+#include "kvq_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_kvq_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+std::atomic<bool> g_set_up[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// Device address of the scratch array on the current device (nullptr on failure).
+// Device address of the scratch array on the current device `dev` (nullptr on failure).
 void* scratch_address(int dev) {
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p) return p;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  p = g_scratch_addr[dev].load(std::memory_order_relaxed);
-  if (p) return p;
   void* addr = nullptr;
-  if (cudaGetSymbolAddress(&addr, g_kvq_noalloc_scratch) != cudaSuccess || addr == nullptr) return nullptr;
-  g_scratch_addr[dev].store(addr, std::memory_order_release);
+  if (!g_set_up[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_set_up[dev].load(std::memory_order_relaxed)) {
+      if (cudaGetSymbolAddress(&addr, g_kvq_noalloc_scratch) != cudaSuccess || addr == nullptr) return nullptr;
+      g_set_up[dev].store(true, std::memory_order_release);
+      return addr;
+    }
+  }
+  if (cudaGetSymbolAddress(&addr, g_kvq_noalloc_scratch) != cudaSuccess) return nullptr;
   return addr;
 }
 
@@ -52,9 +64,11 @@ extern "C" kvq_status kvq_decode_attn_int4_noalloc(const kvq_int4_cache* cache, 
                                                    const int32_t* ctx_len, const void* k_new, const void* v_new,
                                                    float sm_scale, float eps, float* out, float* q_rot_out,
                                                    int32_t* dev_err, kvq_stream_t stream) {
-  if (!cache) return KVQ_ERR_INVALID_ARG;
+  // the same argument checks (and status codes) as kvq_decode_attn_int4, before the scratch size
+  const kvq_status st = kvq::check_decode_int4_args(cache, Mq, Mk, q, dtype, B, S, num_q_heads, ctx_len, k_new,
+                                                    v_new, sm_scale, eps, out, q_rot_out, dev_err);
+  if (st != KVQ_OK) return st;
   const size_t need = kvq_decode_workspace_bytes(B, S, num_q_heads, cache->num_kv_heads);
-  if (need == 0) return KVQ_ERR_UNSUPPORTED;
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_SCRATCH_TOO_SMALL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;

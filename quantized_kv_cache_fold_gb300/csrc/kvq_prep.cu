@@ -131,6 +131,7 @@ __device__ __forceinline__ Quant4 quantize(const float (&y)[4]) {
     sb = 0x7BFFu;
     r.flags |= KVQ_DEVERR_RANGE;
   }
+  if (sb == 0x8000u) sb = 0;  // canonical +0 (zeros whose maximum came out as -0)
   const float s = __half2float(__ushort_as_half(sb));
 #pragma unroll
   for (int u = 0; u < 4; ++u) {

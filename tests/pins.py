@@ -166,16 +166,27 @@ def _golden_quant_cases():
     return cases
 
 
-def check_quantizer_cases(O):
-    g = _golden_quant_cases()
+def quantizer_case_rows():
+    """The 128-vectors of tests/golden/quantizer_cases.txt, built as the file's second column says."""
     i = np.arange(128)
-    ys = {
+    return {
         "ramp": (0.5 * (i % 16)).astype(np.float32),
         "const_exact": np.full(128, 1.5, np.float32),
         "const_1p3": np.full(128, 1.3, np.float32),
         "ties": np.array([0, 15] + [k + 0.5 for k in range(15)] + [0] * 111, np.float32),
         "neg_offset": np.array([-1.0001] + [0] * 127, np.float32),
     }
+
+
+def golden_quantizer_cases():
+    """name -> (scale bits, offset bits) from tests/golden/quantizer_cases.txt."""
+    return {k: v[:2] for k, v in _golden_quant_cases().items()}
+
+
+def check_quantizer_cases(O):
+    g = _golden_quant_cases()
+    i = np.arange(128)
+    ys = quantizer_case_rows()
     expect_codes = {
         "ramp": i % 16,
         "const_exact": np.zeros(128),

@@ -134,3 +134,25 @@ def test_stream_k_split_arithmetic():
                     assert slot not in used
                     used.add(slot)
         assert max(used) < n + B * Hkv
+
+
+def _noalloc(cache, **over):
+    a = dict(Mq=0x60000, Mk=0x70000, q=0x80000, dtype=1, B=2, S=1, Hq=20, ctx=0x90000, k_new=None, v_new=None,
+             sm=0.088, eps=1e-6, out=0xA0000, qrot=None, err=0xC0000, stream=None)
+    a.update(over)
+    return kvq.lib.kvq_decode_attn_int4_noalloc(ctypes.byref(cache), a["Mq"], a["Mk"], a["q"], a["dtype"], a["B"],
+                                                a["S"], a["Hq"], a["ctx"], a["k_new"], a["v_new"], a["sm"], a["eps"],
+                                                a["out"], a["qrot"], a["err"], a["stream"])
+
+
+def test_noalloc_rejects_like_the_workspace_call():
+    """The allocation-free entry point returns the same status as kvq_decode_attn_int4 for the same
+    bad argument, before its scratch-size check and before any CUDA call."""
+    big = _fake_cache(num_seqs=1024, max_pages_per_seq=8)
+    for cache, over in ((_fake_cache(), dict(B=0)), (_fake_cache(), dict(B=5)), (big, dict(B=1025)),
+                        (_fake_cache(head_dim=64), {}), (_fake_cache(), dict(S=9)), (_fake_cache(), dict(q=0x80004)),
+                        (_fake_cache(), dict(dtype=7)), (_fake_cache(pages=0), {}), (big, dict(B=1024, q=None))):
+        want = _attn(cache, **over)
+        assert want in (1, 2)
+        assert _noalloc(cache, **over) == want, over
+    assert _noalloc(_fake_cache(), B=0) == 1  # KVQ_ERR_INVALID_ARG

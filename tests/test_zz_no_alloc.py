@@ -7,9 +7,10 @@ collected last on purpose, and it must pass both on its own in a fresh process (
 first call performs the per-device scratch set-up) and after every other test.
 
 The check: through the C ABI, the new entry point gives the same attention output as
-kvq_decode_attn_int4 with a caller workspace, within the tolerance of the other GPU tests,
-on two consecutive rounds with different queries and contexts (so a stale scratch from
-the previous call would show); and a request larger than the scratch is refused.
+kvq_decode_attn_int4 with a caller workspace, within the tolerance of the other GPU tests and
+in fact bit for bit (the same kernels run on the same inputs), on two consecutive rounds with
+different queries and contexts (so a stale scratch from the previous call would show); and a
+request larger than the scratch is refused.
 """
 
 import ctypes
@@ -58,7 +59,10 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert _noalloc(L.cache, L.Mq, L.Mk, q, ctx, got, err) == 0
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        assert_close(got.cpu().numpy(), ref.cpu().numpy(), "noalloc vs workspace entry point")
+        g, r = got.cpu().numpy(), ref.cpu().numpy()
+        assert_close(g, r, "noalloc vs workspace entry point")
+        # the same kernels on the same inputs with a workspace of the same layout: bit for bit
+        assert np.array_equal(g, r), "noalloc output differs in some bit from the workspace entry point's"
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
