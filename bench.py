@@ -288,14 +288,11 @@ def run_64k(device, steps=30, warmup=3):
             "session_layer_steps_per_s": round(w.B / t, 1), "algorithmic_bytes": by}
 
 
-def run_verify(device, steps=30, warmup=3):
-    """The speculative-verify workload: 64 sequences at 16,384 context, 20/4 heads, S = 1, 4 and 8
-    query rows per sequence with the S new K/V rows rotated, quantised and appended inside the
-    call (at the same positions every repetition), one int4 layer. S = 8 (40 rows per KV head) is
-    timed with the default split-K kernel and with the two kernels KVQ_MANY_ROWS_KERNEL selects
-    for many rows (the mma.sync shared-tile kernel and the tcgen05 variant)."""
-    import os
-
+def run_verify(device, steps=30, warmup=3, S_values=(1, 4, 8)):
+    """The speculative-verify workload: 64 sequences at 16,384 context, 20/4 heads, S query rows per
+    sequence (S = 1, 4, 8) with the S new K/V rows rotated, quantised and appended inside the call
+    (at the same positions every repetition), one int4 layer, random page order. Each call is timed
+    with CUDA events (median of `steps`); the cache (570 MB) is larger than L2."""
     import torch
 
     import synth
@@ -303,9 +300,10 @@ def run_verify(device, steps=30, warmup=3):
     from synth.workloads import config
 
     w = config(4)
+    peak, _ = measured_peak()
     stream = torch.cuda.current_stream().cuda_stream
     perm = lambda l, n: synth.page_permutation(w.seed, l, n)  # noqa: E731
-    Smax = 8
+    Smax = max(S_values)
     st = DecodeStack(w.B, w.Hq, w.Hkv, Smax, w.max_pages() + 1, 1, 1, page_perm=perm, device=device)
     gq, gk = synth.gains(w.seed, 0)
     st.set_int4_params(0, synth.rotation_seed(w.seed, 0), gq, gk)
@@ -317,43 +315,81 @@ def run_verify(device, steps=30, warmup=3):
     st.prefill_int4(0, w.ctx, fill, chunk_tokens=32768)
     ctx = torch.from_numpy(w.ctx.astype(np.int32)).to(device)
     rows = []
-    for S, kernel in ((1, None), (4, None), (8, None), (8, "tile"), (8, "tcgen05")):
+    for S in S_values:
         q = torch.empty((w.B, S, w.Hq, 128), dtype=torch.bfloat16, device=device)
         kn = torch.empty((w.B, S, w.Hkv, 128), dtype=torch.bfloat16, device=device)
         vn = torch.empty_like(kn)
         for t, key in ((q, synth.S_QUERIES), (kn, synth.S_KEYS), (vn, synth.S_VALUES)):
             synth.normals_device(synth.key(w.seed + 2000 + S, key), 0, t.numel(), t.data_ptr(), None, True, stream)
         out = torch.empty((w.B, S, w.Hq, 128), dtype=torch.float32, device=device)
-        old = os.environ.get("KVQ_MANY_ROWS_KERNEL")
-        if kernel:
-            os.environ["KVQ_MANY_ROWS_KERNEL"] = kernel
-        try:
-            for _ in range(warmup):
-                st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)
-            torch.cuda.synchronize()
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(min(steps, 30))]
-            for e0, e1 in evs:
-                e0.record()
-                st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)
-                e1.record()
-            torch.cuda.synchronize()
-        finally:
-            if kernel:
-                if old is None:
-                    del os.environ["KVQ_MANY_ROWS_KERNEL"]
-                else:
-                    os.environ["KVQ_MANY_ROWS_KERNEL"] = old
+        for _ in range(warmup):
+            st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(steps, 30))]
+        for e0, e1 in evs:
+            e0.record()
+            st.decode_layer(0, q, ctx, out, k_new=kn, v_new=vn)
+            e1.record()
+        torch.cuda.synchronize()
         assert st.read_error() == 0
         t = statistics.median([e0.elapsed_time(e1) for e0, e1 in evs]) * 1e-3
         by = int((w.ctx + S).sum()) * w.Hkv * 136
-        rows.append({"S": S, "rows_per_kv_head": S * w.G, "many_row_kernel": kernel or "split",
-                     "int4_call_us": round(t * 1e6, 1), "hbm_gbs": round(by / t / 1e9, 1),
-                     "query_rows_per_s": round(w.B * S / t, 1)})
+        rows.append({"S": S, "rows_per_kv_head": S * w.G, "int4_call_us": round(t * 1e6, 1),
+                     "hbm_gbs": round(by / t / 1e9, 1), "frac_of_measured": round(by / t / 1e9 / peak, 4),
+                     "query_rows_per_s": round(w.B * S / t, 1), "algorithmic_bytes": by})
     del st
     torch.cuda.empty_cache()
-    return {"workload": "speculative verify: 64 sequences x 16,384 context, 20/4 heads, new rows appended in the "
-                        "call, one int4 layer, random page order", "points": rows}
+    return {"workload": "speculative verify: 64 sequences x 16,384 context, 20/4 heads, S new rows appended in "
+                        "the call, one int4 layer, random page order", "points": rows}
+
+
+def run_config2(device, steps=30, warmup=3):
+    """16 sequences x 8,192 context, one int4 layer, pages in order, one query row: the cache
+    (71 MB) fits in L2, so a 256 MB buffer is written between timed calls (outside the events)
+    to flush it."""
+    import torch
+
+    import synth
+    from quantized_kv_cache_fold_gb300.runner import DecodeStack
+    from synth.workloads import config
+
+    w = config(2)
+    peak, _ = measured_peak()
+    stream = torch.cuda.current_stream().cuda_stream
+    st = DecodeStack(w.B, w.Hq, w.Hkv, 1, w.max_pages(), 1, 1, device=device)
+    gq, gk = synth.gains(w.seed, 0)
+    st.set_int4_params(0, synth.rotation_seed(w.seed, 0), gq, gk)
+
+    def fill(b, p0, T, kb, vb):
+        synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "k", True, kb.data_ptr(), stream)
+        synth.kv_rows_device(w.seed, 0, b, p0, T, w.Hkv, "v", True, vb.data_ptr(), stream)
+
+    st.prefill_int4(0, w.ctx, fill, chunk_tokens=32768)
+    q = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.bfloat16, device=device)
+    synth.normals_device(synth.key(w.seed + 1000, synth.S_QUERIES), 0, q.numel(), q.data_ptr(), None, True, stream)
+    ctx = torch.from_numpy(w.ctx.astype(np.int32)).to(device)
+    out = torch.empty((w.B, 1, w.Hq, 128), dtype=torch.float32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    for _ in range(warmup):
+        st.decode_layer(0, q, ctx, out)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (e0, e1) in enumerate(evs):
+        flush.fill_(i & 0xFF)
+        e0.record()
+        st.decode_layer(0, q, ctx, out)
+        e1.record()
+    torch.cuda.synchronize()
+    assert st.read_error() == 0
+    t = statistics.median([e0.elapsed_time(e1) for e0, e1 in evs]) * 1e-3
+    by = int((w.ctx + 1).sum()) * w.Hkv * 136
+    del st, flush
+    torch.cuda.empty_cache()
+    return {"workload": "16 sequences x 8,192 context, one int4 layer, pages in order, 1 query row",
+            "l2": "256 MB buffer written between timed calls", "int4_call_us": round(t * 1e6, 1),
+            "hbm_gbs": round(by / t / 1e9, 1), "frac_of_measured": round(by / t / 1e9 / peak, 4),
+            "algorithmic_bytes": by}
 
 
 def run_swa(device, steps=30, warmup=3, sequences=None, layers=None):
@@ -561,13 +597,45 @@ def run_ab(device, steps=30, warmup=3):
                         % int(w.ctx.mean()), "variants": res}
 
 
+# Kolibri-1's attention stack as the pages describe it: 50 layers, 10 with full attention and
+# 40 sliding-window layers (window 513), 4 KV heads of 128.
+N_FULL, N_SWA, HKV_MODEL = 10, 40, 4
+
+
+def session_bytes(fmt: str, ctx_len: int, window_slots: int) -> int:
+    """KV bytes one session holds: the 10 full-attention layers at ctx_len positions (int4: 136 B
+    per token-head, K and V codes 64 B each plus an fp16 scale and offset each; FP8: 256 B) and the
+    40 window layers at window_slots positions of FP8 (256 B per token-head)."""
+    per_th = {"int4": 136, "fp8": 256}[fmt]
+    return N_FULL * HKV_MODEL * ctx_len * per_th + N_SWA * HKV_MODEL * window_slots * 256
+
+
+def fill_pool_random(tensors, gen):
+    """Seeded random cache contents in place (plumbing: torch's generator; no kernel of the path).
+    int4 page blocks: random K and V code bytes (every byte is a valid record), fp16 scales in
+    [2^-7, 2^-3) and offsets in (-2, -0.5]; FP8 ring blocks: random e4m3 bytes with the top exponent
+    bit cleared (|value| <= 1.875, never NaN)."""
+    import torch
+    if "pages" in tensors:
+        pages = tensors["pages"]
+        pages.random_(0, 256, generator=gen)  # in place
+        meta = pages[..., 8192:8704].view(torch.int16).unflatten(-1, (128, 2))
+        meta[..., 0].random_(0x2000, 0x3000, generator=gen)
+        meta[..., 1].random_(-18432, -16384, generator=gen)  # bit patterns 0xB800 .. 0xBFFF
+    else:
+        data = tensors["data"]
+        data.random_(0, 256, generator=gen)
+        data.bitwise_and_(0xBF)
+
+
 def run_capacity(device, budget_gb=160.0, steps=32, warmup=3):
     """Capacity and throughput of a fixed KV pool, rotated int4 full layers against FP8 everywhere.
 
     A pool of `budget_gb` holds as many sessions as fit at 64k and at 256k context, 50 layers per
     session (10 full-attention layers: int4 pages, 136 B per token-head, or FP8 rings, 256 B; 40
-    window-513 layers: 576-slot FP8 rings). The pools are zero-filled (valid codes: zero scale,
-    offset and e4m3 values; the kernels' time does not depend on the values). Then the decode step
+    window-513 layers: 576-slot FP8 rings; session_bytes). The pools hold seeded random codes,
+    scales and offsets (fill_pool_random), so scores vary as on data and the attention kernels'
+    softmax base moves as it would there. Then the decode step
     (all 50 layers, one query row, the new key/value row appended in each call) is timed for B
     sessions, B from the pool's maximum down to one: each step is one replay of a one-step CUDA
     graph bracketed by events, giving the median step time and the slowest tenth over the median."""
@@ -577,14 +645,14 @@ def run_capacity(device, budget_gb=160.0, steps=32, warmup=3):
     from quantized_kv_cache_fold_gb300.runner import DecodeStack
     from synth.workloads import SWA_K_SCALE, SWA_V_SCALE
 
-    Hq, Hkv, G, n_full, n_swa, ring, window = 20, 4, 5, 10, 40, 576, 513
+    Hq, Hkv, G, n_full, n_swa, ring, window = 20, HKV_MODEL, 5, N_FULL, N_SWA, 576, 513
     stream = torch.cuda.current_stream().cuda_stream
-    result = {"budget_gb": budget_gb, "points": []}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7)
+    result = {"budget_gb": budget_gb, "points": [],
+              "fill": "seeded random codes, fp16 scales in [2^-7, 2^-3), offsets in (-2, -0.5]; random e4m3"}
     for ctx_len in (65536, 262144):
-        per_session = {
-            "int4": n_full * Hkv * ctx_len * 136 + n_swa * Hkv * ring * 256,
-            "fp8": n_full * Hkv * ctx_len * 256 + n_swa * Hkv * ring * 256,
-        }
+        per_session = {fmt: session_bytes(fmt, ctx_len, ring) for fmt in ("int4", "fp8")}
         for fmt in ("int4", "fp8"):
             n_max = int(budget_gb * 1e9 // per_session[fmt])
             max_pages = (ctx_len + 1 + 63) // 64
@@ -600,6 +668,9 @@ def run_capacity(device, budget_gb=160.0, steps=32, warmup=3):
                                    swa_v_scale=SWA_V_SCALE, device=device)
             swa = DecodeStack(n_max, Hq, Hkv, 1, 1, n_layers=n_swa, full_every=n_swa + 1, ring_capacity=ring,
                               window=window, swa_k_scale=SWA_K_SCALE, swa_v_scale=SWA_V_SCALE, device=device)
+            for stack in (full, swa):
+                for layer in stack.layers:
+                    fill_pool_random(layer.tensors, gen)
             held = torch.cuda.memory_allocated() / 1e9
             q = torch.empty((n_max, 1, Hq, 128), dtype=torch.bfloat16, device=device)
             kn = torch.empty((n_max, 1, Hkv, 128), dtype=torch.bfloat16, device=device)
@@ -671,48 +742,96 @@ def run_capacity(device, budget_gb=160.0, steps=32, warmup=3):
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(seconds_budget=20.0):
-    """Oracle (CPU, fp64) on a bounded sample of the 256k step: the attention of one KV head (5
-    query rows) of one int4 layer over 262,145 positions, and one window layer of one sequence
-    (4 KV heads), on a cache of seeded random codes. Scaled to session-steps/s."""
-    import oracle
-    import synth
-    from synth.workloads import config
+def _oracle_heads_concurrently(calls, threads_total):
+    """Run one oracle call per KV head on its own host thread (ctypes releases the GIL), each with
+    threads_total // len(calls) oracle threads. Returns (seconds, threads actually busy)."""
+    import concurrent.futures
 
-    w = config(5)
-    O = oracle.Oracle()
-    L = int(w.ctx[0]) + 1
-    k = synth.key(99, 1)
-    d = synth.draws(k, 0, L * 128 // 8 * 2 + 4 * L)
-    raw = d.view(np.uint8)
-    kc = (raw[: L * 128] & 15).reshape(L, 128)
-    vc = (raw[L * 128: 2 * L * 128] >> 4).reshape(L, 128)
-    ks = np.full(L, 0x2E66, np.uint16)
-    ko = np.full(L, 0xC1A0, np.uint16)
-    q = synth.normals(synth.key(99, 2), 0, w.G * 128).reshape(w.G, 128)
-    vis = np.full(w.G, L)
+    import oracle
+
+    per = max(1, threads_total // len(calls))
+    Os = [oracle.Oracle(threads=per) for _ in calls]
     t0 = time.perf_counter()
-    reps = 0
+    with concurrent.futures.ThreadPoolExecutor(len(calls)) as pool:
+        list(pool.map(lambda a: a[0](a[1]), zip(calls, Os)))
+    return time.perf_counter() - t0, per
+
+
+class OracleStepSample:
+    """The fp64 oracle on a bounded sample of the 256k decode step, on the host's cores: one int4
+    layer of one sequence (its 4 KV heads, 5 query rows each, over 262,145 positions of seeded
+    random codes) and one window-513 layer of one sequence (4 KV heads, 5 rows each). Each KV head
+    is one oracle call on its own host thread; an oracle call threads over its query rows, so
+    4 x min(5, cores / 4) threads do the attention (cores() reports that number). A session-step
+    is 10 int4 layers and 40 window layers: seconds per session-step = 10 t_int4 + 40 t_window."""
+
+    def __init__(self):
+        import synth
+        from synth.workloads import config
+
+        w = config(5)
+        self.w = w
+        self.threads_total = max(1, os.cpu_count() or 1)
+        L = int(w.ctx[0]) + 1
+        self.L = L
+        self.int4 = []
+        for h in range(w.Hkv):
+            raw = synth.draws(synth.key(99, 10 + h), 0, L * 128 // 4).view(np.uint8)
+            kc = np.ascontiguousarray((raw[: L * 128] & 15).reshape(L, 128))
+            vc = np.ascontiguousarray((raw[: L * 128] >> 4).reshape(L, 128))
+            q = synth.normals(synth.key(99, 20 + h), 0, w.G * 128).reshape(w.G, 128)
+            self.int4.append((q, kc, vc))
+        self.ks = np.full(L, 0x2E66, np.uint16)
+        self.ko = np.full(L, 0xC1A0, np.uint16)
+        W = w.window
+        self.W = W
+        self.swa = []
+        for h in range(w.Hkv):
+            raw = synth.draws(synth.key(99, 30 + h), 0, W * 128 // 4).view(np.uint8)
+            k8 = np.ascontiguousarray((raw[: W * 128] & 0x77).reshape(W, 128))
+            v8 = np.ascontiguousarray((raw[: W * 128] >> 1 & 0x77).reshape(W, 128))
+            q8 = synth.normals(synth.key(99, 40 + h), 0, w.G * 128).reshape(w.G, 128)
+            self.swa.append((q8, k8, v8))
+
+    def cores(self):
+        return self.w.Hkv * min(self.w.G, max(1, self.threads_total // self.w.Hkv))
+
+    def layer_seconds(self):
+        """(t_int4_layer, t_window_layer) for one sequence, all KV heads."""
+        w, L, W = self.w, self.L, self.W
+        vis = np.full(w.G, L)
+        calls = [lambda O, a=a: O.attention_int4(a[0], vis, a[1], self.ks, self.ko, a[2], self.ks, self.ko,
+                                                  128 ** -0.5) for a in self.int4]
+        t_int4, _ = _oracle_heads_concurrently(calls, self.threads_total)
+        lo = np.zeros(w.G, np.int64)
+        hi = np.full(w.G, W - 1, np.int64)
+        calls = [lambda O, a=a: O.attention_fp8(a[0], lo, hi, a[1], a[2], 0.01, 0.01, 128 ** -0.5) for a in self.swa]
+        t_swa, _ = _oracle_heads_concurrently(calls, self.threads_total)
+        return t_int4, t_swa
+
+    def per_session_step(self, t_int4, t_swa):
+        return self.w.int4_layers * t_int4 + self.w.swa_layers * t_swa
+
+    def describe(self):
+        return (f"fp64 oracle, per sample one int4 layer of one sequence (4 KV heads x 5 query rows over {self.L} "
+                f"positions) and one window-513 layer of one sequence (4 KV heads x 5 rows), each KV head an "
+                f"oracle call on its own host thread; seconds per session-step = "
+                f"{self.w.int4_layers} x int4 layer + {self.w.swa_layers} x window layer")
+
+
+def oracle_sample(seconds_budget=20.0):
+    """cpu_baseline of the kvq arm: OracleStepSample repeated within the budget (at most 4
+    samples), the median sample scaled to session-steps/s."""
+    smp = OracleStepSample()
+    res = []
+    t0 = time.perf_counter()
     while True:
-        O.attention_int4(q, vis, kc, ks, ko, vc, ks, ko, 128 ** -0.5)
-        reps += 1
-        if time.perf_counter() - t0 > seconds_budget / 2 or reps >= 4:
+        res.append(smp.layer_seconds())
+        if time.perf_counter() - t0 > seconds_budget / 2 or len(res) >= 4:
             break
-    t_head = (time.perf_counter() - t0) / reps
-    W = w.window
-    k8 = (raw[: W * 128].reshape(W, 128) & 0x77)
-    q8 = synth.normals(synth.key(99, 3), 0, w.Hq * 128).reshape(w.Hq, 128)
-    lo = np.zeros(w.Hq, np.int64)
-    hi = np.full(w.Hq, W - 1, np.int64)
-    t1 = time.perf_counter()
-    O.attention_fp8(q8, lo, hi, k8, k8, 0.01, 0.01, 128 ** -0.5)
-    t_swa = time.perf_counter() - t1
-    per_step = w.int4_layers * w.Hkv * t_head + w.swa_layers * t_swa
-    return {"value": round(1.0 / per_step, 4), "unit": "session-steps/s", "cores": O.threads, "kind": "oracle",
-            "sample": ("fp64 oracle attention of 1 KV head (5 query rows) of 1 int4 layer at 262,145 positions "
-                       f"({reps}x, {t_head:.3f} s each) scaled x{w.int4_layers * w.Hkv} (10 layers x 4 heads), "
-                       f"plus 1 window-513 layer of 1 sequence ({t_swa:.4f} s) scaled x{w.swa_layers}"),
-            "seconds_per_session_step": per_step}
+    per = statistics.median([smp.per_session_step(a, b) for a, b in res])
+    return {"value": round(1.0 / per, 4), "unit": "session-steps/s", "cores": smp.cores(), "kind": "oracle",
+            "sample": smp.describe() + f"; {len(res)} samples, median", "seconds_per_session_step": per}
 
 
 # ---------------------------------------------------------------- arms
@@ -790,6 +909,27 @@ def run_kvq(args, rank, world, local):
     achieved = sum(call_bytes) / (sum(call_ms) * 1e-3) / 1e9
     del graph
 
+    # ---- per-step times: one decode step captured alone, replayed n_dist times with events
+    # around each replay (the pages' method times 512 steps per point and reports the slowest
+    # tenth against the median)
+    n_dist = 512
+    g1 = torch.cuda.CUDAGraph()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g1, stream=cap):
+            bench.step(W + K - 1)
+    torch.cuda.synchronize()
+    dist_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dist)]
+    for d0, d1 in dist_evs:
+        d0.record()
+        g1.replay()
+        d1.record()
+    torch.cuda.synchronize()
+    step_ms = np.array([d0.elapsed_time(d1) for d0, d1 in dist_evs])
+    step_med = float(np.median(step_ms))
+    assert bench.st.read_error() == 0
+    del g1
+
     # ---- end to end: every step copies its inputs from pinned host memory and reads its
     # outputs back, through the same public calls (captured into a graph with the copies)
     Ke = min(K, 64)
@@ -832,6 +972,8 @@ def run_kvq(args, rank, world, local):
     torch.cuda.empty_cache()
 
     sec = run_64k(device) if rank == 0 else None
+    verify = run_verify(device) if rank == 0 else None
+    cfg2 = run_config2(device) if rank == 0 else None
     cpu = oracle_sample() if rank == 0 else None
 
     if rank == 0:
@@ -845,12 +987,17 @@ def run_kvq(args, rank, world, local):
                          "frac": round(frac, 4), "traffic": attn_traffic(int(np.mean(call_bytes))),
                          "traffic_how": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the attention kernel "
                                         "on the 64k workload, scaled to this call by algorithmic bytes "
-                                        "(profiles/attn_int4_64k.md); null once its sources changed",
+                                        "(one capture, cold cache); null once its sources changed",
                          "peak_kind": peak_kind,
                          "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
                          "kernel": "kvq_decode_attn_int4 call (query prologue/append + split-K attention + combine kernels)",
                          "bytes_per_call": int(np.mean(call_bytes)), "avg_call_us": round(1e3 * np.mean(call_ms), 2)},
             "at_64k": sec,
+            "step_ms_median": round(step_med, 4),
+            "p90_over_median": round(float(np.percentile(step_ms, 90)) / step_med, 4),
+            "step_distribution": f"{n_dist} replays of one decode step captured alone, CUDA events around each",
+            "verify": verify,
+            "config2": cfg2,
             "e2e": {"value": round(e2e_value, 2), "unit": "session-steps/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": Ke,
                     "how": "per step: q, k_new, v_new of all 50 layers copied from pinned host memory, the step, "
@@ -881,41 +1028,26 @@ def bench_ctx0():
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands, on the machine's host cores: each step is a bounded sample of the
-    256k decode step (one KV head of one int4 layer); rank 0 only."""
+    """The oracle as it stands, on the machine's host cores: each step is one OracleStepSample (one
+    int4 layer and one window layer of one sequence, all KV heads), the same scope as the kvq
+    arm's cpu_baseline; the value is session-steps/s; rank 0 only."""
     if rank != 0:
         return
-    import oracle
-    import synth
-    from synth.workloads import config
-
-    w = config(5)
-    O = oracle.Oracle()
-    L = int(w.ctx[0]) + 1
-    raw = synth.draws(synth.key(99, 1), 0, L * 128 // 4).view(np.uint8)
-    kc = (raw[: L * 128] & 15).reshape(L, 128)
-    vc = (raw[: L * 128] >> 4).reshape(L, 128)
-    ks = np.full(L, 0x2E66, np.uint16)
-    ko = np.full(L, 0xC1A0, np.uint16)
-    q = synth.normals(synth.key(99, 2), 0, w.G * 128).reshape(w.G, 128)
-    vis = np.full(w.G, L)
+    smp = OracleStepSample()
     for _ in range(args.warmup):
-        O.attention_int4(q, vis, kc, ks, ko, vc, ks, ko, 128 ** -0.5)
-    t0 = time.perf_counter()
+        smp.layer_seconds()
+    per = []
     for _ in range(args.steps):
-        O.attention_int4(q, vis, kc, ks, ko, vc, ks, ko, 128 ** -0.5)
-    t = time.perf_counter() - t0
-    per_sample = t / args.steps
-    frac = 1.0 / (w.int4_layers * w.Hkv)      # one KV head of one int4 layer of one sequence
-    value = frac / per_sample
-    sample = (f"each step: fp64 oracle attention of 1 KV head (5 query rows) of 1 int4 layer at {L} positions "
-              f"= 1/{w.int4_layers * w.Hkv} of one sequence's int4 work per decode step (window layers excluded)")
+        per.append(smp.per_session_step(*smp.layer_seconds()))
+    per_step = float(np.mean(per))
+    value = 1.0 / per_step
+    sample = smp.describe() + "; one sample per step"
     line = {"metric": METRIC, "value": round(value, 5), "unit": "session-steps/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_sample * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": step_config(args, world),
-            "cpu_baseline": {"value": round(value, 5), "unit": "session-steps/s", "cores": O.threads,
+            "cpu_baseline": {"value": round(value, 5), "unit": "session-steps/s", "cores": smp.cores(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 5), "unit": "session-steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -934,11 +1066,12 @@ def main():
     ap.add_argument("--sequences", type=int, default=None,
                     help="--only swa: this many sequences instead of the 256k step's 8")
     ap.add_argument("--layers", type=int, default=None, help="--only swa: this many window layers instead of 40")
-    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity", "verify"],
+    ap.add_argument("--only", default=None, choices=["64k", "swa", "ab", "capacity", "verify", "config2"],
                     help="run only the 64k single-layer int4 point, only the 40 window layers of the 256k "
                          "step (small cases for profiling), the A/B of full-layer formats (ab), the "
-                         "capacity and throughput sweep of a fixed KV pool (capacity), or the speculative "
-                         "verify workload with both many-row kernels (verify)")
+                         "capacity and throughput sweep of a fixed KV pool (capacity), the speculative "
+                         "verify workload at S = 1..8 (verify), or the 16 x 8,192 layer with L2 flushed "
+                         "between calls (config2)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -958,7 +1091,12 @@ def main():
     elif args.only == "verify":
         import torch
         torch.cuda.set_device(local)
-        print(json.dumps(run_verify(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
+        print(json.dumps(run_verify(f"cuda:{local}", steps=args.steps, warmup=args.warmup,
+                                    S_values=tuple(range(1, 9)))), flush=True)
+    elif args.only == "config2":
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_config2(f"cuda:{local}", steps=args.steps, warmup=args.warmup)), flush=True)
     elif args.only == "swa":
         import torch
         torch.cuda.set_device(local)

@@ -29,7 +29,8 @@
  *    or by a kernel that allows dependent launch only after writing them. Within a call each
  *    kernel waits for the one before it before reading anything that kernel writes.
  *  - Fixed geometry: head_dim 128, 64 tokens per page.
- *  - Thread-safe: no mutable global state beyond per-device attribute caches.
+ *  - Thread-safe: no mutable global state beyond per-device attribute caches and the
+ *    test-only wait limit of kvq_set_stage_wait_limit_ns.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -281,6 +282,18 @@ kvq_status kvq_decode_attn_fp8_swa(const kvq_fp8_ring* ring, const void* q, kvq_
  * arguments as kvq_decode_attn_fp8_swa (capacity a positive multiple of 64).
  */
 kvq_status kvq_fp8_swa_plan(int capacity, int B, int S, int num_q_heads, int num_kv_heads, int32_t out[4]);
+
+/*
+ * kvq_set_stage_wait_limit_ns -- test hook for the failure path of the bounded waits: sets, for
+ * every later launch in the process, how long the split-K attention kernel of
+ * kvq_decode_attn_int4 (and of the window path's split-K form) waits for a page's copy into a
+ * shared-memory stage, and for a stage to be released, before it gives up, sets
+ * KVQ_DEVERR_TIMEOUT and abandons the call's remaining pages (outputs then invalid). ns = 0 gives
+ * up at the first unsuccessful check. The wait for copies still in flight before a CTA exits
+ * always keeps the default. Default 2000000000 (2 s); the default is what a caller should run
+ * with. Always returns KVQ_OK.
+ */
+kvq_status kvq_set_stage_wait_limit_ns(uint64_t ns);
 
 /*
  * kvq_decode_attn_int4_noalloc -- the same computation as kvq_decode_attn_int4 for callers

@@ -73,6 +73,8 @@ def _load():
     L.kvq_decode_attn_int4_noalloc.restype = i32
     L.kvq_decode_attn_int4_noalloc.argtypes = [ctypes.POINTER(Int4Cache), vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                                f32, f32, vp, vp, vp, vp]
+    L.kvq_set_stage_wait_limit_ns.restype = i32
+    L.kvq_set_stage_wait_limit_ns.argtypes = [u64]
     L.kvq_decode_attn_fp8_swa.restype = i32
     L.kvq_decode_attn_fp8_swa.argtypes = [ctypes.POINTER(Fp8Ring), vp, i32, i32, i32, i32, vp, i32, vp, vp, f32,
                                           f32, f32, vp, vp, sz, vp, vp]
@@ -240,6 +242,14 @@ def kvq_decode_attn_int4_noalloc(cache: Int4Cache, Mq, Mk, q, ctx_len, out, dev_
            lib.kvq_decode_attn_int4_noalloc(ctypes.byref(cache), _ptr(Mq), _ptr(Mk), _ptr(q), _dtype_code(q), B, S,
                                             Hq, _ptr(ctx_len), _ptr(k_new), _ptr(v_new), sm_scale, eps, _ptr(out),
                                             _ptr(q_rot_out), _ptr(dev_err), _stream(stream)))
+
+
+STAGE_WAIT_DEFAULT_NS = 2_000_000_000
+
+
+def kvq_set_stage_wait_limit_ns(ns: int):
+    """Test hook: the split-K attention kernel's stage-wait limit for later launches (default 2 s)."""
+    _check("kvq_set_stage_wait_limit_ns", lib.kvq_set_stage_wait_limit_ns(int(ns)))
 
 
 def kvq_fp8_append(ring: Fp8Ring, k, v, seq_ids, positions, k_scale: float, v_scale: float, dev_err, stream=None):

@@ -251,6 +251,11 @@ kvq_status kvq_decode_attn_int4_fwht(const kvq_int4_cache* cache, const float* w
                           workspace, workspace_bytes, q_rot_out, dev_err, stream, 1);
 }
 
+kvq_status kvq_set_stage_wait_limit_ns(uint64_t ns) {
+  kvq::set_stage_wait_limit_ns(ns);
+  return KVQ_OK;
+}
+
 kvq_status kvq_fp8_swa_plan(int capacity, int B, int S, int num_q_heads, int num_kv_heads, int32_t out[4]) {
   if (!out) return KVQ_ERR_INVALID_ARG;
   if (capacity < KVQ_PAGE_SIZE || capacity % KVQ_PAGE_SIZE || num_kv_heads < 1) return KVQ_ERR_INVALID_ARG;

@@ -30,6 +30,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -103,6 +104,9 @@ struct AttnParams {
   int32_t* dev_err;
   int ntg, nkg, nstages, rows_pad;
   int n_cta;
+  // limit of the split kernel's waits on its shared-memory stages (consumers on a page's
+  // copy, the producer on a stage's release); the drain of copies in flight keeps kWaitLimitNs
+  unsigned long long stage_wait_ns;
 };
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -256,7 +260,7 @@ __device__ __forceinline__ void produce_pages(const AttnParams& p, const int* pr
     for (int j = 0; j < n; ++j) {
       const long long sj = __shfl_sync(0xffffffffu, src, j);
       if (lane == 0 && !halt) {
-        if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1)) {
+        if (f > 0 && !mbar_wait_bounded(&empty[s], (f - 1) & 1, p.stage_wait_ns)) {
           set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
           flags[0] = 1;
           halt = 1;
@@ -464,7 +468,7 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
       const long long pg = p0 + k;
       const int s = k % nst;
       const int f = k / nst;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], f & 1));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], f & 1, p.stage_wait_ns));
       if (!ok) {
         if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
         flags[0] = 1;
@@ -2005,6 +2009,10 @@ cudaError_t launch_tc(AttnParams& p, long long p_max, cudaStream_t stream) {
 
 }  // namespace
 
+std::atomic<unsigned long long> g_stage_wait_ns{kWaitLimitNs};
+
+void set_stage_wait_limit_ns(unsigned long long ns) { g_stage_wait_ns.store(ns, std::memory_order_relaxed); }
+
 size_t workspace_qrot_bytes(int B, int S, int Hq) { return align_up((size_t)B * S * Hq * kD * 4, 256); }
 
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv) {
@@ -2014,6 +2022,7 @@ size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv) {
 
 cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
   AttnParams p{};
+  p.stage_wait_ns = g_stage_wait_ns.load(std::memory_order_relaxed);
   p.B = job.B;
   p.S = job.S;
   p.Hq = job.Hq;

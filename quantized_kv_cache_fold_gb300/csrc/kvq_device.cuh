@@ -70,15 +70,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed. Gives up after
-// kWaitLimitNs (or 2^30 polls) and returns false; the caller records
-// KVQ_DEVERR_TIMEOUT and abandons its work.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits until the phase with the given parity has completed. Gives up after limit_ns
+// (kWaitLimitNs unless a caller passes a shorter limit; 0: after the first unsuccessful
+// try) or 2^30 polls and returns false; the caller records KVQ_DEVERR_TIMEOUT and abandons
+// its work.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((it & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
   return false;
 }

@@ -98,6 +98,9 @@ kvq_status check_decode_int4_args(const kvq_int4_cache* cache, const float* Mq, 
                                   const void* k_new, const void* v_new, float sm_scale, float eps, const float* out,
                                   const float* q_rot_out, const int32_t* dev_err);
 
+// Limit of the split-K attention kernel's stage waits for later launches (kvq_set_stage_wait_limit_ns).
+void set_stage_wait_limit_ns(unsigned long long ns);
+
 size_t workspace_qrot_bytes(int B, int S, int Hq);
 size_t workspace_partials_bytes(int B, int S, int Hq, int Hkv);
 
