@@ -211,12 +211,6 @@ size_t kvq_decode_workspace_bytes(int B, int S, int num_q_heads, int num_kv_head
  *             256-byte aligned; contents need no initialisation.
  *   q_rot_out: optional device float [B][S][num_q_heads][128] copy of q~ (NULL to skip).
  * Requires 1 <= B <= KVQ_MAX_SEQS, 1 <= S <= 8, S*(num_q_heads/num_kv_heads) <= 48.
- * Every call runs the split-K kernel on mma.sync tensor cores by default. For calls with more
- * than 32 query rows per KV head the environment variable KVQ_MANY_ROWS_KERNEL selects one of two
- * other kernels: "tile" a shared-tile mma.sync kernel (each page's codes converted once into f16
- * tiles that every 8-row tile reads), "tcgen05" a variant on the asynchronous tcgen05 tensor
- * cores (accumulators in tensor memory); same results within the stated tolerance. Any other
- * value, or none, keeps the default.
  */
 kvq_status kvq_decode_attn_int4(const kvq_int4_cache* cache, const float* Mq, const float* Mk, const void* q,
                                 kvq_dtype dtype, int B, int S, int num_q_heads, const int32_t* ctx_len,

@@ -16,16 +16,17 @@
 // on mbarriers; consumer warps are arranged as token groups x tile groups. A tile is 8
 // query rows (rows = S x G query heads of the KV head, row n = r*G + g). Per page a warp:
 //   QK^T on tensor cores (mma.m16n8k16, fp32 accumulate): A = 16 tokens x 16 dims of K codes
-//        read as f16 1024 + c (low nibbles) or 1024 + 16c (high nibbles, whose query values
-//        are divided by 16), B = 16 dims x 8 query rows of q~ in f16; the accumulator starts at
-//        -1024 sum(q~ fragment), so it holds sum q~ c exactly up to fp32 rounding;
+//        read as the f16 subnormals c 2^-24 (low nibbles) or 16c 2^-24 (high nibbles, whose
+//        query values are divided by 16), B = 16 dims x 8 query rows of q~ in f16, so the
+//        accumulator holds 2^-24 sum q~ c up to fp32 rounding;
 //   score = log2(e)*sm_scale*(s_K*dot + o_K*sum(q~)) -- scale and offset per token;
 //   online softmax with exp2 against a lazily moved base (moved only when a score passes it
 //        by more than 8, or by anything on pages with a V scale of 255 or more);
 //   PV on tensor cores: A = 16 dims x 16 tokens of V codes read as f16 subnormals
-//        (c - 7.5) 2^(k - 23), B = 16 tokens x 8 rows of p*s_V in f16 (movmatrix transposes
-//        the QK accumulator), plus
-//        sum_j p_j (o_V + 7.5 s_V) added per row; the partial undoes 2^(k - 23) per dim.
+//        (c - 7.5) 2^(k - 23), exact and centred (which keeps the fp32 sums of long contexts
+//        small), B = 16 tokens x 8 rows of p*s_V in f16 (movmatrix transposes the QK
+//        accumulator), plus sum_j p_j (o_V + 7.5 s_V) added per row; the partial undoes
+//        2^(k - 23) per dim.
 
 #include <algorithm>
 #include <cmath>
@@ -48,10 +49,6 @@ namespace {
 #endif
 #ifndef KVQ_STAGES_INT4
 #define KVQ_STAGES_INT4 12
-#endif
-// K codes enter QK^T as 1024+c (no per-element bias subtraction); see unpack8_biased.
-#ifndef KVQ_K_BIASED
-#define KVQ_K_BIASED 1
 #endif
 #ifndef KVQ_INT4_MAXREG
 #define KVQ_INT4_MAXREG 168
@@ -355,7 +352,6 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
     // ---- segment setup: query fragments and per-row limits
     uint32_t qf[NT][8][2];
     float qs[NT][2];
-    float negbias[NT][2];  // biased K path: -1024 * sum of the row's query fragment values
     int lim_lo[NT][2], lim_hi[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -397,26 +393,16 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
       for (int i = 0; i < 32; ++i) part += qv[i];
       if (FMT == 0) {
         // k-step 2wi+e, slots (2t,2t+1) <- dims (8wi+2e, +4), slots (2t+8,2t+9) <- (+1, +5);
-        // the second pair meets high nibbles, read as 16*code in the biased K path, so its
-        // query values are divided by 16 (exact).
-        const float hs = KVQ_K_BIASED ? 0.0625f : 1.0f;
-        float bsum = 0.0f;
+        // the second pair meets high nibbles, read as 16 c 2^-24 (unpack8_sub), so its query
+        // values are divided by 16 (exact).
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int d0 = 8 * wi + 2 * e;
-            const uint32_t b0 = pack_f16x2(qv[d0], qv[d0 + 4]);
-            const uint32_t b1 = pack_f16x2(qv[d0 + 1] * hs, qv[d0 + 5] * hs);
-            qf[nt][2 * wi + e][0] = b0;
-            qf[nt][2 * wi + e][1] = b1;
-            bsum += (h2f_lo(b0) + h2f_hi(b0)) + (h2f_lo(b1) + h2f_hi(b1));
+            qf[nt][2 * wi + e][0] = pack_f16x2(qv[d0], qv[d0 + 4]);
+            qf[nt][2 * wi + e][1] = pack_f16x2(qv[d0 + 1] * 0.0625f, qv[d0 + 5] * 0.0625f);
           }
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          negbias[nt][j] = KVQ_K_BIASED ? -1024.0f * __shfl_sync(0xffffffffu, bsum, (2 * t + j) * 4) : 0.0f;
       } else {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -493,8 +479,8 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
                 const int tok = 16 * (mt0 + u) + g + 8 * hh;
                 const uint32_t mk = Km[tok], mv = Vm[tok];
                 const float sk = h2f_lo(mk), ok_ = h2f_hi(mk), sv = h2f_lo(mv), ovv = h2f_hi(mv);
-                ka[u][hh] = sk * p.score_scale;
-                kb[u][hh] = KVQ_K_BIASED ? ok_ : fmaf(8.0f, sk, ok_);
+                ka[u][hh] = sk * p.score_scale * 16777216.0f;  // the MMA's products carry 2^-24
+                kb[u][hh] = ok_;
                 va[u][hh] = sv;
                 vb[u][hh] = fmaf(7.5f, sv, ovv);
               }
@@ -526,19 +512,14 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 #pragma unroll
               for (int u = 0; u < MTU; ++u)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) d[nt][u][c] = negbias[nt][c & 1];
+                for (int c = 0; c < 4; ++c) d[nt][u][c] = 0.0f;
 #pragma unroll
             for (int wi = 0; wi < 4; ++wi) {
               uint32_t ha[MTU][4], hb[MTU][4];
 #pragma unroll
               for (int u = 0; u < MTU; ++u) {
-                if (KVQ_K_BIASED) {
-                  unpack8_biased(A[u][wi], ha[u]);
-                  unpack8_biased(Bw[u][wi], hb[u]);
-                } else {
-                  unpack8_centred(A[u][wi], ha[u]);
-                  unpack8_centred(Bw[u][wi], hb[u]);
-                }
+                unpack8_sub(A[u][wi], ha[u]);
+                unpack8_sub(Bw[u][wi], hb[u]);
               }
 #pragma unroll
               for (int e = 0; e < 2; ++e)
@@ -822,955 +803,6 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 
 }
 
-// ------------------------------------------------------------ many query rows per KV head
-// For S x G > 8 query rows (verify blocks) the rows span several 8-row tiles. Converting each
-// page's 4-bit codes once per tile would repeat the dominant ALU work, so here the conversion
-// is done once per page into shared f16 tiles that every tile warp reads with ldmatrix:
-//
-//   warp 0          producer: page-head blocks into kVStages int4 stages (produce_pages)
-//   kConvWarps      converters: K codes -> f16 biased (1024 + c / 1024 + 16c, see
-//                   unpack8_biased), V codes -> f16 subnormals (c - 7.5) 2^(k - 23) (see
-//                   unpack8_v), per-token scale/offset -> fp32, into one of kVBufs tile
-//                   buffers; each converts an equal share of the 64 tokens
-//   T tile warps    one per 8 query rows: QK^T, online softmax and PV on tensor
-//                   cores over every page of the CTA's range, partial per segment and row
-//
-// A tile buffer holds K16 [64 tokens][16 chunks of 16 B], V16 the same, meta [64] float4. Chunk
-// j of a token row holds the eight f16 values of code word j (dims 8j .. 8j+7) in the order the
-// unpack produces them (dims 8j + {0,4,1,5,2,6,3,7}) and sits at chunk position j ^ (token & 7),
-// so the eight rows an ldmatrix 8x8 matrix reads fall in eight different bank groups.
-constexpr int kVStages = 8;
-constexpr int kVBufs = 3;
-constexpr int kTileRow = 256;                                // bytes per token row of an f16 tile
-constexpr int kVBuf = 2 * kPage * kTileRow + kPage * 16;     // K16, V16, meta
-#ifndef KVQ_VERIFY_CONV
-#define KVQ_VERIFY_CONV 2
-#endif
-// Row tiles (8 query rows each) from which the environment variable KVQ_MANY_ROWS_KERNEL may
-// select this shared-tile kernel ("tile") or the tcgen05 kernel ("tcgen05") instead of the split
-// kernel, which is the default for every call (faster at 5 and 6 tiles as well: 516 against
-// 560 us at S = 8, GQA 5, 64 x 16,384).
-#ifndef KVQ_VERIFY_MIN_TILES
-#define KVQ_VERIFY_MIN_TILES 5
-#endif
-constexpr int kConvWarps = KVQ_VERIFY_CONV;  // 64 / kConvWarps tokens each
-static_assert(64 % (2 * kConvWarps) == 0, "converter warps split the page's tokens in pairs of rows");
-
-struct VerifyLayout {
-  size_t bufs, full, empty, ready, freeb, valid, vvalid, pre, flags, total;
-  __host__ __device__ explicit VerifyLayout(int B) {
-    bufs = (size_t)kVStages * kStage4;  // int4 stages first, from offset 0
-    full = bufs + (size_t)kVBufs * kVBuf;
-    empty = full + 8 * kVStages;
-    ready = empty + 8 * kVStages;
-    freeb = ready + 8 * kVBufs;
-    valid = freeb + 8 * kVBufs;
-    vvalid = valid + 4 * kVStages;
-    pre = vvalid + 4 * kVBufs;
-    flags = align_up(pre + 4 * (size_t)(B + 1), 16);
-    total = flags + 16;
-  }
-};
-
-// Dim held by element e (0..7) of chunk j of a tile row.
-__device__ __forceinline__ int tile_dim(int j, int e) { return 8 * j + (e >> 1) + 4 * (e & 1); }
-
-__global__ void __launch_bounds__((1 + kConvWarps + 6) * 32, 1) attn_verify_kernel(const AttnParams p) {
-  constexpr int kTokPerConv = kPage / kConvWarps;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const VerifyLayout L(p.B);
-  uint8_t* stages = smem;
-  uint8_t* bufs = smem + L.bufs;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
-  uint64_t* ready = reinterpret_cast<uint64_t*>(smem + L.ready);
-  uint64_t* freeb = reinterpret_cast<uint64_t*>(smem + L.freeb);
-  volatile int* valid = reinterpret_cast<volatile int*>(smem + L.valid);
-  volatile int* vvalid = reinterpret_cast<volatile int*>(smem + L.vvalid);
-  int* pre = reinterpret_cast<int*>(smem + L.pre);
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = p.ntg;  // tile warps
-
-  griddep_wait();
-  griddep_launch_dependents();
-  build_prefix(p, 0, pre, flags);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvWarps);
-    }
-    for (int b = 0; b < kVBufs; ++b) {
-      mbar_init(&ready[b], kConvWarps);
-      mbar_init(&freeb[b], T);
-    }
-  }
-  fence_barrier_init();
-  __syncthreads();
-
-  if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
-  const long long P = (long long)p.Hkv * pre[p.B];
-  const int n_eff = (int)min((long long)p.n_cta, P);
-  if ((int)blockIdx.x >= n_eff) return;
-  const long long p0 = (long long)blockIdx.x * P / n_eff;
-  const long long p1 = (long long)(blockIdx.x + 1) * P / n_eff;
-  const int npages = (int)(p1 - p0);
-
-  if (warp == 0) {
-    produce_pages<0>(p, pre, stages, full, empty, valid, flags, kVStages, p0, p1, lane);
-    return;
-  }
-
-  // ------------------------------------------------------------ converter warps
-  if (warp <= kConvWarps) {
-    const int cw = warp - 1;
-    for (int k = 0; k < npages; ++k) {
-      const int s = k % kVStages, b = k % kVBufs;
-      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(k / kVStages) & 1u));
-      if (ok && k >= kVBufs)  // the buffer's previous page has been released by every tile warp
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&freeb[b], (uint32_t)(k / kVBufs - 1) & 1u));
-      if (!ok) {
-        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-        flags[0] = 1;
-        break;
-      }
-      const uint8_t* st4 = stages + (size_t)s * kStage4;
-      uint8_t* buf = bufs + (size_t)b * kVBuf;
-      const int vpage = valid[s];
-      if (cw == 0 && lane == 0) vvalid[b] = vpage;
-      if (vpage) {
-        // lane = (row of a token pair, code word j); all loads of the share are issued first
-        constexpr int kIt = kTokPerConv / 2;
-        const int j = lane & 15;
-        uint32_t kw[kIt], vw[kIt];
-#pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-          const int tok = kTokPerConv * cw + 2 * it + (lane >> 4);
-          kw[it] = *reinterpret_cast<const uint32_t*>(st4 + tok * kRec4 + 4 * j);
-          // V records: 16-byte chunk c of slot s stored at chunk c ^ ((s >> 1) & 3)
-          vw[it] = *reinterpret_cast<const uint32_t*>(st4 + kPage * kRec4 + tok * kRec4 +
-                                                      16 * ((j >> 2) ^ ((tok >> 1) & 3)) + 4 * (j & 3));
-        }
-#pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-          const int tok = kTokPerConv * cw + 2 * it + (lane >> 4);
-          uint32_t h[4];
-          unpack8_biased(kw[it], h);
-          *reinterpret_cast<uint4*>(buf + tok * kTileRow + 16 * (j ^ (tok & 7))) = make_uint4(h[0], h[1], h[2], h[3]);
-          unpack8_v(vw[it], h);
-          *reinterpret_cast<uint4*>(buf + kPage * kTileRow + tok * kTileRow + 16 * (j ^ (tok & 7))) =
-              make_uint4(h[0], h[1], h[2], h[3]);
-        }
-        if (lane < kTokPerConv) {
-          const int tok = kTokPerConv * cw + lane;
-          const uint32_t* meta = reinterpret_cast<const uint32_t*>(st4 + 2 * kPage * kRec4);
-          const uint32_t mk = meta[tok], mv = meta[kPage + tok];
-          const float sv = h2f_lo(mv);
-          reinterpret_cast<float4*>(buf + 2 * kPage * kTileRow)[tok] =
-              make_float4(h2f_lo(mk) * p.score_scale, h2f_hi(mk), sv, fmaf(7.5f, sv, h2f_hi(mv)));
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&ready[b]);
-        mbar_arrive(&empty[s]);
-      }
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ tile warps
-  const int tg = warp - 1 - kConvWarps;
-  const int g = lane >> 2, t = lane & 3;
-  const int R = p.R, G = p.G;
-  long long seg_start = p0;
-  int k = 0;  // page index within the CTA's range
-  while (seg_start < p1) {
-    int b, h, lp0, np;
-    decode_page(pre, p.B, p.Hkv, seg_start, b, h, lp0, np);
-    const long long seg_end = min(p1, seg_start + (np - lp0));
-    const int seg = b * p.Hkv + h;
-    bool bad_ctx = false;
-    const int ctxb = eff_ctx(p, b, bad_ctx, 0);
-
-    // ---- query fragments of this warp's 8 rows. Element pairs of k-step ks: b0 <- dims
-    // (16 ks + t, 16 ks + t + 4), b1 <- (16 ks + 8 + t, 16 ks + 12 + t) (the tile's dim order);
-    // odd t meets high nibbles (1024 + 16c), so those query values are divided by 16 (exact).
-    uint32_t qf[8][2];
-    float qs[2], negbias[2];
-    int lim_hi[2];
-    {
-      const int nB = 8 * tg + g;
-      float qv[32];  // qv[4 ks + i] = q~[dim 16 ks + t + 4 i]
-      if (nB < R) {
-        const float* qrow = p.q_rot + (((size_t)b * p.S + nB / G) * p.Hq + h * G + nB % G) * kD;
-#pragma unroll
-        for (int m = 0; m < 32; ++m) qv[m] = qrow[4 * m + t];
-      } else {
-#pragma unroll
-        for (int m = 0; m < 32; ++m) qv[m] = 0.0f;
-      }
-      float part = 0.0f, bsum = 0.0f;
-      const float hs = (t & 1) ? 0.0625f : 1.0f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t b0 = pack_f16x2(qv[4 * ks] * hs, qv[4 * ks + 1] * hs);
-        const uint32_t b1 = pack_f16x2(qv[4 * ks + 2] * hs, qv[4 * ks + 3] * hs);
-        qf[ks][0] = b0;
-        qf[ks][1] = b1;
-        bsum += (h2f_lo(b0) + h2f_hi(b0)) + (h2f_lo(b1) + h2f_hi(b1));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) part += qv[4 * ks + i];
-      }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-      bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        qs[j] = __shfl_sync(0xffffffffu, part, (2 * t + j) * 4) * p.score_scale;
-        negbias[j] = -1024.0f * __shfl_sync(0xffffffffu, bsum, (2 * t + j) * 4);
-        const int nC = 8 * tg + 2 * t + j;
-        lim_hi[j] = ctxb + (nC < R ? nC / G : 0);
-      }
-    }
-
-    // lazy exponent base, as in attn_kernel: m, muse, thr per accumulator row
-    float m[2] = {-INFINITY, -INFINITY}, muse[2] = {0.0f, 0.0f}, thr[2] = {-INFINITY, -INFINITY};
-    float l[2] = {0.0f, 0.0f}, ov[2] = {0.0f, 0.0f}, acc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
-
-    for (long long pg = seg_start; pg < seg_end; ++pg, ++k) {
-      const int bi = k % kVBufs;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ready[bi], (uint32_t)(k / kVBufs) & 1u));
-      if (!ok) {
-        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-        flags[0] = 1;
-      }
-      if (__any_sync(0xffffffffu, flags[0] != 0)) break;
-      const int lp = lp0 + (int)(pg - seg_start);
-      if (vvalid[bi]) {
-        const uint8_t* buf = bufs + (size_t)bi * kVBuf;
-        const uint32_t Kt = smem_addr(buf), Vt = smem_addr(buf + kPage * kTileRow);
-        const float4* meta = reinterpret_cast<const float4*>(buf + 2 * kPage * kTileRow);
-        const bool need_mask = (lp + 1) * kPage > ctxb + 1;
-
-        // ---- scores for the page's 4 m-tiles (16 tokens each), chains interleaved over m-tiles
-        float d[4][4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) d[u][c] = negbias[c & 1];
-        const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), achunk = lane >> 4;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t a[4][4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int tok = 16 * u + arow, ch = 2 * ks + achunk;
-            ldsm_x4(a[u], Kt + tok * kTileRow + 16 * (ch ^ (tok & 7)));
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) mma_16816(d[u], a[u][0], a[u][1], a[u][2], a[u][3], qf[ks][0], qf[ks][1]);
-        }
-        float sc[4][4], va[4][2], vb[4][2];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float4 mt = meta[16 * u + g + 8 * hh];
-            va[u][hh] = mt.z;
-            vb[u][hh] = mt.w;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) sc[u][2 * hh + j] = fmaf(d[u][2 * hh + j], mt.x, fmaf(mt.y, qs[j], -muse[j]));
-          }
-        if (need_mask) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int pos = lp * kPage + 16 * u + g + 8 * hh;
-#pragma unroll
-              for (int j = 0; j < 2; ++j)
-                if (pos > lim_hi[j]) sc[u][2 * hh + j] = -INFINITY;
-            }
-        }
-
-        // ---- online softmax (lazy base: moved only when a score exceeds it by more than 8,
-        // or by anything on a page holding a V scale >= 255; see attn_kernel)
-        {
-          float mx[2];
-          bool need = false;
-          float vmax = 0.0f;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) vmax = fmaxf(vmax, fmaxf(va[u][0], va[u][1]));
-          const bool big = vmax >= 255.0f;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float v = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v = fmaxf(v, fmaxf(sc[u][j], sc[u][2 + j]));
-            mx[j] = v;
-            need |= v > (big ? fminf(thr[j], 0.0f) : thr[j]);
-          }
-          if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const float mnew = fmaxf(m[j], muse[j] + warp_max_g(mx[j]));
-              if (mnew != m[j]) {
-                const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
-                const float alpha = fast_exp2(m[j] - mu2);
-                const float delta = muse[j] - mu2;
-                l[j] *= alpha;
-                ov[j] *= alpha;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  acc[i][j] *= alpha;
-                  acc[i][2 + j] *= alpha;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  sc[u][j] += delta;
-                  sc[u][2 + j] += delta;
-                }
-                m[j] = mnew;
-                muse[j] = mu2;
-                thr[j] = mnew == -INFINITY ? -INFINITY : 8.0f;
-              }
-            }
-          }
-        }
-
-        // ---- P and PV (A = V^T from the f16 V tile with ldmatrix.trans)
-        const int vtok = (lane & 7) + 8 * (lane >> 4), vchunk = (lane >> 3) & 1;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float pr[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) pr[c] = fast_exp2(sc[u][c]);
-          l[0] += pr[0] + pr[2];
-          l[1] += pr[1] + pr[3];
-          ov[0] = fmaf(pr[0], vb[u][0], fmaf(pr[2], vb[u][1], ov[0]));
-          ov[1] = fmaf(pr[1], vb[u][0], fmaf(pr[3], vb[u][1], ov[1]));
-          const uint32_t pb0 = movmatrix_trans(pack_f16x2_sat(pr[0] * va[u][0], pr[1] * va[u][0]));
-          const uint32_t pb1 = movmatrix_trans(pack_f16x2_sat(pr[2] * va[u][1], pr[3] * va[u][1]));
-          const int tok = 16 * u + vtok;
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const int ch = 2 * cc + vchunk;
-            uint32_t a[4];
-            ldsm_x4_trans(a, Vt + tok * kTileRow + 16 * (ch ^ (tok & 7)));
-            mma_16816(acc[cc], a[0], a[1], a[2], a[3], pb0, pb1);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&freeb[bi]);
-    }
-
-    // ---- segment end: this warp's rows of the CTA partial
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float lt = warp_sum_g(l[j]);
-      const float ot = warp_sum_g(ov[j]);
-      const int row = 8 * tg + 2 * t + j;
-      if (row < R) {
-        float* dst = p.partials + ((size_t)(blockIdx.x + seg) * R + row) * kPartialStride;
-        if (g == 0) {
-          dst[0] = m[j];
-          dst[1] = lt;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int d0 = tile_dim(2 * i, g), d1 = tile_dim(2 * i + 1, g);
-          dst[2 + d0] = fmaf(acc[i][j], v_unscale(d0 & 3), ot);  // V tiles hold unpack8_v values
-          dst[2 + d1] = fmaf(acc[i][2 + j], v_unscale(d1 & 3), ot);
-        }
-      }
-    }
-    if (__any_sync(0xffffffffu, flags[0] != 0)) break;
-    seg_start = seg_end;
-  }
-}
-
-// ------------------------------------------------------------ many query rows: tcgen05 variant
-// The shared-tile kernel above is bound by shared-memory reads: every 8-row tile warp reads the
-// page's f16 tiles through ldmatrix. Here the two contractions run on the asynchronous tensor
-// cores (tcgen05.mma, accumulators in tensor memory), so each tile is read once per product for
-// all query rows. Work unit: up to two pages (128 tokens) of one segment.
-//
-//   warp 0       producer: page-head blocks into kTcStages int4 stages (produce_pages)
-//   warps 1-2    converters: K codes -> K^ (unpack8_biased values), V codes -> V^ (unpack8_v
-//                values), per-token fp32 (s_K * score scale, o_K, s_V, o_V + 7.5 s_V); K^ and
-//                V^ token-major, 128-byte rows of 64 dims, 128-byte swizzle, dims in the
-//                unpacked order 8w + {0, 4, 1, 5, 2, 6, 3, 7}
-//   warp 3       MMA: S = K^ Q'^T into tensor memory (M = 128 tokens, N = rows rounded up to
-//                16, K = 128 dims, K-major operands); O += V^T P (M = 128 dims, N = rows,
-//                K = 128 tokens; both operands token-major, i.e. MN-major)
-//   warps 4-15   softmax: thread = token (tensor-memory lane 32 (warp % 4) + lane), rows split
-//                in three groups of 16 between warps w, w + 4 and w + 8; lazy exponent base as in
-//                attn_kernel; P s_V written token-major (f16) for the PV product
-//
-// Q' is the query with the high-nibble dims divided by 16 (K^ holds 1024 + c and 1024 + 16c);
-// the bias 1024 sum(Q') of each row is subtracted from S in fp32. Every wait is bounded; the
-// softmax warps take every decision that steers their named barriers through barrier
-// reductions, so they always meet at the same barriers.
-constexpr int kTcStages = 4;
-constexpr int kTcConv = 2;
-constexpr int kTcSoft = 12;
-constexpr int kTcThreads = (1 + kTcConv + 1 + kTcSoft) * 32;
-constexpr int kTcHalf = 16;  // rows per softmax thread (three row groups)
-constexpr int kTcMaxRows = 48;
-
-struct TcLayout {  // offsets from the 1024-byte aligned start of dynamic shared memory
-  size_t kt, vt, pt, qt, meta, stages, bars, valid, vvalid, flags, taddr, rowc, rowst, ovrow, rowm, red, pre, total;
-  __host__ __device__ explicit TcLayout(int B) {
-    kt = 0;                     // [2][2 dim-atoms][128 tokens][128 B]
-    vt = kt + 2 * 32768;        // [2][2 dim-atoms][128 tokens][128 B]
-    pt = vt + 2 * 32768;        // [2][128 tokens][128 B] (rows 0..63)
-    qt = pt + 2 * 16384;        // [2 dim-atoms][48 rows][128 B]
-    meta = qt + 2 * 6144;       // [2][128] float4
-    stages = meta + 2 * 2048;   // kTcStages int4 stages
-    bars = stages + (size_t)kTcStages * kStage4;
-    valid = bars + 8 * 32;
-    vvalid = valid + 4 * kTcStages;  // [2][2]
-    flags = vvalid + 16;
-    taddr = flags + 32;
-    rowc = align_up(taddr + 16, 16);     // [48] float4: -bias, qs, -muse, thr
-    rowst = rowc + 16 * kTcMaxRows;      // [48] m
-    ovrow = rowst + 4 * kTcMaxRows;      // [48] offset sums of the finished segment
-    rowm = ovrow + 4 * kTcMaxRows;       // [12][16] per-warp row maxima
-    red = rowm + 4 * kTcSoft * kTcHalf;  // [12][16][2] per-warp l, ov sums
-    pre = red + 8 * kTcSoft * kTcHalf;
-    total = pre + 4 * (size_t)(B + 1);
-  }
-};
-
-// Unit iterator shared by all roles: consecutive pairs of pages within each segment of the
-// CTA's range.
-struct TcUnits {
-  const AttnParams& p;
-  const int* pre;
-  long long seg_start, seg_end, p1;
-  int b, h, lp0, np, j0, kseg, sidx;
-  __device__ TcUnits(const AttnParams& p_, const int* pre_, long long p0, long long p1_)
-      : p(p_), pre(pre_), seg_start(p0), seg_end(p0), p1(p1_), b(0), h(0), lp0(0), np(0), j0(0), kseg(0), sidx(-1) {}
-  // advance to the next unit; false at the end. first = the unit starts a segment.
-  __device__ bool next(bool& first) {
-    j0 += 2;
-    first = false;
-    if (sidx < 0 || seg_start + j0 >= seg_end) {
-      if (sidx >= 0) {
-        kseg += (int)(seg_end - seg_start);
-        seg_start = seg_end;
-      }
-      if (seg_start >= p1) return false;
-      decode_page(pre, p.B, p.Hkv, seg_start, b, h, lp0, np);
-      seg_end = min(p1, seg_start + (np - lp0));
-      j0 = 0;
-      ++sidx;
-      first = true;
-    }
-    return true;
-  }
-  __device__ int npg() const { return (int)min(2LL, seg_end - seg_start - j0); }
-  __device__ int k0() const { return kseg + j0; }   // CTA page index of the unit's first page
-  __device__ int lp() const { return lp0 + j0; }    // sequence page of the unit's first page
-  __device__ bool last() const { return seg_start + j0 + 2 >= seg_end; }  // last unit of its segment
-};
-
-__device__ __forceinline__ int tc_chunk(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
-__device__ __forceinline__ int tc_dim(int m) {  // dim at position m of a unpacked 8-dim group
-  return 8 * (m >> 3) + ((m & 1) ? 4 : 0) + ((m & 7) >> 1);
-}
-
-__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const TcLayout L(p.B);
-  uint8_t* stages = smem + L.stages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  // Buffers of unit u: K^, V^, meta, S (tensor memory) and P, all u % 2.
-  uint64_t* full = bars;             // [4]
-  uint64_t* empty = bars + 4;        // [4]
-  uint64_t* tready = bars + 8;       // [2] unit converted -> MMA / softmax
-  uint64_t* tfree = bars + 10;       // [2] PV(u) done -> buffers free
-  uint64_t* sfull = bars + 12;       // [2] QK(u) done
-  uint64_t* sfree = bars + 14;       // [2] S of unit u read
-  uint64_t* pready = bars + 16;      // [2] P of unit u written
-  uint64_t* qready = bars + 18;      // Q' of the next segment written
-  uint64_t* ofree = bars + 19;       // O of the finished segment read
-  uint64_t* fin = bars + 20;         // final MMA completion
-  volatile int* valid = reinterpret_cast<volatile int*>(smem + L.valid);
-  volatile int* vvalid = reinterpret_cast<volatile int*>(smem + L.vvalid);
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
-  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + L.taddr);
-  float4* rowc = reinterpret_cast<float4*>(smem + L.rowc);
-  float* rowst = reinterpret_cast<float*>(smem + L.rowst);
-  float* ovrow = reinterpret_cast<float*>(smem + L.ovrow);
-  float* rowm = reinterpret_cast<float*>(smem + L.rowm);
-  float* red = reinterpret_cast<float*>(smem + L.red);
-  int* pre = reinterpret_cast<int*>(smem + L.pre);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  griddep_wait();
-  griddep_launch_dependents();
-  build_prefix(p, 0, pre, flags);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kTcConv);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tready[b], kTcConv);
-      mbar_init(&tfree[b], 1);
-      mbar_init(&sfull[b], 1);
-      mbar_init(&sfree[b], kTcSoft);
-      mbar_init(&pready[b], kTcSoft);
-    }
-    mbar_init(qready, 1);
-    mbar_init(ofree, 1);
-    mbar_init(fin, 1);
-  }
-  // V^ tiles start finite (a one-page unit multiplies the other page's rows by P = 0)
-  for (int i = threadIdx.x; i < 2 * 32768 / 16; i += kTcThreads)
-    reinterpret_cast<uint4*>(smem + L.vt)[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = threadIdx.x; i < 2 * 16384 / 16; i += kTcThreads)
-    reinterpret_cast<uint4*>(smem + L.pt)[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = threadIdx.x; i < 2 * 6144 / 16; i += kTcThreads)
-    reinterpret_cast<uint4*>(smem + L.qt)[i] = make_uint4(0u, 0u, 0u, 0u);
-  fence_barrier_init();
-  fence_proxy_async_shared();
-  if (warp == 3) tmem_alloc_256(taddr_s);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *taddr_s;
-
-  if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
-  const long long P = (long long)p.Hkv * pre[p.B];
-  const int n_eff = (int)min((long long)p.n_cta, P);
-  const bool active = (int)blockIdx.x < n_eff;
-  const long long p0 = active ? (long long)blockIdx.x * P / n_eff : 0;
-  const long long p1 = active ? (long long)(blockIdx.x + 1) * P / n_eff : 0;
-  const int R = p.R, G = p.G;
-  const int NP = (R + 15) & ~15;
-  const uint32_t idesc_qk = umma_idesc_f16(NP, false, false);
-  const uint32_t idesc_pv = umma_idesc_f16(NP, true, true);
-
-  // ------------------------------------------------------------ producer
-  if (warp == 0) {
-    if (active) produce_pages<0>(p, pre, stages, full, empty, valid, flags, kTcStages, p0, p1, lane);
-    return;
-  }
-
-  // ------------------------------------------------------------ converters
-  if (warp <= kTcConv) {
-    const int cw = warp - 1;
-    TcUnits U(p, pre, p0, p1);
-    bool first;
-    for (int u = 0; active && U.next(first); ++u) {
-      const int b = u & 1;
-      bool ok = u < 2 || __all_sync(0xffffffffu, mbar_wait_bounded(&tfree[b], (uint32_t)((u >> 1) - 1) & 1u));
-      uint8_t* kt = smem + L.kt + b * 32768;
-      uint8_t* vt = smem + L.vt + b * 32768;
-      float4* meta = reinterpret_cast<float4*>(smem + L.meta + b * 2048);
-      for (int jj = 0; ok && jj < U.npg(); ++jj) {
-        const int k = U.k0() + jj, s = k % kTcStages;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)(k / kTcStages) & 1u));
-        if (!ok) break;
-        const uint8_t* st4 = stages + (size_t)s * kStage4;
-        const int vpage = valid[s];
-        if (cw == 0 && lane == 0) vvalid[2 * b + jj] = vpage;
-        if (vpage) {
-          const int w = lane & 15;
-#pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int tt = 32 * cw + 2 * it + (lane >> 4);  // token of the page
-            const int slot = 64 * jj + tt;                  // token of the unit
-            const uint32_t kw = *reinterpret_cast<const uint32_t*>(st4 + tt * kRec4 + 4 * w);
-            const uint32_t vw = *reinterpret_cast<const uint32_t*>(st4 + kPage * kRec4 + tt * kRec4 +
-                                                                 16 * ((w >> 2) ^ ((tt >> 1) & 3)) + 4 * (w & 3));
-            uint32_t hk[4], hv[4];
-            unpack8_biased(kw, hk);
-            unpack8_v(vw, hv);
-            const int off = (w >> 3) * 16384 + tc_chunk(slot, w & 7);
-            *reinterpret_cast<uint4*>(kt + off) = make_uint4(hk[0], hk[1], hk[2], hk[3]);
-            *reinterpret_cast<uint4*>(vt + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          }
-          const int tt = 32 * cw + lane;
-          const uint32_t* mw = reinterpret_cast<const uint32_t*>(st4 + 2 * kPage * kRec4);
-          const uint32_t mk = mw[tt], mv = mw[kPage + tt];
-          const float sv = h2f_lo(mv);
-          meta[64 * jj + tt] = make_float4(h2f_lo(mk) * p.score_scale, h2f_hi(mk), sv, fmaf(7.5f, sv, h2f_hi(mv)));
-        }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-      }
-      if (!ok) {
-        if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-        flags[0] = 1;
-        break;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tready[b]);
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ MMA warp
-  if (warp == 3) {
-    if (lane == 0 && active) {
-      // Polls the readiness of the next QK (tiles converted, its S buffer read, Q' of a new
-      // segment written) and of the oldest PV (P written, O of the previous segment read) and
-      // issues whichever is ready, so neither waits behind the other.
-      TcUnits Uq(p, pre, p0, p1), Up(p, pre, p0, p1);
-      bool fq = false, fp = false;
-      bool qmore = Uq.next(fq), pmore = Up.next(fp);
-      int vq = 0, vp = 0;  // next unit to get its QK / its PV
-      bool ok = true;
-      uint64_t t_idle = 0;
-      uint32_t idle = 0;
-      while (pmore) {
-        bool progressed = false;
-        if (qmore) {
-          const int b = vq & 1;
-          if (mbar_test(&tready[b], (uint32_t)(vq >> 1) & 1u) &&
-              (vq < 2 || mbar_test(&sfree[b], (uint32_t)((vq >> 1) - 1) & 1u)) &&
-              (!fq || mbar_test(qready, (uint32_t)Uq.sidx & 1u))) {
-            tc_fence_after();
-            const uint32_t kt = smem_addr(smem + L.kt + b * 32768), qt = smem_addr(smem + L.qt);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_f16(tmem + 64 * b, umma_sdesc(kt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                       umma_sdesc(qt + (kk >> 2) * 6144 + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
-            umma_commit(&sfull[b]);
-            ++vq;
-            qmore = Uq.next(fq);
-            progressed = true;
-          }
-        }
-        if (vp < vq) {
-          const int b = vp & 1;
-          if (mbar_test(&pready[b], (uint32_t)(vp >> 1) & 1u) &&
-              (!fp || Up.sidx == 0 || mbar_test(ofree, (uint32_t)(Up.sidx - 1) & 1u))) {
-            tc_fence_after();
-            const uint32_t vt = smem_addr(smem + L.vt + b * 32768), pt = smem_addr(smem + L.pt + b * 16384);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_f16(tmem + 128, umma_sdesc(vt + kk * 2048, 16384, 1024), umma_sdesc(pt + kk * 2048, 16384, 1024),
-                       idesc_pv, (fp && kk == 0) ? 0u : 1u);
-            umma_commit(&tfree[b]);
-            ++vp;
-            pmore = Up.next(fp);
-            progressed = true;
-          }
-        }
-        if (progressed) {  // the clock is read only every 1024 idle polls (it is slow to read)
-          idle = 0;
-          t_idle = 0;
-        } else if ((++idle & 1023u) == 0) {
-          if (t_idle == 0) {
-            t_idle = globaltimer();
-          } else if (globaltimer() - t_idle > kWaitLimitNs) {
-            ok = false;
-            break;
-          }
-        }
-      }
-      if (!ok) {
-        set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-        flags[0] = 1;
-      }
-      umma_commit(fin);  // every MMA issued above has completed once this arrives
-      if (!mbar_wait_bounded(fin, 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-    }
-    __syncwarp();
-    tc_fence_before();
-    named_barrier(3, 32 + kTcSoft * 32);
-    tc_fence_after();
-    tmem_dealloc_256(tmem);
-    return;
-  }
-
-  // ------------------------------------------------------------ softmax warps
-  const int sw = warp - 4, q = sw & 3, rh = sw >> 2;
-  const int tok = 32 * q + lane;                  // token of the unit = tensor-memory lane
-  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-  const int nsoft = kTcSoft * 32;
-  const int tid = threadIdx.x - 4 * 32;           // 0..255
-  float l[kTcHalf], ov[kTcHalf];
-#pragma unroll
-  for (int j = 0; j < kTcHalf; ++j) l[j] = ov[j] = 0.0f;
-
-  // Q' tile and per-row constants of the segment of sequence bq, KV head hq
-  auto load_segment = [&](int bq, int hq) {
-    for (int e = tid; e < kTcMaxRows * 16; e += nsoft) {  // 16 threads per row, one 8-dim chunk each
-      const int r = e >> 4, w = e & 15;
-      float qv[8];
-      if (r < R) {
-        const float* qrow = p.q_rot + (((size_t)bq * p.S + r / G) * p.Hq + hq * G + r % G) * kD + 8 * w;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) qv[m] = qrow[tc_dim(m) - 8 * (m >> 3)];
-      } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) qv[m] = 0.0f;
-      }
-      uint32_t hq4[4];
-      float part = 0.0f, bsum = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float hs = (i & 1) ? 0.0625f : 1.0f;  // positions 2, 3, 6, 7 meet high nibbles
-        hq4[i] = pack_f16x2(qv[2 * i] * hs, qv[2 * i + 1] * hs);
-        bsum += h2f_lo(hq4[i]) + h2f_hi(hq4[i]);
-        part += qv[2 * i] + qv[2 * i + 1];
-      }
-      *reinterpret_cast<uint4*>(smem + L.qt + (w >> 3) * 6144 + tc_chunk(r, w & 7)) =
-          make_uint4(hq4[0], hq4[1], hq4[2], hq4[3]);
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) {
-        part += __shfl_xor_sync(0xffffffffu, part, o);
-        bsum += __shfl_xor_sync(0xffffffffu, bsum, o);
-      }
-      if (w == 0) {
-        rowc[r] = make_float4(-1024.0f * bsum, part * p.score_scale, 0.0f, -INFINITY);
-        rowst[r] = -INFINITY;
-      }
-    }
-    fence_proxy_async_shared();
-  };
-
-  TcUnits U(p, pre, p0, p1);
-  bool first = false;
-  bool more = active && U.next(first);
-  bool err = false;
-  if (more) load_segment(U.b, U.h);
-  err = named_barrier_or(2, nsoft, false);
-  if (more && tid == 0) mbar_arrive(qready);
-  int ctxb = 0;
-  bool pend = false;  // a failed wait of the previous step, reported at the next barrier
-  for (int v = 0; more && !err; ++v) {
-    const int b = v & 1;
-    const uint32_t rb = (uint32_t)(v >> 1) & 1u;
-    if (first) {
-      bool bad = false;
-      ctxb = eff_ctx(p, U.b, bad, 0);
-    }
-    bool ok = mbar_wait_bounded(&tready[b], rb) && mbar_wait_bounded(&sfull[b], rb);
-    float d[kTcHalf];
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kTcHalf / 8; ++c) {
-        float t8[8];
-        tmem_ld8(tmem + lane_base + 64 * b + kTcHalf * rh + 8 * c, t8);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d[8 * c + i] = t8[i];
-      }
-      tmem_wait_ld();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sfree[b]);
-
-    // ---- scores of this token for rows kTcHalf * rh + j (causal limits only on a unit that
-    // reaches past the context)
-    const int npg = U.npg(), jj = tok >> 6;
-    const bool tvalid = ok && jj < npg && vvalid[2 * b + jj] != 0;
-    const int pos = (U.lp() + jj) * kPage + (tok & 63);
-    const bool unit_mask = (U.lp() + npg) * kPage - 1 > ctxb;
-    const float4 mt = tvalid ? reinterpret_cast<const float4*>(smem + L.meta + b * 2048)[tok]
-                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    const bool big = mt.z >= 255.0f;
-    bool need = false;
-#pragma unroll
-    for (int j = 0; j < kTcHalf; ++j) {
-      const int r = kTcHalf * rh + j;
-      float sc = -INFINITY;
-      if (r < R && tvalid && (!unit_mask || pos <= ctxb + r / G)) {
-        const float4 c = rowc[r];
-        sc = fmaf(d[j] + c.x, mt.x, fmaf(mt.y, c.y, c.z));
-        need |= sc > (big ? fminf(c.w, 0.0f) : c.w);
-      }
-      d[j] = sc;
-    }
-    if (named_barrier_or(2, nsoft, need || !ok || pend)) {
-      err = named_barrier_or(2, nsoft, !ok || pend);
-      if (err) break;
-      // ---- rare: move the base of the rows that need it (per-row maximum over the 128 tokens)
-#pragma unroll
-      for (int j = 0; j < kTcHalf; ++j) {
-        float mx = d[j];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) rowm[sw * kTcHalf + j] = mx;
-      }
-      named_barrier(2, nsoft);
-      bool resc = false;
-      float alpha[kTcHalf];
-#pragma unroll
-      for (int j = 0; j < kTcHalf; ++j) {
-        const int r = kTcHalf * rh + j;
-        alpha[j] = 1.0f;
-        if (r >= R) continue;
-        float mt4 = rowm[(4 * rh) * kTcHalf + j];
-        for (int qq = 1; qq < 4; ++qq) mt4 = fmaxf(mt4, rowm[(4 * rh + qq) * kTcHalf + j]);
-        const float4 c = rowc[r];
-        const float mold = rowst[r], muse = -c.z;
-        const float mnew = fmaxf(mold, muse + mt4);
-        if (mnew != mold) {
-          const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
-          alpha[j] = fast_exp2(mold - mu2);
-          d[j] += muse - mu2;
-          l[j] *= alpha[j];
-          ov[j] *= alpha[j];
-          resc = true;
-        }
-      }
-      // O rows of this warp's tensor-memory lanes, columns of its row half (not on a
-      // segment's first unit: O starts from zero there)
-      const bool any_resc = named_barrier_or(2, nsoft, resc);
-      if (any_resc && !first) {
-        const bool okp = mbar_wait_bounded(&tfree[b ^ 1], (uint32_t)((v - 1) >> 1) & 1u);
-        if (okp) {
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < kTcHalf / 8; ++c) {
-            float t8[8];
-            tmem_ld8(tmem + lane_base + 128 + kTcHalf * rh + 8 * c, t8);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t8[i] *= alpha[8 * c + i];
-            tmem_st8(tmem + lane_base + 128 + kTcHalf * rh + 8 * c, t8);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        err = named_barrier_or(2, nsoft, !okp);
-        if (err) break;
-      }
-      if (q == 0 && lane < kTcHalf) {  // one writer per row publishes the new base
-        const int r = kTcHalf * rh + lane;
-        if (r < R) {
-          float mt4 = rowm[(4 * rh) * kTcHalf + lane];
-          for (int qq = 1; qq < 4; ++qq) mt4 = fmaxf(mt4, rowm[(4 * rh + qq) * kTcHalf + lane]);
-          const float4 c = rowc[r];
-          const float mold = rowst[r];
-          const float mnew = fmaxf(mold, -c.z + mt4);
-          if (mnew != mold) {
-            rowst[r] = mnew;
-            rowc[r] = make_float4(c.x, c.y, mnew == -INFINITY ? 0.0f : -mnew, mnew == -INFINITY ? -INFINITY : 8.0f);
-          }
-        }
-      }
-      named_barrier(2, nsoft);
-    }
-
-    // ---- P and P s_V (f16, token-major) for the PV product
-    uint32_t pk[kTcHalf / 2];
-#pragma unroll
-    for (int j = 0; j < kTcHalf; j += 2) {
-      const float p0v = fast_exp2(d[j]), p1v = fast_exp2(d[j + 1]);
-      l[j] += p0v;
-      l[j + 1] += p1v;
-      ov[j] = fmaf(p0v, mt.w, ov[j]);
-      ov[j + 1] = fmaf(p1v, mt.w, ov[j + 1]);
-      pk[j / 2] = pack_f16x2_sat(p0v * mt.z, p1v * mt.z);
-    }
-    ok = v < 2 || mbar_wait_bounded(&tfree[b], (uint32_t)((v >> 1) - 1) & 1u);
-    if (ok) {
-      uint8_t* pt = smem + L.pt + b * 16384;
-#pragma unroll
-      for (int c = 0; c < kTcHalf / 8; ++c)
-        *reinterpret_cast<uint4*>(pt + tc_chunk(tok, (kTcHalf / 8) * rh + c)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_shared();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&pready[b]);
-    pend = !ok;
-
-    if (U.last()) {
-      // ---- segment end: token sums per row, next segment's Q', then O -> CTA partial
-      const int bs = U.b, hs = U.h, seg = bs * p.Hkv + hs;
-#pragma unroll
-      for (int j = 0; j < kTcHalf; ++j) {
-        float lt = l[j], ot = ov[j];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-          lt += __shfl_xor_sync(0xffffffffu, lt, o);
-          ot += __shfl_xor_sync(0xffffffffu, ot, o);
-        }
-        if (lane == 0) {
-          red[(sw * kTcHalf + j) * 2] = lt;
-          red[(sw * kTcHalf + j) * 2 + 1] = ot;
-        }
-        l[j] = ov[j] = 0.0f;
-      }
-      err = named_barrier_or(2, nsoft, pend);
-      if (err) break;
-      pend = false;
-      if (q == 0 && lane < kTcHalf && kTcHalf * rh + lane < R) {
-        const int r = kTcHalf * rh + lane;
-        float lt = 0.0f, ot = 0.0f;
-        for (int qq = 0; qq < 4; ++qq) {
-          lt += red[((4 * rh + qq) * kTcHalf + lane) * 2];
-          ot += red[((4 * rh + qq) * kTcHalf + lane) * 2 + 1];
-        }
-        float* dst = p.partials + ((size_t)(blockIdx.x + seg) * R + r) * kPartialStride;
-        dst[0] = rowst[r];
-        dst[1] = lt;
-        ovrow[r] = ot;
-      }
-      named_barrier(2, nsoft);
-      bool f2 = false;
-      more = U.next(f2);
-      if (more) load_segment(U.b, U.h);
-      named_barrier(2, nsoft);
-      if (more && tid == 0) mbar_arrive(qready);
-      // O of the finished segment (lane = dim position, columns = rows of this half)
-      ok = mbar_wait_bounded(&tfree[b], rb);
-      if (ok) {
-        tc_fence_after();
-        float o[kTcHalf];
-#pragma unroll
-        for (int c = 0; c < kTcHalf / 8; ++c) {
-          float t8[8];
-          tmem_ld8(tmem + lane_base + 128 + kTcHalf * rh + 8 * c, t8);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[8 * c + i] = t8[i];
-        }
-        tmem_wait_ld();
-        const int m = tok, dim = tc_dim(m);
-        const float us = v_unscale(dim & 3);
-#pragma unroll
-        for (int j = 0; j < kTcHalf; ++j) {
-          const int r = kTcHalf * rh + j;
-          if (r < R)
-            p.partials[((size_t)(blockIdx.x + seg) * R + r) * kPartialStride + 2 + dim] = fmaf(o[j], us, ovrow[r]);
-        }
-      }
-      tc_fence_before();
-      err = named_barrier_or(2, nsoft, !ok);
-      if (!err && more && tid == 0) mbar_arrive(ofree);
-      first = f2;
-    } else {
-      more = U.next(first);
-    }
-  }
-  if (err && tid == 0) {
-    set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
-    flags[0] = 1;
-  }
-  tc_fence_before();
-  named_barrier(3, 32 + kTcSoft * 32);
-}
-
-// One block per (segment, query row): merges the segment's CTA partials and normalises.
 template <int FMT>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
@@ -1838,10 +870,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
 
 struct DevCache {
   int sm = 0;
-  bool vattr = false;  // many-row kernel: shared-memory attribute set, occupancy cache
-  bool tattr = false;  // tcgen05 many-row kernel: shared-memory attribute set
-  size_t vocc_smem = 0;
-  int vocc_threads = 0, vocc = 0;
   bool attr[2][4] = {{false}};
   size_t occ_smem[2][4] = {{0}};  // occupancy cache: last (smem, threads) queried per instantiation
   int occ_threads[2][4] = {{0}};
@@ -1903,110 +931,6 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
 }
 
-// int4 with S x G > 8 rows: the shared-tile kernel (T = row tiles), then the same combine.
-cudaError_t launch_verify(AttnParams& p, int T, long long p_max, cudaStream_t stream) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  p.ntg = T;
-  p.nkg = 1;
-  p.nstages = kVStages;
-  p.rows_pad = 8 * T;
-  const size_t smem = VerifyLayout(p.B).total;
-  const int threads = (1 + kConvWarps + T) * 32;
-  cudaError_t e = cudaSuccess;
-  int occ = 1, sm = 1;
-  {
-    std::lock_guard<std::mutex> lock(g_dev_mu);
-    DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
-    if (dc.sm == 0) {
-      int n = 0;
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      dc.sm = n > 0 ? n : 1;
-    }
-    if (!dc.vattr) {
-      e = cudaFuncSetAttribute(attn_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-      if (e != cudaSuccess) return e;
-      dc.vattr = true;
-    }
-    if (dc.vocc_smem != smem || dc.vocc_threads != threads) {
-      int o = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, attn_verify_kernel, threads, smem);
-      if (e != cudaSuccess) return e;
-      dc.vocc = std::max(o, 1);
-      dc.vocc_smem = smem;
-      dc.vocc_threads = threads;
-    }
-    occ = dc.vocc;
-    sm = dc.sm;
-  }
-  long long grid = std::min<long long>((long long)sm * occ, kMaxCtas);
-  grid = std::max<long long>(1, std::min(grid, p_max));
-  p.n_cta = (int)grid;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3((unsigned)threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_verify_kernel, p);
-  if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
-}
-
-// int4 with many query rows through the tcgen05 kernel, then the same combine.
-cudaError_t launch_tc(AttnParams& p, long long p_max, cudaStream_t stream) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const size_t smem = TcLayout(p.B).total + 1024;  // + alignment of the tile atoms
-  cudaError_t e = cudaSuccess;
-  int sm = 1;
-  {
-    std::lock_guard<std::mutex> lock(g_dev_mu);
-    DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
-    if (dc.sm == 0) {
-      int n = 0;
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      dc.sm = n > 0 ? n : 1;
-    }
-    if (!dc.tattr) {
-      e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      if (e != cudaSuccess) return e;
-      dc.tattr = true;
-    }
-    sm = dc.sm;
-  }
-  long long grid = std::min<long long>((long long)sm, kMaxCtas);  // one CTA per SM
-  grid = std::max<long long>(1, std::min(grid, p_max));
-  p.n_cta = (int)grid;
-  p.ntg = 1;
-  p.nkg = 1;
-  p.nstages = kTcStages;
-  p.rows_pad = kTcMaxRows;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3((unsigned)kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p);
-  if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
-}
-
 }  // namespace
 
 std::atomic<unsigned long long> g_stage_wait_ns{kWaitLimitNs};
@@ -2053,11 +977,6 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p_max = (long long)p.Hkv * p.B * (p.cap / kPage);
   }
   const int ntiles = (p.R + 7) / 8;
-  if (job.fmt == 0 && ntiles >= KVQ_VERIFY_MIN_TILES) {
-    const char* sel = getenv("KVQ_MANY_ROWS_KERNEL");
-    if (sel && strcmp(sel, "tcgen05") == 0) return launch_tc(p, p_max, stream);
-    if (sel && strcmp(sel, "tile") == 0) return launch_verify(p, ntiles, p_max, stream);
-  }
   int NT;
   if (ntiles <= 3) {
     NT = ntiles;

@@ -159,47 +159,18 @@ __device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// Eight 4-bit codes n0..n7 (n_k in bits 4k..4k+3) -> four f16x2 holding the centred
-// values (n-8): h[0] = (n0,n4), h[1] = (n1,n5), h[2] = (n2,n6), h[3] = (n3,n7), low half
-// first. The exponent trick 0x6400|n = 1024+n is exact; the low nibbles then take an exact
-// f16 subtract of 1032, the high nibbles (read in place as 1024+16n) an exact f16 fma by
-// 1/16 and -72. Centring keeps the tensor-core sums free of a large common term.
-__device__ __forceinline__ void unpack8_centred(uint32_t x, uint32_t (&h)[4]) {
-  constexpr uint32_t kMagic = 0x64006400u;      // (1024, 1024)
-  constexpr uint32_t kBias = 0x64086408u;       // (1032, 1032)
-  constexpr uint32_t kSixteenth = 0x2C002C00u;  // (1/16, 1/16)
-  constexpr uint32_t kNeg72 = 0xD480D480u;      // (-72, -72)
+// Eight 4-bit codes n0..n7 (n_k in bits 4k..4k+3, one 32-bit word of a K record) -> four f16x2
+// of exact f16 subnormals: h[0] = (n0, n4) 2^-24, h[1] = (n1, n5) 2^-20, h[2] = (n2, n6) 2^-24,
+// h[3] = (n3, n7) 2^-20 (a nibble masked into an f16 with a zero exponent is its value times
+// 2^-24; the high nibbles keep their place and so carry 16 n). Used for K against query fragments
+// whose high-nibble slots are pre-divided by 16, so every product is q c 2^-24 exactly and the
+// scores take one factor 2^24 with the per-token scale; no bias enters the fp32 sums.
+__device__ __forceinline__ void unpack8_sub(uint32_t x, uint32_t (&h)[4]) {
   const uint32_t x8 = x >> 8;
-  h[0] = hsub2_u(lop3<0xEA>(x, 0x000F000Fu, kMagic), kBias);
-  h[1] = hfma2_u(lop3<0xEA>(x, 0x00F000F0u, kMagic), kSixteenth, kNeg72);
-  h[2] = hsub2_u(lop3<0xEA>(x8, 0x000F000Fu, kMagic), kBias);
-  h[3] = hfma2_u(lop3<0xEA>(x8, 0x00F000F0u, kMagic), kSixteenth, kNeg72);
-}
-
-// Eight 4-bit codes -> four f16x2 without the bias subtraction (one lop3 each):
-// h[0] = (1024+n0, 1024+n4), h[1] = (1024+16 n1, 1024+16 n5), h[2] = (1024+n2, 1024+n6),
-// h[3] = (1024+16 n3, 1024+16 n7). Used for K against query fragments whose high-nibble slots
-// are pre-divided by 16 and an accumulator started at -1024 * (sum of the query fragment), so
-// the 1024 bias cancels inside the fp32 accumulation.
-__device__ __forceinline__ void unpack8_biased(uint32_t x, uint32_t (&h)[4]) {
-  constexpr uint32_t kMagic = 0x64006400u;
-  const uint32_t x8 = x >> 8;
-  h[0] = lop3<0xEA>(x, 0x000F000Fu, kMagic);
-  h[1] = lop3<0xEA>(x, 0x00F000F0u, kMagic);
-  h[2] = lop3<0xEA>(x8, 0x000F000Fu, kMagic);
-  h[3] = lop3<0xEA>(x8, 0x00F000F0u, kMagic);
+  h[0] = x & 0x000F000Fu;
+  h[1] = x & 0x00F000F0u;
+  h[2] = x8 & 0x000F000Fu;
+  h[3] = x8 & 0x00F000F0u;
 }
 
 // V code records: each 16-bit element holds the codes c0..c3 of dims 4j..4j+3 of one token in
