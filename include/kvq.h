@@ -75,14 +75,16 @@ typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
  *     bytes 4096..8191  V codes [64 tokens][64 bytes]
  *     bytes 8192..8447  K meta  [64 tokens] uint32
  *     bytes 8448..8703  V meta  [64 tokens] uint32
- *   A K record: byte b holds code 2b in its low nibble and code 2b+1 in its high nibble.
+ *   A K record: byte b holds code 2b in its low nibble and code 2b+1 in its high nibble; its
+ *     four 16-byte chunks are stored in XOR order: logical chunk c of token slot t at physical
+ *     chunk c ^ (((t >> 1) & 1) | ((t >> 2) & 2)).
  *   A V record: 32 little-endian 16-bit elements; element l holds dims 4l..4l+3, each code c
  *     as a sign bit (c < 8) and a 3-bit magnitude e (7 - c if the sign is set, else c - 8),
  *     so that c - 7.5 = (sign ? -1 : 1) * (e + 0.5). Field bits (e, sign) per dim:
  *     dim 4l: 1-3, 15; dim 4l+1: 4-6, 14; dim 4l+2: 11-13, 7; dim 4l+3: 8-10, 0. With these
  *     positions one lop3 on the element, on it shifted left by 1, on its bytes swapped, or on
  *     those shifted left by 7, gives an f16 subnormal of (c - 7.5) times a power of two.
- *   K records are stored as is. In V records the four 16-byte chunks of token slot t (0..63)
+ *   In V records the four 16-byte chunks of token slot t (0..63)
  *   are stored in XOR order: logical chunk c at physical chunk c ^ ((t >> 1) & 3), so a
  *   transposing shared-memory read of eight consecutive tokens touches eight bank groups.
  *   A meta word: bits 0..15 the fp16 scale, bits 16..31 the fp16 offset; value = code*scale + offset.

@@ -201,9 +201,16 @@ __device__ __forceinline__ void decode_page(const int* pre, int B, int Hkv, long
   }
   b = lo;
   np = pre[b + 1] - pre[b];
-  const long long rem = pg - (long long)Hkv * pre[b];
-  h = (int)(rem / np);
-  lp = (int)(rem - (long long)h * np);
+  // page of the sequence's head-major block: head = rem / np (< Hkv), by subtraction, which
+  // keeps this inlined helper free of a 64-bit division
+  long long rem = pg - (long long)Hkv * pre[b];
+  int hh = 0;
+  while (rem >= np) {
+    rem -= np;
+    ++hh;
+  }
+  h = hh;
+  lp = (int)rem;
 }
 
 // CTA whose page range [floor(i P / n), floor((i+1) P / n)) contains page pg (n <= P).
@@ -495,8 +502,10 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
             uint32_t A[MTU][4], Bw[MTU][4];
 #pragma unroll
             for (int u = 0; u < MTU; ++u) {
-              const uint4 wa = *reinterpret_cast<const uint4*>(Ks + (16 * (mt0 + u) + g) * kRec4 + 16 * t);
-              const uint4 wb = *reinterpret_cast<const uint4*>(Ks + (16 * (mt0 + u) + g + 8) * kRec4 + 16 * t);
+              // K record chunks sit at c ^ k_chunk_swz(slot): (g >> 1) & 1 for slot 16m + g, | 2 for + 8
+              const int cw = 16 * (t ^ ((g >> 1) & 1));
+              const uint4 wa = *reinterpret_cast<const uint4*>(Ks + (16 * (mt0 + u) + g) * kRec4 + cw);
+              const uint4 wb = *reinterpret_cast<const uint4*>(Ks + (16 * (mt0 + u) + g + 8) * kRec4 + (cw ^ 32));
               A[u][0] = wa.x;
               A[u][1] = wa.y;
               A[u][2] = wa.z;
@@ -803,6 +812,709 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
 
 }
 
+// ------------------------------------------------------------ many query rows: tcgen05 kernel
+// Verify blocks put S x G query rows (up to 48) on every KV head; both products then are small
+// dense contractions per 128 tokens, run here as tcgen05.mma with the accumulators in tensor
+// memory and the converted K and V codes there as well (A operands read from tensor memory), so
+// that shared memory carries only the page copies, the query tile Q', the probabilities P and
+// the per-token scales. Work split and partials are those of attn_kernel (stream-K over pages,
+// combine_kernel after).
+//
+// Units: up to two pages (128 tokens) of one segment. Within each 16-token group the tokens
+// take the order sigma(k) = 2 (k >> 2 & 3) + 8 (k >> 1 & 1) + (k & 1) (k = 0..15) along the
+// contraction of PV, so that the V fragments of ldmatrix.trans + unpack8_v store as
+// tcgen05.st.16x256b blocks; QK^T uses the same order for its M index (tensor-memory lane k
+// holds token sigma(k)), and so does the row order of P.
+//
+//   warps 0-3   converters: warp q owns tensor-memory lanes 32q..32q+31. Per unit: the K codes of
+//               unit tokens sigma(32q + lane) -> exact f16 subnormals (unpack8_sub) -> A_K
+//               (tcgen05.st.32x32b), their scales and offsets -> shared memory; the V codes of
+//               dims 32q + 4g + 2e + h of both pages -> ldmatrix.trans -> unpack8_v (exact
+//               centred f16 subnormals) -> A_V lanes 32q + 16e + 8h + g (tcgen05.st.16x256b).
+//   warps 4-11  softmax: warp 4 + 4 grp + q owns lanes 32q..32q+31 (the unit's tokens) and row
+//               half grp (rows grp*H .. grp*H + H - 1, H = NR / 2): its token's scores from S,
+//               the online softmax (lazy base as attn_kernel, decided per row half), P = p s_V
+//               in f16 into shared memory (MN-major, 128-byte swizzle); at a segment end the
+//               row sums, the next segment's Q' rows and the partial rows from O.
+//   warp 12     producer (produce_pages into kTcStages stages).
+//   warp 13     tensor-memory allocation and the QK issue: S[u&1] = A_K Q'^T (M = 128 tokens,
+//               N = NR rounded up to 16, K = 128 dims, Q' K-major).
+//   warp 14     the PV issue: O += A_V P (M = 128 dims, N, K = tokens, P MN-major). One issuing
+//               thread for both products would be the slowest part of a unit: it shares its
+//               scheduler with converter and softmax warps, and a unit takes 16 MMAs.
+//   warp 15     idle (completes the warpgroup of 12-14 for the register split).
+// Conversion of unit u + 1 runs on the converters while the softmax warps work on unit u.
+// Tensor memory: A_K[2] cols 0..127, A_V[3] 128..319, S[2] 320..447, O 448..511 (512 allocated).
+constexpr int kTcStages = 8;
+// Calls with more query rows per KV head than this take the tcgen05 kernel; up to 16 rows the
+// split kernel's mma.sync tiles finish first (measured: 16 rows 179 us there, 222 us here, on
+// 64 x 16,384 tokens; 20 rows 249 us there, 235 us here).
+constexpr int kTcMinRows = 16;
+constexpr int kTcWarps = 16;  // warp 15 only completes the last warpgroup (setmaxnreg is per warpgroup)
+// registers per thread of the converters (warps 0-3), the softmax warps (4-11) and the producer /
+// issuer warpgroup (12-15), set by setmaxnreg from the launch's 128
+constexpr int kTcRegConv = 104, kTcRegSoftmax = 168, kTcRegAux = 64;
+static_assert(128 * kTcRegConv + 256 * kTcRegSoftmax + 128 * kTcRegAux <= kTcWarps * 32 * 128,
+              "register shares above the launch's allocation");
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcMaxRows = 48;
+constexpr uint32_t kColAK = 0, kColAV = 128, kColS = 320, kColO = 448;
+constexpr int kTcHalf = kTcMaxRows * 128;  // bytes of one 64-dim half of Q'
+constexpr int kTcBars = 32;                // mbarriers of the kernel (see its list)
+
+struct TcLayout {  // offsets from the 1024-byte aligned start of dynamic shared memory
+  size_t stages, qt, pt, meta, bars, valid, flags, taddr, rowc, rowst, ovrow, red, rowm, rcx, rcy, ralpha, rdelta, pre,
+      total;
+  __host__ __device__ explicit TcLayout(int B) {
+    stages = 0;
+    qt = kTcStages * (size_t)kStage4;  // 69632 = 68 * 1024
+    pt = qt + 2 * kTcHalf;             // + 12288
+    meta = pt + 3 * 128 * 128;         // P[3]: 128 token rows of 128 bytes
+    bars = meta + 3 * 128 * 16;        // per-token (k scale, k offset, v scale, v term) of 3 units
+    valid = bars + 8 * kTcBars;
+    flags = valid + 4 * kTcStages;
+    taddr = flags + 16;
+    rowc = align_up(taddr + 16, 16);
+    rowst = rowc + 16 * kTcMaxRows;
+    ovrow = rowst + 4 * kTcMaxRows;
+    red = ovrow + 4 * kTcMaxRows;
+    rowm = red + 4 * 2 * 4 * kTcMaxRows;
+    rcx = rowm + 4 * 4 * kTcMaxRows;
+    rcy = rcx + 4 * kTcMaxRows;
+    ralpha = rcy + 4 * kTcMaxRows;
+    rdelta = ralpha + 4 * kTcMaxRows;
+    pre = rdelta + 4 * kTcMaxRows;
+    total = align_up(pre + 4 * (size_t)(B + 1), 16);
+  }
+};
+
+// The CTA's pages [p0, p1) as units of up to two pages of one segment, in order.
+struct TcUnits {
+  const AttnParams& p;
+  const int* pre;
+  long long p0, p1, k, seg_start, seg_end, ustart;
+  int b, h, lp0, np, segi, npg;
+  bool first, last;
+  __device__ TcUnits(const AttnParams& p_, const int* pre_, long long a, long long e)
+      : p(p_), pre(pre_), p0(a), p1(e), k(a), seg_start(0), seg_end(-1), ustart(0), b(0), h(0), lp0(0), np(1),
+        segi(-1), npg(0), first(false), last(false) {}
+  __device__ bool next() {
+    if (k >= p1) return false;
+    if (k >= seg_end) {
+      decode_page(pre, p.B, p.Hkv, k, b, h, lp0, np);
+      seg_start = k;
+      seg_end = min(p1, k + (np - lp0));
+      ++segi;
+      first = true;
+    } else {
+      first = false;
+    }
+    ustart = k;
+    npg = (int)min(2LL, seg_end - k);
+    k += npg;
+    last = k >= seg_end;
+    return true;
+  }
+  __device__ int lp() const { return lp0 + (int)(ustart - seg_start); }  // local page of the unit's first page
+  __device__ int kidx() const { return (int)(ustart - p0); }              // CTA page index of that page
+};
+
+// Token of unit lane k (0..127): 16 (k >> 4) + sigma(k & 15).
+__device__ __forceinline__ int tc_token(int k) {
+  return (k & ~15) + 2 * ((k >> 2) & 3) + 8 * ((k >> 1) & 1) + (k & 1);
+}
+
+// Byte offset of K-index kd (0..127) of row r in Q' (K-major, two 64-index halves of rows of 128
+// bytes, 8-row groups, 16-byte chunk c of row r at c ^ (r & 7)).
+__device__ __forceinline__ int tc_q_offset(int r, int kd) {
+  return (kd >> 6) * kTcHalf + r * 128 + 16 * (((kd & 63) >> 3) ^ (r & 7)) + 2 * (kd & 7);
+}
+
+// NR: softmax rows of the CTA (R rounded up to 8, at most 48); the MMAs take N = NR rounded up
+// to 16 (P columns beyond NR are never written: their D columns are not read).
+template <int NR>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams p) {
+  constexpr int H = NR / 2;  // rows of one softmax group (a multiple of 4)
+  constexpr int NM = (NR + 15) & ~15;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const TcLayout L(p.B);
+  uint8_t* stages = smem + L.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* full = bars;            // [8] page copied
+  uint64_t* empty = bars + 8;       // [8] page read (the 4 converters)
+  uint64_t* cready = bars + 16;     // [3] A_K[u & 1], A_V[u % 3] and the scales of unit u written
+  uint64_t* sfull = bars + 19;      // [2] QK(u) done
+  uint64_t* pready = bars + 21;     // [3] P[u % 3] of unit u written (so S[u & 1] has been read)
+  uint64_t* vfree = bars + 24;      // [3] PV(u) done: A_V, P and scales of u % 3 free
+  uint64_t* qready = bars + 27;     // Q' of a segment written (both groups)
+  uint64_t* ofull = bars + 28;      // a segment's last PV done
+  uint64_t* ofree = bars + 29;      // O of a segment read (both groups)
+  uint64_t* fin = bars + 30;        // [2] final MMA completion of the QK / PV issuer
+  static_assert(31 < kTcBars, "mbarrier list larger than its shared-memory region");
+  volatile int* valid = reinterpret_cast<volatile int*>(smem + L.valid);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L.flags);
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + L.taddr);
+  float4* tmeta = reinterpret_cast<float4*>(smem + L.meta);  // [3][128 unit lanes]
+  float4* rowc = reinterpret_cast<float4*>(smem + L.rowc);    // (qs * scale, -muse, threshold, last position)
+  float* rowst = reinterpret_cast<float*>(smem + L.rowst);    // running maximum m (log2 units)
+  float* ovrow = reinterpret_cast<float*>(smem + L.ovrow);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* rowm = reinterpret_cast<float*>(smem + L.rowm);
+  float* rcx = reinterpret_cast<float*>(smem + L.rcx);        // rowc x and y by row, for 16-byte loads
+  float* rcy = reinterpret_cast<float*>(smem + L.rcy);
+  float* ralpha = reinterpret_cast<float*>(smem + L.ralpha);  // a base move: factor on a row's sums and O
+  float* rdelta = reinterpret_cast<float*>(smem + L.rdelta);  // and shift of its scores
+  int* pre = reinterpret_cast<int*>(smem + L.pre);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t kFinBar = 1;
+  constexpr int kGrp = 128, kFinThreads = 14 * 32;
+
+  griddep_wait();
+  griddep_launch_dependents();
+  build_prefix(p, 0, pre, flags);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    for (int b = 0; b < 2; ++b) mbar_init(&sfull[b], 1);
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(&cready[b], 4);
+      mbar_init(&pready[b], 8);
+      mbar_init(&vfree[b], 1);
+    }
+    mbar_init(qready, 2);
+    mbar_init(ofull, 1);
+    mbar_init(ofree, 2);
+    mbar_init(&fin[0], 1);
+    mbar_init(&fin[1], 1);
+  }
+  // Q' rows beyond R stay zero
+  for (int i = threadIdx.x; i < 2 * kTcHalf / 16; i += kTcThreads)
+    reinterpret_cast<uint4*>(smem + L.qt)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_barrier_init();
+  fence_proxy_async_shared();
+  if (warp == 13) tmem_alloc_512(taddr_s);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *taddr_s;
+
+  if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
+  const long long P = (long long)p.Hkv * pre[p.B];
+  const int n_eff = (int)min((long long)p.n_cta, P);
+  const bool active = (int)blockIdx.x < n_eff;
+  const long long p0 = active ? (long long)blockIdx.x * P / n_eff : 0;
+  const long long p1 = active ? (long long)(blockIdx.x + 1) * P / n_eff : 0;
+  const int R = p.R, G = p.G;
+
+  // Registers per thread by warpgroup: the softmax warps hold a score and two running sums per
+  // row; the producer and issuer threads need few. The shares add up to at most the launch's
+  // 128 per thread (setmaxnreg.inc waits for registers released by .dec).
+  // Each role's code is entered only after its warpgroup's setmaxnreg and ends in a return.
+  if (warp >= 12) {
+  reg_dealloc<kTcRegAux>();
+  if (warp == 15) return;
+
+  // ------------------------------------------------------------ producer
+  if (warp == 12) {
+    if (active) produce_pages<0>(p, pre, stages, full, empty, valid, flags, kTcStages, p0, p1, lane);
+    return;
+  }
+
+  // ------------------------------------------------------------ MMA issue
+  // Two issuing threads, each on its own scheduler: warp 13 issues QK, warp 14 PV. A commit
+  // tracks only its own thread's MMAs; the two write disjoint tensor memory (S, O) and read
+  // operands whose reuse each side orders on its own barriers. PV(u) reads A_V[u % 3]: it was
+  // written before cready(u), which the softmax warps waited for before they arrived on pready(u).
+  {  // warps 13 and 14
+    if (lane == 0 && active) {
+      TcUnits Uu(p, pre, p0, p1);
+      bool ok = true;
+      int b3 = 0;       // unit % 3
+      uint32_t ph3 = 0;  // (unit / 3) & 1
+      if (warp == 13) {
+        const uint32_t idesc = umma_idesc_f16(NM, false, false);
+        const uint64_t dq = umma_sdesc(smem_addr(smem + L.qt), 16, 1024);
+        int pb3 = 0;       // (unit - 2) % 3, from unit 2 on
+        uint32_t pph3 = 0;  // ((unit - 2) / 3) & 1
+        for (int v = 0; Uu.next(); ++v) {
+          const int b = v & 1;
+          ok = mbar_wait_bounded(&cready[b3], ph3);
+          // S[b] was read before P of unit v - 2 was written
+          ok = ok && (v < 2 || mbar_wait_bounded(&pready[pb3], pph3));
+          ok = ok && (!Uu.first || mbar_wait_bounded(qready, (uint32_t)Uu.segi & 1u));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kColS + 64 * b, a0 = tmem + kColAK + 64 * b;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // k-steps of 16 dims: 32 bytes within a 64-dim half
+            umma_f16_ts(d, a0 + 8 * kk, dq + (uint64_t)(((kk >> 2) * kTcHalf + (kk & 3) * 32) >> 4), idesc, kk > 0);
+          umma_commit(&sfull[b]);
+          if (++b3 == 3) { b3 = 0; ph3 ^= 1u; }
+          if (v >= 2 && ++pb3 == 3) { pb3 = 0; pph3 ^= 1u; }
+        }
+      } else {
+        const uint32_t idesc = umma_idesc_f16(NM, false, true);
+        const uint64_t dp = umma_sdesc(smem_addr(smem + L.pt), 16384, 1024);
+        while (Uu.next()) {
+          ok = mbar_wait_bounded(&pready[b3], ph3);
+          ok = ok && (!Uu.first || Uu.segi == 0 || mbar_wait_bounded(ofree, (uint32_t)(Uu.segi - 1) & 1u));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a0 = tmem + kColAV + 64 * b3;
+          const uint64_t d0 = dp + (uint64_t)(b3 * (16384 >> 4));
+          const uint32_t acc0 = Uu.first ? 0u : 1u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // k-steps of 16 tokens: 2048 bytes of P each
+            umma_f16_ts(tmem + kColO, a0 + 8 * kk, d0 + (uint64_t)(kk * (2048 >> 4)), idesc, kk > 0 ? 1u : acc0);
+          if (Uu.npg == 2) {
+#pragma unroll
+            for (int kk = 4; kk < 8; ++kk)
+              umma_f16_ts(tmem + kColO, a0 + 8 * kk, d0 + (uint64_t)(kk * (2048 >> 4)), idesc, 1u);
+          }
+          umma_commit(&vfree[b3]);
+          if (Uu.last) umma_commit(ofull);
+          if (++b3 == 3) { b3 = 0; ph3 ^= 1u; }
+        }
+      }
+      if (!ok) {
+        set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+        flags[0] = 1;
+      }
+      uint64_t* done = warp == 13 ? fin : fin + 1;
+      umma_commit(done);  // every MMA this thread issued has completed once this arrives
+      if (!mbar_wait_bounded(done, 0)) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_barrier(kFinBar, kFinThreads);
+    tc_fence_after();
+    if (warp == 13) tmem_dealloc_512(tmem);
+    return;
+  }
+  }  // warps 12-15
+
+  // ------------------------------------------------------------ converters
+  if (warp < 4) {
+    reg_dealloc<kTcRegConv>();
+    const int q = warp;
+    const int kl = 32 * q + lane;              // unit lane of this thread's token
+    const int tok = tc_token(kl);              // token of the unit (0..127)
+    const int jj = tok >> 6, slot = tok & 63;  // its page (warp-uniform) and slot
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    TcUnits Uc(p, pre, p0, p1);
+    bool ok = true;
+    int bv = 0;           // u % 3
+    uint32_t fph = 1;     // ((u - 3) / 3) & 1 for vfree, from u = 3 on (flipped before use)
+    for (int u = 0; active && ok && Uc.next(); ++u) {
+      const int bk = u & 1;
+      if (u >= 3 && bv == 0) fph ^= 1u;
+      // A_V, P and scales of u % 3 were last used by PV(u - 3); A_K[u & 1] by QK(u - 2). Every
+      // barrier of the unit is tested at once; only an incomplete one is waited for in turn.
+      const int kp0 = Uc.kidx(), npg = Uc.npg;
+      const int s0 = kp0 % kTcStages, s1 = (kp0 + 1) % kTcStages;
+      const uint32_t f0 = (uint32_t)(kp0 / kTcStages) & 1u, f1 = (uint32_t)((kp0 + 1) / kTcStages) & 1u;
+      const uint32_t sph = (uint32_t)((u - 2) >> 1) & 1u;
+      bool ready = mbar_test(&full[s0], f0);
+      if (npg == 2) ready &= mbar_test(&full[s1], f1);
+      if (u >= 3) ready &= mbar_test(&vfree[bv], fph);
+      if (u >= 2) ready &= mbar_test(&sfull[bk], sph);
+      if (!__all_sync(0xffffffffu, ready)) {
+        bool w = u < 3 || mbar_wait_bounded(&vfree[bv], fph);
+        w = w && (u < 2 || mbar_wait_bounded(&sfull[bk], sph));
+        w = w && mbar_wait_bounded(&full[s0], f0);
+        w = w && (npg < 2 || mbar_wait_bounded(&full[s1], f1));
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+      }
+      // ---- K: this thread's token (page jj) -> A_K[u & 1], its scales -> shared memory
+      float4 mt = make_float4(0.f, 0.f, -1.f, 0.f);  // v scale -1: no token
+      if (jj < npg) {
+        const int s = jj ? s1 : s0;
+        const uint8_t* st = stages + (size_t)s * kStage4;
+        const int sw = k_chunk_swz(slot);
+        uint4 kc[4];  // all four 16-byte chunks loaded before any is converted
+#pragma unroll
+        for (int c = 0; c < 4; ++c) kc[c] = *reinterpret_cast<const uint4*>(st + slot * kRec4 + 16 * (c ^ sw));
+        const bool vld = valid[s] != 0;
+        const uint32_t mk = reinterpret_cast<const uint32_t*>(st + 2 * kPage * kRec4)[slot];
+        const uint32_t mv = reinterpret_cast<const uint32_t*>(st + 2 * kPage * kRec4)[kPage + slot];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // chunk c (words 4c..4c+3) -> columns 16c .. 16c + 15
+          const uint32_t wd[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
+          uint32_t w16[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t h4[4];
+            unpack8_sub(wd[i], h4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w16[4 * i + j] = h4[j];
+          }
+          tmem_st16u(tmem + lane_base + kColAK + 64 * bk + 16 * c, w16);
+        }
+        if (vld) {
+          const float sv = h2f_lo(mv);
+          mt = make_float4(h2f_lo(mk) * p.score_scale * 16777216.0f, h2f_hi(mk), sv, fmaf(7.5f, sv, h2f_hi(mv)));
+        }
+      }
+      tmeta[bv * 128 + kl] = mt;
+      // ---- V codes of dims 32q .. 32q + 31 of both pages: every ldmatrix before any conversion
+      uint32_t rr[2][2][4];  // [page][half of the page]
+#pragma unroll
+      for (int pg = 0; pg < 2; ++pg) {
+        if (pg < npg) {
+          const uint8_t* Vs = stages + (size_t)(pg ? s1 : s0) * kStage4 + kPage * kRec4;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t8 = 32 * hf + 8 * (lane >> 3) + (lane & 7);
+            ldsm_x4_trans(rr[pg][hf], smem_addr(Vs + t8 * kRec4 + 16 * (q ^ ((t8 >> 1) & 3))));
+          }
+        }
+      }
+      __syncwarp();
+      mbar_arrive_if(&empty[s0], lane == 0);  // both pages read (K above, V into registers)
+      if (npg == 2) mbar_arrive_if(&empty[s1], lane == 0);
+#pragma unroll
+      for (int pg = 0; pg < 2; ++pg) {
+        if (pg < npg) {
+          uint32_t ra[16], rb[16];  // dims of class 2e + h at lanes 32q + 16e + 8h + g, e = 0 / 1
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int gq = 0; gq < 2; ++gq) {
+              uint32_t h0[4], h1[4];
+              unpack8_v(rr[pg][hf][2 * gq], h0);      // tokens 16 gq + 2t, +1 of this half
+              unpack8_v(rr[pg][hf][2 * gq + 1], h1);  // tokens 16 gq + 8 + 2t, +1
+              const int j = 2 * hf + gq;              // 16-token group of the page
+              ra[4 * j] = h0[0];
+              ra[4 * j + 1] = h1[0];
+              ra[4 * j + 2] = h0[1];
+              ra[4 * j + 3] = h1[1];
+              rb[4 * j] = h0[2];
+              rb[4 * j + 1] = h1[2];
+              rb[4 * j + 2] = h0[3];
+              rb[4 * j + 3] = h1[3];
+            }
+          }
+          const uint32_t col = tmem + kColAV + 64 * bv + 32 * pg;
+          tmem_st_16x256b_x4(col + lane_base, ra);
+          tmem_st_16x256b_x4(col + ((uint32_t)(32 * q + 16) << 16), rb);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_if(&cready[bv], lane == 0);
+      if (++bv == 3) bv = 0;
+    }
+    if (!ok) {
+      if (lane == 0) set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+      flags[0] = 1;
+    }
+    tc_fence_before();
+    named_barrier(kFinBar, kFinThreads);
+    return;
+  }
+
+  // ------------------------------------------------------------ softmax warps
+  reg_alloc<kTcRegSoftmax>();
+  const int q = warp & 3, grp = (warp - 4) >> 2;  // lane quarter, row half
+  const uint32_t kGrpBar = 2 + grp;               // named barrier of the row half
+  const int kl = 32 * q + lane;                   // unit lane: row of S and of P
+  const int tok = tc_token(kl);                   // token of the unit (0..127)
+  const int jj = tok >> 6, slot = tok & 63;       // page of the unit (warp-uniform) and slot
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int gt = threadIdx.x - 128 - 128 * grp;   // 0..127 within the row half
+  const int r0 = grp * H;                         // first row of the half
+  // running sums of p and of p * (v term) of this thread's tokens; pair i holds rows 2i, 2i + 1
+  uint64_t l2[H / 2], ov2[H / 2];
+#pragma unroll
+  for (int i = 0; i < H / 2; ++i) l2[i] = ov2[i] = 0ull;  // (0.0f, 0.0f)
+
+  // Q' rows and row constants of this half for segment (bq, hq): K-index kd of a row holds dim
+  // 8w + j + 4e (kd = 8w + 2j + e, the order of unpack8_sub), divided by 16 for odd j. Row
+  // constants: (sum q~ * scale, -base (0 while the base is -inf; -inf on padding rows, whose
+  // scores then are -inf), threshold of the lazy base (+inf on padding rows), last visible
+  // position of the row's query).
+  auto load_segment = [&](int bq, int hq) {
+    bool bad = false;
+    const int cb = eff_ctx(p, bq, bad, 0);
+    for (int e = gt; e < H * 16; e += kGrp) {
+      const int r = r0 + (e >> 4), w = e & 15;
+      float part = 0.0f;
+      uint32_t hq4[4];
+      if (r < R) {
+        const float* qrow = p.q_rot + (((size_t)bq * p.S + r / G) * p.Hq + hq * G + r % G) * kD + 8 * w;
+        const float4 a = reinterpret_cast<const float4*>(qrow)[0], c4 = reinterpret_cast<const float4*>(qrow)[1];
+        const float qv[8] = {a.x, a.y, a.z, a.w, c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part += qv[i];
+        hq4[0] = pack_f16x2(qv[0], qv[4]);
+        hq4[1] = pack_f16x2(qv[1] * 0.0625f, qv[5] * 0.0625f);
+        hq4[2] = pack_f16x2(qv[2], qv[6]);
+        hq4[3] = pack_f16x2(qv[3] * 0.0625f, qv[7] * 0.0625f);
+      } else {
+        hq4[0] = hq4[1] = hq4[2] = hq4[3] = 0u;
+      }
+      *reinterpret_cast<uint4*>(smem + L.qt + tc_q_offset(r, 8 * w)) = make_uint4(hq4[0], hq4[1], hq4[2], hq4[3]);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (w == 0) {
+        const float4 c = r < R ? make_float4(part * p.score_scale, 0.0f, -INFINITY, (float)(cb + r / G))
+                               : make_float4(0.0f, -INFINITY, INFINITY, -1.0f);
+        rowc[r] = c;
+        rcx[r] = c.x;
+        rcy[r] = c.y;
+        rowst[r] = -INFINITY;
+      }
+    }
+    fence_proxy_async_shared();
+  };
+
+  TcUnits U(p, pre, p0, p1);
+  bool more = active && U.next();
+  bool err = false;
+  if (more) load_segment(U.b, U.h);
+  err = named_barrier_or(kGrpBar, kGrp, false);
+  if (more && gt == 0) mbar_arrive(qready);
+  int ctxb = 0;
+  // smallest lazy-base threshold over the half's rows (-inf until every row has a base)
+  float thr_grp = -INFINITY;
+  for (int v = 0; more && !err; ++v) {
+    const int b = v & 1, bv = v % 3;
+    if (U.first) {
+      bool bad = false;
+      ctxb = eff_ctx(p, U.b, bad, 0);
+    }
+    // waits are made warp-uniform: the tensor-memory loads after them are warp-collective
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sfull[b], (uint32_t)(v >> 1) & 1u) &&
+                                          mbar_wait_bounded(&cready[bv], (uint32_t)(v / 3) & 1u));
+    float d[H];
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < H / 4; ++c) {
+        float t4[4];
+        tmem_ld4(tmem + lane_base + kColS + 64 * b + r0 + 4 * c, t4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[4 * c + i] = t4[i];
+      }
+      tmem_wait_ld();
+    }
+    tc_fence_before();
+    const float4 mt = tmeta[bv * 128 + kl];  // (k scale * score scale * 2^24, k offset, v scale, v term)
+
+    // ---- scores of this token relative to each row's base; branch-free over the rows (padding
+    // rows carry a -inf base); the causal limits apply only on a unit that reaches past the context
+    const bool tvalid = ok && mt.z >= 0.0f;
+    const bool unit_mask = (U.lp() + U.npg) * kPage - 1 > ctxb;
+    float mx = -INFINITY;
+    if (!tvalid) {
+#pragma unroll
+      for (int i = 0; i < H; ++i) d[i] = -INFINITY;
+    } else if (!unit_mask) {
+      // d mt.x + (mt.y c.x + c.y), four rows at a time in fp32 pairs
+      const uint64_t mtx2 = f2(mt.x, mt.x), mty2 = f2(mt.y, mt.y);
+#pragma unroll
+      for (int c = 0; c < H / 4; ++c) {
+        const float4 cx = reinterpret_cast<const float4*>(rcx + r0)[c];
+        const float4 cy = reinterpret_cast<const float4*>(rcy + r0)[c];
+        const uint64_t s01 = fma_f2(f2(d[4 * c], d[4 * c + 1]), mtx2, fma_f2(mty2, f2(cx.x, cx.y), f2(cy.x, cy.y)));
+        const uint64_t s23 = fma_f2(f2(d[4 * c + 2], d[4 * c + 3]), mtx2, fma_f2(mty2, f2(cx.z, cx.w), f2(cy.z, cy.w)));
+        d[4 * c] = f2lo(s01);
+        d[4 * c + 1] = f2hi(s01);
+        d[4 * c + 2] = f2lo(s23);
+        d[4 * c + 3] = f2hi(s23);
+        mx = fmax3(mx, d[4 * c], d[4 * c + 1]);
+        mx = fmax3(mx, d[4 * c + 2], d[4 * c + 3]);
+      }
+    } else {
+      const float fpos = (float)((U.lp() + jj) * kPage + slot);
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float4 c = rowc[r0 + i];
+        const float sc = fmaf(d[i], mt.x, fmaf(mt.y, c.x, c.y));
+        d[i] = fpos <= c.w ? sc : -INFINITY;
+        mx = fmaxf(mx, d[i]);
+      }
+    }
+    const bool need = mx > (mt.z >= 255.0f ? fminf(thr_grp, 0.0f) : thr_grp);  // large V scale: any excess
+    if (__builtin_expect(named_barrier_or(kGrpBar, kGrp, need || !ok), 0)) {
+      err = named_barrier_or(kGrpBar, kGrp, !ok);
+      if (err) break;
+      // ---- rare: move the base of the rows whose maximum passed it (row maxima over the 128 tokens)
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        float m1 = d[i];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        if (lane == 0) rowm[q * kTcMaxRows + r0 + i] = m1;
+      }
+      named_barrier(kGrpBar, kGrp);
+      // one thread per row: the new base (published), the factor alpha on the row's sums and O
+      // and the shift of this unit's scores to the new base (1 and 0 where the base stays)
+      bool changed = false;
+      if (gt < H) {
+        const int r = r0 + gt;
+        float alpha = 1.0f, delta = 0.0f;
+        if (r < R) {
+          const float mt4 = fmaxf(fmaxf(rowm[r], rowm[kTcMaxRows + r]), fmaxf(rowm[2 * kTcMaxRows + r], rowm[3 * kTcMaxRows + r]));
+          const float4 c = rowc[r];
+          const float mold = rowst[r], muse = -c.y;
+          const float mnew = fmaxf(mold, muse + mt4);
+          if (mnew != mold) {
+            const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
+            alpha = fast_exp2(mold - mu2);
+            delta = muse - mu2;
+            changed = true;
+            const float nb = mnew == -INFINITY ? 0.0f : -mnew;
+            rowst[r] = mnew;
+            rowc[r] = make_float4(c.x, nb, mnew == -INFINITY ? -INFINITY : 8.0f, c.w);
+            rcy[r] = nb;
+          }
+        }
+        ralpha[r] = alpha;
+        rdelta[r] = delta;
+      }
+      if (named_barrier_or(kGrpBar, kGrp, changed)) {
+#pragma unroll
+        for (int i = 0; i < H / 2; ++i) {
+          const uint64_t a2 = f2(ralpha[r0 + 2 * i], ralpha[r0 + 2 * i + 1]);
+          l2[i] = mul_f2(l2[i], a2);
+          ov2[i] = mul_f2(ov2[i], a2);
+        }
+#pragma unroll
+        for (int i = 0; i < H; ++i) d[i] += rdelta[r0 + i];
+        // O (this thread's lane, the half's rows) -- not on a segment's first unit: O starts from
+        // zero there. PV(v - 1) must have completed.
+        if (!U.first) {
+          const bool okp = __all_sync(0xffffffffu, mbar_wait_bounded(&vfree[(v - 1) % 3], (uint32_t)((v - 1) / 3) & 1u));
+          if (okp) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < H / 4; ++c) {
+              float t4[4];
+              tmem_ld4(tmem + lane_base + kColO + r0 + 4 * c, t4);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) t4[i] *= ralpha[r0 + 4 * c + i];
+              tmem_st4(tmem + lane_base + kColO + r0 + 4 * c, t4);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          err = named_barrier_or(kGrpBar, kGrp, !okp);
+          if (err) break;
+        }
+      }
+      thr_grp = INFINITY;
+#pragma unroll
+      for (int i = 0; i < H; ++i)
+        if (r0 + i < R) thr_grp = fminf(thr_grp, rowc[r0 + i].z);
+    }
+
+    // ---- P s_V in f16 (row kl of P[v % 3], MN-major: query row r at byte 2 (r & 7) of chunk r >> 3)
+    uint32_t pk[H / 2];
+    const uint64_t mtz2 = f2(mt.z, mt.z), mtw2 = f2(mt.w, mt.w);
+#pragma unroll
+    for (int i = 0; i < H / 2; ++i) {
+      const uint64_t pp = f2(fast_exp2(d[2 * i]), fast_exp2(d[2 * i + 1]));
+      l2[i] = add_f2(l2[i], pp);
+      ov2[i] = fma_f2(pp, mtw2, ov2[i]);
+      const uint64_t ps = mul_f2(pp, mtz2);
+      pk[i] = pack_f16x2_sat(f2lo(ps), f2hi(ps));
+    }
+    // P[v % 3] was read by PV(v - 3), complete since the converters waited for it before
+    // writing this unit's codes (cready above)
+    {
+      uint8_t* prow = smem + L.pt + bv * 16384 + kl * 128;
+#pragma unroll
+      for (int m = 0; m < H / 4; ++m) {  // rows r0 + 4m .. + 3 (8 bytes)
+        const int r = r0 + 4 * m;
+        *reinterpret_cast<uint2*>(prow + 16 * ((r >> 3) ^ (kl & 7)) + 2 * (r & 7)) = make_uint2(pk[2 * m], pk[2 * m + 1]);
+      }
+      fence_proxy_async_shared();
+    }
+    __syncwarp();
+    mbar_arrive_if(&pready[bv], lane == 0);
+
+    if (__builtin_expect(U.last, 0)) {
+      // ---- segment end: token sums per row, the next segment's Q', then O -> CTA partial
+      const int seg = U.b * p.Hkv + U.h, segi = U.segi;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        float lt = (i & 1) ? f2hi(l2[i / 2]) : f2lo(l2[i / 2]);
+        float ot = (i & 1) ? f2hi(ov2[i / 2]) : f2lo(ov2[i / 2]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          lt += __shfl_xor_sync(0xffffffffu, lt, o);
+          ot += __shfl_xor_sync(0xffffffffu, ot, o);
+        }
+        if (lane == 0) {
+          red[(q * kTcMaxRows + r0 + i) * 2] = lt;
+          red[(q * kTcMaxRows + r0 + i) * 2 + 1] = ot;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < H / 2; ++i) l2[i] = ov2[i] = 0ull;
+      named_barrier(kGrpBar, kGrp);
+      if (gt < H && r0 + gt < R) {
+        const int r = r0 + gt;
+        float lt = 0.0f, ot = 0.0f;
+        for (int qq = 0; qq < 4; ++qq) {
+          lt += red[(qq * kTcMaxRows + r) * 2];
+          ot += red[(qq * kTcMaxRows + r) * 2 + 1];
+        }
+        float* dst = p.partials + ((size_t)(blockIdx.x + seg) * R + r) * kPartialStride;
+        dst[0] = rowst[r];
+        dst[1] = lt;
+        ovrow[r] = ot;
+      }
+      named_barrier(kGrpBar, kGrp);
+      TcUnits Un = U;
+      const bool nmore = Un.next();
+      if (nmore) load_segment(Un.b, Un.h);
+      named_barrier(kGrpBar, kGrp);
+      if (nmore && gt == 0) mbar_arrive(qready);
+      thr_grp = -INFINITY;
+      // O of the finished segment: lane kl holds dim 32q + 4g + 2e + h for kl = 32q + 16e + 8h + g
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)segi & 1u));
+      if (ok) {
+        tc_fence_after();
+        float o[H];
+#pragma unroll
+        for (int c = 0; c < H / 4; ++c) {
+          float t4[4];
+          tmem_ld4(tmem + lane_base + kColO + r0 + 4 * c, t4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[4 * c + i] = t4[i];
+        }
+        tmem_wait_ld();
+        const int e = (lane >> 4) & 1, hh = (lane >> 3) & 1, g = lane & 7;
+        const int dim = 32 * q + 4 * g + 2 * e + hh;
+        const float us = v_unscale(dim & 3);
+#pragma unroll
+        for (int i = 0; i < H; ++i)
+          if (r0 + i < R)
+            p.partials[((size_t)(blockIdx.x + seg) * R + r0 + i) * kPartialStride + 2 + dim] = fmaf(o[i], us, ovrow[r0 + i]);
+      }
+      tc_fence_before();
+      err = named_barrier_or(kGrpBar, kGrp, !ok);
+      if (!err && nmore && gt == 0) mbar_arrive(ofree);
+    }
+    more = U.next();
+  }
+  if (err && gt == 0) {
+    set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
+    flags[0] = 1;
+  }
+  tc_fence_before();
+  named_barrier(kFinBar, kFinThreads);
+}
+
+// One block per (segment, query row): merges the segment's CTA partials and normalises.
 template <int FMT>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
@@ -871,6 +1583,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
 struct DevCache {
   int sm = 0;
   bool attr[2][4] = {{false}};
+  bool tc_attr[4] = {false, false, false, false};  // attn_tc_kernel<24 / 32 / 40 / 48>: shared-memory attribute set
   size_t occ_smem[2][4] = {{0}};  // occupancy cache: last (smem, threads) queried per instantiation
   int occ_threads[2][4] = {{0}};
   int occ[2][4] = {{0}};
@@ -931,6 +1644,56 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
 }
 
+// int4 with more than 8 query rows per KV head: the tcgen05 kernel (NR = rows rounded up to 8),
+// one CTA per SM (it takes all 512 tensor-memory columns), then the same combine.
+template <int NR>
+cudaError_t launch_tc_t(AttnParams& p, long long p_max, cudaStream_t stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = TcLayout(p.B).total + 1024;  // + alignment to 1024 bytes
+  cudaError_t e = cudaSuccess;
+  int sm = 1;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevCache& dc = g_dev[(dev >= 0 && dev < 64) ? dev : 0];
+    if (dc.sm == 0) {
+      int n = 0;
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      dc.sm = n > 0 ? n : 1;
+    }
+    static_assert(NR >= 24 && NR <= 48 && NR % 8 == 0, "attn_tc_kernel row counts: 24, 32, 40, 48");
+    if (!dc.tc_attr[NR / 8 - 3]) {
+      e = cudaFuncSetAttribute(attn_tc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) return e;
+      dc.tc_attr[NR / 8 - 3] = true;
+    }
+    sm = dc.sm;
+  }
+  long long grid = std::min<long long>((long long)sm, kMaxCtas);
+  grid = std::max<long long>(1, std::min(grid, p_max));
+  p.n_cta = (int)grid;
+  p.ntg = 1;
+  p.nkg = 1;
+  p.nstages = kTcStages;
+  p.rows_pad = NR;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<NR>, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
+}
+
 }  // namespace
 
 std::atomic<unsigned long long> g_stage_wait_ns{kWaitLimitNs};
@@ -977,6 +1740,14 @@ cudaError_t launch_attention(const AttnJob& job, cudaStream_t stream) {
     p_max = (long long)p.Hkv * p.B * (p.cap / kPage);
   }
   const int ntiles = (p.R + 7) / 8;
+  if (job.fmt == 0 && p.R > kTcMinRows) {
+    switch ((p.R + 7) / 8) {
+      case 3: return launch_tc_t<24>(p, p_max, stream);
+      case 4: return launch_tc_t<32>(p, p_max, stream);
+      case 5: return launch_tc_t<40>(p, p_max, stream);
+      default: return launch_tc_t<48>(p, p_max, stream);
+    }
+  }
   int NT;
   if (ntiles <= 3) {
     NT = ntiles;

@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
         if (j.fwht) {
           prologue_fwht(w4, x, j.eps, lane, y);  // lane holds y[4 lane + e]: codes 4l..4l+3 = bytes 2l, 2l+1
           q = quantize(y);
-          *reinterpret_cast<uint16_t*>(dst + 2 * lane) =
+          *reinterpret_cast<uint16_t*>(dst + 16 * ((lane >> 3) ^ k_chunk_swz(slot)) + ((2 * lane) & 15)) =
               (uint16_t)((q.c[0] | (q.c[1] << 4)) | ((q.c[2] | (q.c[3] << 4)) << 8));
         } else {
           prologue(Ms, nbuf, x, j.eps, lane, y);  // lane holds y[lane + 32u]
@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t hi = __shfl_down_sync(0xffffffffu, q.c[u], 1);
-            if ((lane & 1) == 0) dst[(lane + 32 * u) >> 1] = (uint8_t)(q.c[u] | (hi << 4));
+            const int byte = (lane + 32 * u) >> 1;  // codes 2 byte, 2 byte + 1
+            if ((lane & 1) == 0) dst[16 * ((byte >> 4) ^ k_chunk_swz(slot)) + (byte & 15)] = (uint8_t)(q.c[u] | (hi << 4));
           }
         }
         if (lane == 0) {

@@ -69,7 +69,10 @@ def unpack_int4(tensors, b, h, L):
     blk = tensors["pages"][pages, h].cpu().numpy()          # [L, 8704]: each position's page-head block
     slot = pos % 64
     rows = np.arange(L)
-    kc = blk[rows[:, None], slot[:, None] * 64 + np.arange(64)[None, :]]
+    # K chunk c of slot s sits at physical chunk c ^ (((s >> 1) & 1) | ((s >> 2) & 2))
+    ksw = ((slot >> 1) & 1) | ((slot >> 2) & 2)
+    kbyte = np.arange(64)[None, :]
+    kc = blk[rows[:, None], slot[:, None] * 64 + 16 * ((kbyte >> 4) ^ ksw[:, None]) + (kbyte & 15)]
     vc = blk[rows[:, None], 4096 + slot[:, None] * 64 + np.arange(64)[None, :]]
     meta = blk[:, 8192:8704].copy().view(np.uint32)          # [L, 128]: K meta 0..63, V meta 64..127
     km = meta[rows, slot]
