@@ -1514,9 +1514,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   named_barrier(kFinBar, kFinThreads);
 }
 
-// One block per (segment, query row): merges the segment's CTA partials and normalises.
+// Query rows per combine block: the page prefix is built once for them and the partial loads of
+// all of them are in flight together.
+constexpr int kCombRows = 4;
+
+// Work items (segment, group of up to kCombRows query rows), spread over a grid of a few blocks
+// per SM: each block builds the page prefix once (before the wait, so while the attention grid
+// finishes), then merges each item's CTA partials row by row and normalises. Thread d owns
+// output dim d.
 template <int FMT>
-__global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(128, 4) combine_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
   volatile int* flags = cpre + p.B + 1;
   // The previous grid is the same call's attention kernel. It triggers this launch only after
@@ -1526,8 +1533,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   griddep_wait();
   griddep_launch_dependents();
   __syncthreads();
-  const int R = p.R;
-  const int seg = blockIdx.x / R, row = blockIdx.x - (blockIdx.x / R) * R;
+  const int R = p.R, ngr = (R + kCombRows - 1) / kCombRows;
+  const int n_items = p.B * p.Hkv * ngr;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  const int seg = item / ngr, rg = item - seg * ngr;
+  const int r0 = rg * kCombRows, nr = min(kCombRows, R - r0);
   const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
   const long long P = (long long)p.Hkv * cpre[p.B];
   const int n_eff = (int)min((long long)p.n_cta, P);
@@ -1535,49 +1545,75 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p) {
   const long long first_pg = (long long)p.Hkv * cpre[b] + (long long)h * np;
   const int c0 = (int)cta_of(first_pg, P, n_eff), c1 = (int)cta_of(first_pg + np - 1, P, n_eff);
   const int d = threadIdx.x;
-  // chunks of up to 8 partials: all loads of a chunk are issued before any is used; the chunk
-  // is merged with log-sum-exp weights against its own maximum, then folded into the total
-  float M = -INFINITY, lsum = 0.0f, a = 0.0f;
-  for (int cb = c0; cb <= c1; cb += 8) {
-    float mv[8], lv[8], av[8];
+  // per row: chunks of up to 8 partials, every load of a chunk (of all the block's rows) issued
+  // before any is used; a chunk is merged with log-sum-exp weights against its own maximum,
+  // then folded into the row's total
+  float M[kCombRows], lsum[kCombRows], a[kCombRows];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (cb + k <= c1) {
-        const float* src = p.partials + ((size_t)(cb + k + seg) * R + row) * kPartialStride;
-        mv[k] = src[0];
-        lv[k] = src[1];
-        av[k] = src[2 + d];
-      } else {
-        mv[k] = -INFINITY;
-        lv[k] = 0.0f;
-        av[k] = 0.0f;
+  for (int i = 0; i < kCombRows; ++i) {
+    M[i] = -INFINITY;
+    lsum[i] = 0.0f;
+    a[i] = 0.0f;
+  }
+  for (int cb = c0; cb <= c1; cb += 8) {
+    float mv[kCombRows][8], lv[kCombRows][8], av[kCombRows][8];
+#pragma unroll
+    for (int i = 0; i < kCombRows; ++i) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (i < nr && cb + k <= c1) {
+          const float* src = p.partials + ((size_t)(cb + k + seg) * R + r0 + i) * kPartialStride;
+          mv[i][k] = src[0];
+          lv[i][k] = src[1];
+          av[i][k] = src[2 + d];
+        } else {
+          mv[i][k] = -INFINITY;
+          lv[i][k] = 0.0f;
+          av[i][k] = 0.0f;
+        }
       }
     }
-    float Mc = mv[0];
 #pragma unroll
-    for (int k = 1; k < 8; ++k) Mc = fmaxf(Mc, mv[k]);
-    if (Mc == -INFINITY) continue;  // nothing visible in this chunk
-    float lc = 0.0f, ac = 0.0f;
+    for (int i = 0; i < kCombRows; ++i) {
+      float Mc = mv[i][0];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float w = fast_exp2(mv[k] - Mc);
-      lc += w * lv[k];
-      ac += w * av[k];
-    }
-    if (M == -INFINITY) {
-      M = Mc;
-      lsum = lc;
-      a = ac;
-    } else {
-      const float Mn = fmaxf(M, Mc);
-      const float so = fast_exp2(M - Mn), sc = fast_exp2(Mc - Mn);
-      lsum = lsum * so + lc * sc;
-      a = a * so + ac * sc;
-      M = Mn;
+      for (int k = 1; k < 8; ++k) Mc = fmaxf(Mc, mv[i][k]);
+      if (Mc == -INFINITY) continue;  // nothing visible in this chunk
+      float lc = 0.0f, ac = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float w = fast_exp2(mv[i][k] - Mc);
+        lc += w * lv[i][k];
+        ac += w * av[i][k];
+      }
+      if (M[i] == -INFINITY) {
+        M[i] = Mc;
+        lsum[i] = lc;
+        a[i] = ac;
+      } else {
+        const float Mn = fmaxf(M[i], Mc);
+        const float so = fast_exp2(M[i] - Mn), sc = fast_exp2(Mc - Mn);
+        lsum[i] = lsum[i] * so + lc * sc;
+        a[i] = a[i] * so + ac * sc;
+        M[i] = Mn;
+      }
     }
   }
-  const int r = row / p.G, gi = row - (row / p.G) * p.G;
-  p.out[(((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + d] = a / lsum;
+#pragma unroll
+  for (int i = 0; i < kCombRows; ++i) {
+    if (i < nr) {
+      const int row = r0 + i;
+      const int r = row / p.G, gi = row - (row / p.G) * p.G;
+      p.out[(((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + d] = a[i] / lsum[i];
+    }
+  }
+  }
+}
+
+// Combine grid: the work items, at most 4 blocks per SM (one wave at 128 registers a thread).
+unsigned combine_grid(const AttnParams& p, int sm) {
+  const long long items = (long long)p.B * p.Hkv * ((p.R + kCombRows - 1) / kCombRows);
+  return (unsigned)std::max<long long>(1, std::min<long long>(items, 4LL * sm));
 }
 
 struct DevCache {
@@ -1638,7 +1674,7 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_kernel<FMT, NT>, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
+  cfg.gridDim = dim3(combine_grid(p, sm), 1, 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
   return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
@@ -1688,7 +1724,7 @@ cudaError_t launch_tc_t(AttnParams& p, long long p_max, cudaStream_t stream) {
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<NR>, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((unsigned)(p.B * p.Hkv * p.R), 1, 1);
+  cfg.gridDim = dim3(combine_grid(p, sm), 1, 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
   return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);

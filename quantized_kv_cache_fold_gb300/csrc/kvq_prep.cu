@@ -25,14 +25,28 @@ namespace {
 
 constexpr int kPrepWarps = 8;
 constexpr int kPrepThreads = kPrepWarps * 32;
-constexpr int kMStride = 129;  // padded row stride of the matrix in shared memory (conflict-free)
-constexpr int kPrepSmem = (128 * kMStride + kPrepWarps * 128) * 4;
+// Row stride of the matrix in shared memory: 16-byte rows, and a 16-byte load of 8 lanes' rows
+// (j, j + 1, ..., word offsets 132 j) covers the 32 banks once.
+constexpr int kMStride = 132;
+// Rows per warp and pass of the matrix prologue (1, 2, 4 or 8, from the call's row counts):
+// each matrix entry read from shared memory serves all of them, and row pairs share one
+// fma.rn.f32x2. One row per pass is bound by the matrix reads.
+constexpr int kMaxRows = 8;
+constexpr int kPrepSmem = (128 * kMStride + kPrepWarps * 128 * kMaxRows) * 4;
+
+// Smallest of 1, 2, 4, 8 that covers `rows` rows per warp in one pass (8 at most).
+inline int rows_per_pass(long long rows, long long warps) {
+  const long long per = (rows + warps - 1) / std::max(1LL, warps);
+  return per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
+}
 
 struct PrepParams {
   PrepJobs j;
   int kv_blocks;
   int kv_jobs;
   int q_jobs;
+  int kv_rows;  // key/value jobs per warp and pass (matrix prologue)
+  int q_rows;   // query rows per warp and pass (matrix prologue)
 };
 
 // 1 / sqrt(mean(x^2) + eps) of the 128-vector spread over the warp (lane l holds
@@ -72,33 +86,87 @@ __device__ __forceinline__ void prologue_fwht(const float4 w, const float (&x)[4
   for (int e = 0; e < 4; ++e) y[e] = __fmul_rn(c, v[e]);
 }
 
-// y = M n(x). Lane l holds x[4l..4l+3] and returns y[l + 32u], u = 0..3.
-// Ms: shared [128][kMStride] (Ms[j*kMStride + i] = M[j][i]); nbuf: shared float[128] of this warp.
-__device__ __forceinline__ void prologue(const float* __restrict__ Ms, float* nbuf, const float (&x)[4], float eps,
-                                         int lane, float (&y)[4]) {
-  const float inv = norm_inv(x, eps);
-  reinterpret_cast<float4*>(nbuf)[lane] =
-      make_float4(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv), __fmul_rn(x[2], inv), __fmul_rn(x[3], inv));
-  __syncwarp();
-  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-  const float* m0 = Ms + lane * kMStride;
-#pragma unroll 2
-  for (int i = 0; i < kD; i += 4) {
-    const float4 n4 = reinterpret_cast<const float4*>(nbuf)[i >> 2];
-    const float nv[4] = {n4.x, n4.y, n4.z, n4.w};
+// y[r] = M n(x[r]) for the rows r < nr (rows from nr on are zero and their y is not used).
+// Lane l holds x[r][4l..4l+3] and returns y[r][u] = row r's output l + 32u, u = 0..3, each the
+// fma chain over k = 0..127 in order, acc = fma(M[l + 32u][k], n[k], acc) from 0, with
+// n = fp32(x / sqrt(mean(x^2) + eps)) (norm_inv's order). Rows 2p and 2p + 1 run in the two
+// halves of one fma.rn.f32x2, which rounds each half as fma.rn.f32: the chains are unchanged.
+// Ms: shared [128][kMStride], Ms[j kMStride + k] = M[j][k]; nbuf: shared float[R][128] of this
+// warp (R = 1: n; R even: pair p at float 256 p, element k of rows 2p, 2p + 1 side by side).
+template <int R>
+__device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, float* nbuf, const float (&x)[R][4],
+                                              int nr, float eps, int lane, float (&y)[R][4]) {
+  float nx[R][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      a0 = __fmaf_rn(m0[i + u], nv[u], a0);
-      a1 = __fmaf_rn(m0[32 * kMStride + i + u], nv[u], a1);
-      a2 = __fmaf_rn(m0[64 * kMStride + i + u], nv[u], a2);
-      a3 = __fmaf_rn(m0[96 * kMStride + i + u], nv[u], a3);
+  for (int r = 0; r < R; ++r) {
+    if (r < nr) {
+      const float inv = norm_inv(x[r], eps);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) nx[r][e] = __fmul_rn(x[r][e], inv);
+    } else {
+      nx[r][0] = nx[r][1] = nx[r][2] = nx[r][3] = 0.0f;
+    }
+  }
+  if constexpr (R == 1) {
+    reinterpret_cast<float4*>(nbuf)[lane] = make_float4(nx[0][0], nx[0][1], nx[0][2], nx[0][3]);
+  } else {
+#pragma unroll
+    for (int pr = 0; pr < R / 2; ++pr) {
+      float4* d = reinterpret_cast<float4*>(nbuf + pr * 256) + 2 * lane;
+      d[0] = make_float4(nx[2 * pr][0], nx[2 * pr + 1][0], nx[2 * pr][1], nx[2 * pr + 1][1]);
+      d[1] = make_float4(nx[2 * pr][2], nx[2 * pr + 1][2], nx[2 * pr][3], nx[2 * pr + 1][3]);
     }
   }
   __syncwarp();
-  y[0] = a0;
-  y[1] = a1;
-  y[2] = a2;
-  y[3] = a3;
+  const float* m0 = Ms + lane * kMStride;
+  if constexpr (R == 1) {
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+      const float4 n4 = reinterpret_cast<const float4*>(nbuf)[k >> 2];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 m = *reinterpret_cast<const float4*>(m0 + 32 * c * kMStride + k);
+        a[c] = __fmaf_rn(m.x, n4.x, a[c]);
+        a[c] = __fmaf_rn(m.y, n4.y, a[c]);
+        a[c] = __fmaf_rn(m.z, n4.z, a[c]);
+        a[c] = __fmaf_rn(m.w, n4.w, a[c]);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[0][c] = a[c];
+  } else {
+    uint64_t a2[R / 2][4];
+#pragma unroll
+    for (int pr = 0; pr < R / 2; ++pr) a2[pr][0] = a2[pr][1] = a2[pr][2] = a2[pr][3] = 0ull;
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+      float4 m[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) m[c] = *reinterpret_cast<const float4*>(m0 + 32 * c * kMStride + k);
+#pragma unroll
+      for (int pr = 0; pr < R / 2; ++pr) {
+        const float4 n01 = reinterpret_cast<const float4*>(nbuf + pr * 256)[k >> 1];      // k, k + 1
+        const float4 n23 = reinterpret_cast<const float4*>(nbuf + pr * 256)[(k >> 1) + 1];  // k + 2, k + 3
+        const uint64_t nn[4] = {f2(n01.x, n01.y), f2(n01.z, n01.w), f2(n23.x, n23.y), f2(n23.z, n23.w)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          a2[pr][c] = fma_f2(f2(m[c].x, m[c].x), nn[0], a2[pr][c]);
+          a2[pr][c] = fma_f2(f2(m[c].y, m[c].y), nn[1], a2[pr][c]);
+          a2[pr][c] = fma_f2(f2(m[c].z, m[c].z), nn[2], a2[pr][c]);
+          a2[pr][c] = fma_f2(f2(m[c].w, m[c].w), nn[3], a2[pr][c]);
+        }
+      }
+    }
+#pragma unroll
+    for (int pr = 0; pr < R / 2; ++pr)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        y[2 * pr][c] = f2lo(a2[pr][c]);
+        y[2 * pr + 1][c] = f2hi(a2[pr][c]);
+      }
+  }
+  __syncwarp();
 }
 
 struct Quant4 {
@@ -143,11 +211,156 @@ __device__ __forceinline__ Quant4 quantize(const float (&y)[4]) {
   return r;
 }
 
+// Page block and slot of key/value job `job` (token-head, row index token * Hkv + head), or
+// nullptr after recording the error (position outside the sequence's pages, or a block-table
+// entry outside the pool).
+__device__ __forceinline__ uint8_t* job_block(const PrepJobs& j, int job, int lane, int& slot) {
+  const int Hkv = j.cache.num_kv_heads;
+  const int tok = job / Hkv, h = job - (job / Hkv) * Hkv;
+  int seq, pos;
+  if (j.seq_ids) {
+    seq = j.seq_ids[tok];
+    pos = j.positions[tok];
+  } else {
+    seq = tok / j.S;
+    pos = j.ctx_len[seq] + (tok - seq * j.S);
+  }
+  slot = 0;
+  if (seq < 0 || seq >= j.cache.num_seqs || pos < 0 || pos >= j.cache.max_pages_per_seq * kPage) {
+    if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_POS);
+    return nullptr;
+  }
+  const int page = j.cache.block_table[(size_t)seq * j.cache.max_pages_per_seq + pos / kPage];
+  if (page < 0 || page >= j.cache.num_pages) {
+    if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_PAGE);
+    return nullptr;
+  }
+  slot = pos & (kPage - 1);
+  return j.cache.pages + ((size_t)page * Hkv + h) * KVQ_INT4_BLOCK_BYTES;
+}
+
+// Stores one job's key codes qk (matrix prologue order: lane holds outputs lane + 32u; FWHT
+// order: 4 lane + e) and value codes qv with their scales and offsets into slot `slot` of
+// block `blk`; a row that held a non-finite value is skipped and recorded instead.
+__device__ __forceinline__ void store_job(const PrepJobs& j, uint8_t* blk, int slot, bool k_finite, bool v_finite,
+                                          const Quant4& qk, const Quant4& qv, bool fwht_order, int lane) {
+  uint32_t* meta = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kRec4);
+  if (!k_finite) {
+    if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+  } else {
+    uint8_t* dst = blk + slot * kRec4;
+    if (fwht_order) {  // codes 4l..4l+3 = bytes 2l, 2l+1
+      *reinterpret_cast<uint16_t*>(dst + 16 * ((lane >> 3) ^ k_chunk_swz(slot)) + ((2 * lane) & 15)) =
+          (uint16_t)((qk.c[0] | (qk.c[1] << 4)) | ((qk.c[2] | (qk.c[3] << 4)) << 8));
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, qk.c[u], 1);
+        const int byte = (lane + 32 * u) >> 1;  // codes 2 byte, 2 byte + 1
+        if ((lane & 1) == 0) dst[16 * ((byte >> 4) ^ k_chunk_swz(slot)) + (byte & 15)] = (uint8_t)(qk.c[u] | (hi << 4));
+      }
+    }
+    if (lane == 0) {
+      meta[slot] = qk.meta;
+      if (qk.flags) set_err(j.dev_err, qk.flags);
+    }
+  }
+  if (!v_finite) {
+    if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+  } else {
+    const uint32_t two = v_encode4(qv.c[0], qv.c[1], qv.c[2], qv.c[3]);  // lane holds elements 4l..4l+3
+    const int chunk = (lane >> 3) ^ ((slot >> 1) & 3);
+    *reinterpret_cast<uint16_t*>(blk + kPage * kRec4 + slot * kRec4 + chunk * 16 + ((2 * lane) & 15)) = (uint16_t)two;
+    if (lane == 0) {
+      meta[kPage + slot] = qv.meta;
+      if (qv.flags) set_err(j.dev_err, qv.flags);
+    }
+  }
+}
+
+// Key/value jobs of this block with the matrix prologue, R consecutive jobs per warp and pass.
+// Every row of a pass is loaded, and every job's slot looked up, before any is used; the pass's
+// key and value rows are quantised with no store in between (their shuffle and division chains
+// interleave), then stored.
+template <int R>
+__device__ __forceinline__ void kv_rows_matrix(const PrepParams& p, const float* Ms, float* nbuf, int warp, int lane) {
+  const PrepJobs& j = p.j;
+  for (int job0 = ((int)blockIdx.x * kPrepWarps + warp) * R; job0 < p.kv_jobs; job0 += p.kv_blocks * kPrepWarps * R) {
+    const int nr = min(R, p.kv_jobs - job0);
+    float x[R][4], xv[R][4], y[R][4];
+    uint8_t* blk[R];
+    int slot[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r < nr) {
+        load_row4(j.k, j.kv_bf16, (size_t)(job0 + r), lane, x[r]);
+        load_row4(j.v, j.kv_bf16, (size_t)(job0 + r), lane, xv[r]);
+      } else {
+        x[r][0] = x[r][1] = x[r][2] = x[r][3] = 0.0f;
+        xv[r][0] = xv[r][1] = xv[r][2] = xv[r][3] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) blk[r] = r < nr ? job_block(j, job0 + r, lane, slot[r]) : nullptr;
+    bool kf[R], vf[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      kf[r] = warp_all_finite(x[r]);
+      vf[r] = warp_all_finite(xv[r]);
+    }
+    prologue_rows<R>(Ms, nbuf, x, nr, j.eps, lane, y);
+    Quant4 qk[R], qv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      qk[r] = quantize(y[r]);
+      qv[r] = quantize(xv[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (blk[r]) store_job(j, blk[r], slot[r], kf[r], vf[r], qk[r], qv[r], false, lane);
+  }
+}
+
+// Query rows of this block with the matrix prologue, R rows per warp and pass. Every row of a
+// pass is loaded before any is checked, so the loads are in flight together.
+template <int R>
+__device__ __forceinline__ void q_rows_matrix(const PrepParams& p, const float* Ms, float* nbuf, int qb, int nqb,
+                                              int warp, int lane) {
+  const PrepJobs& j = p.j;
+  for (int row0 = (qb * kPrepWarps + warp) * R; row0 < p.q_jobs; row0 += nqb * kPrepWarps * R) {
+    const int nr = min(R, p.q_jobs - row0);
+    float x[R][4], y[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r < nr) {
+        load_row4(j.q, j.q_bf16, (size_t)(row0 + r), lane, x[r]);
+      } else {
+        x[r][0] = x[r][1] = x[r][2] = x[r][3] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (r < nr && !warp_all_finite(x[r]) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+    prologue_rows<R>(Ms, nbuf, x, nr, j.eps, lane, y);  // lane holds y[r][lane + 32u]
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r < nr) {
+        const size_t row = (size_t)(row0 + r);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          j.q_rot[row * kD + lane + 32 * u] = y[r][u];
+          if (j.q_rot_out) j.q_rot_out[row * kD + lane + 32 * u] = y[r][u];
+        }
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
   extern __shared__ __align__(16) float smem_f[];
   float* Ms = smem_f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* nbuf = smem_f + 128 * kMStride + warp * 128;
+  float* nbuf = smem_f + 128 * kMStride + warp * 128 * kMaxRows;
   const PrepJobs& j = p.j;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
@@ -155,9 +368,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   // first rows, and the folded weights (M, or the FWHT multipliers), which are complete before
   // the call (kvq.h) and are staged into shared memory now.
   const size_t rbytes = (size_t)kD * ((kv_role ? j.kv_bf16 : j.q_bf16) ? 2 : 4);
-  const int job0 = kv_role ? (int)blockIdx.x * kPrepWarps + warp
-                           : ((int)blockIdx.x - p.kv_blocks) * kPrepWarps + warp;
-  const bool has_job0 = job0 < (kv_role ? p.kv_jobs : p.q_jobs);
+  // rows per warp and pass: p.kv_rows / p.q_rows with the matrix prologue, one with the FWHT one
+  const int nrows = j.fwht ? 1 : (kv_role ? p.kv_rows : p.q_rows);
+  const int job0 = kv_role ? ((int)blockIdx.x * kPrepWarps + warp) * nrows
+                           : (((int)blockIdx.x - p.kv_blocks) * kPrepWarps + warp) * nrows;
+  const int njobs = kv_role ? p.kv_jobs : p.q_jobs;
+  const bool has_job0 = job0 < njobs;
   const uint8_t* r0a = nullptr;  // first job's rows (key and value, or query)
   const uint8_t* r0b = nullptr;
   if (has_job0) {
@@ -168,12 +384,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       r0a = static_cast<const uint8_t*>(j.q) + (size_t)job0 * rbytes;
     }
   }
-  if (lane == 0 && r0a) prefetch_l2_bulk(r0a, (uint32_t)rbytes);
-  if (lane == 0 && r0b) prefetch_l2_bulk(r0b, (uint32_t)rbytes);
+  const int n0 = has_job0 ? min(nrows, njobs - job0) : 1;  // the first pass's rows are consecutive
+  if (lane == 0 && r0a) prefetch_l2_bulk(r0a, (uint32_t)(rbytes * n0));
+  if (lane == 0 && r0b) prefetch_l2_bulk(r0b, (uint32_t)(rbytes * n0));
   // the FWHT prologue needs only this lane's four multipliers; the matrix prologue stages M
   const float4 w4 = j.fwht ? reinterpret_cast<const float4*>(M)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   if (!j.fwht) {
-    // 16 independent 16-byte loads per thread, then the padded (conflict-free) shared stores
+    // 16 independent 16-byte loads per thread, then the 16-byte shared stores (padded rows)
     constexpr int kPer = kD * kD / 4 / kPrepThreads;
     float4 v[kPer];
 #pragma unroll
@@ -181,107 +398,53 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int e = 4 * (threadIdx.x + u * kPrepThreads);
-      float* d = Ms + (e >> 7) * kMStride + (e & 127);
-      d[0] = v[u].x;
-      d[1] = v[u].y;
-      d[2] = v[u].z;
-      d[3] = v[u].w;
+      *reinterpret_cast<float4*>(Ms + (e >> 7) * kMStride + (e & 127)) = v[u];
     }
   }
   __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
 
-  const int Hkv = j.cache.num_kv_heads;
   if (kv_role) {
-    for (int job = blockIdx.x * kPrepWarps + warp; job < p.kv_jobs; job += p.kv_blocks * kPrepWarps) {
-      const int tok = job / Hkv, h = job - (job / Hkv) * Hkv;
-      int seq, pos;
-      if (j.seq_ids) {
-        seq = j.seq_ids[tok];
-        pos = j.positions[tok];
-      } else {
-        seq = tok / j.S;
-        pos = j.ctx_len[seq] + (tok - seq * j.S);
-      }
-      if (seq < 0 || seq >= j.cache.num_seqs || pos < 0 || pos >= j.cache.max_pages_per_seq * kPage) {
-        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_POS);
-        continue;
-      }
-      const int page = j.cache.block_table[(size_t)seq * j.cache.max_pages_per_seq + pos / kPage];
-      if (page < 0 || page >= j.cache.num_pages) {
-        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_PAGE);
-        continue;
-      }
-      const int slot = pos & (kPage - 1);
-      uint8_t* blk = j.cache.pages + ((size_t)page * Hkv + h) * KVQ_INT4_BLOCK_BYTES;
-      uint32_t* meta = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kRec4);
-      const size_t row = (size_t)tok * Hkv + h;
-
-      float x[4], xv[4];  // key and value rows, loaded together
-      load_row4(j.k, j.kv_bf16, row, lane, x);
-      load_row4(j.v, j.kv_bf16, row, lane, xv);
-      if (!warp_all_finite(x)) {
-        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
-      } else {
+    if (j.fwht) {
+      for (int job = blockIdx.x * kPrepWarps + warp; job < p.kv_jobs; job += p.kv_blocks * kPrepWarps) {
+        float x[1][4], xv[1][4];
+        load_row4(j.k, j.kv_bf16, (size_t)job, lane, x[0]);  // row index = token * Hkv + head = job
+        load_row4(j.v, j.kv_bf16, (size_t)job, lane, xv[0]);
         float y[4];
-        uint8_t* dst = blk + slot * kRec4;
-        Quant4 q;
-        if (j.fwht) {
-          prologue_fwht(w4, x, j.eps, lane, y);  // lane holds y[4 lane + e]: codes 4l..4l+3 = bytes 2l, 2l+1
-          q = quantize(y);
-          *reinterpret_cast<uint16_t*>(dst + 16 * ((lane >> 3) ^ k_chunk_swz(slot)) + ((2 * lane) & 15)) =
-              (uint16_t)((q.c[0] | (q.c[1] << 4)) | ((q.c[2] | (q.c[3] << 4)) << 8));
-        } else {
-          prologue(Ms, nbuf, x, j.eps, lane, y);  // lane holds y[lane + 32u]
-          q = quantize(y);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t hi = __shfl_down_sync(0xffffffffu, q.c[u], 1);
-            const int byte = (lane + 32 * u) >> 1;  // codes 2 byte, 2 byte + 1
-            if ((lane & 1) == 0) dst[16 * ((byte >> 4) ^ k_chunk_swz(slot)) + (byte & 15)] = (uint8_t)(q.c[u] | (hi << 4));
-          }
-        }
-        if (lane == 0) {
-          meta[slot] = q.meta;
-          if (q.flags) set_err(j.dev_err, q.flags);
-        }
+        prologue_fwht(w4, x[0], j.eps, lane, y);  // lane holds y[4 lane + e]
+        int slot;
+        uint8_t* blk = job_block(j, job, lane, slot);
+        if (blk)
+          store_job(j, blk, slot, warp_all_finite(x[0]), warp_all_finite(xv[0]), quantize(y), quantize(xv[0]), true,
+                    lane);
       }
-
-      if (!warp_all_finite(xv)) {
-        if (lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
-      } else {
-        const Quant4 q = quantize(xv);  // lane holds elements 4l..4l+3
-        const uint32_t two = v_encode4(q.c[0], q.c[1], q.c[2], q.c[3]);
-        const int chunk = (lane >> 3) ^ ((slot >> 1) & 3);
-        *reinterpret_cast<uint16_t*>(blk + kPage * kRec4 + slot * kRec4 + chunk * 16 + ((2 * lane) & 15)) =
-            (uint16_t)two;
-        if (lane == 0) {
-          meta[kPage + slot] = q.meta;
-          if (q.flags) set_err(j.dev_err, q.flags);
-        }
-      }
+      return;
+    }
+    switch (p.kv_rows) {
+      case 4: kv_rows_matrix<4>(p, Ms, nbuf, warp, lane); break;
+      case 2: kv_rows_matrix<2>(p, Ms, nbuf, warp, lane); break;
+      default: kv_rows_matrix<1>(p, Ms, nbuf, warp, lane); break;
     }
   } else {
     const int qb = blockIdx.x - p.kv_blocks, nqb = gridDim.x - p.kv_blocks;
-    for (int row = qb * kPrepWarps + warp; row < p.q_jobs; row += nqb * kPrepWarps) {
-      float x[4];
-      load_row4(j.q, j.q_bf16, (size_t)row, lane, x);
-      if (!warp_all_finite(x) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
-      float y[4];
-      if (j.fwht) {  // lane holds q~[4 lane + e]
-        prologue_fwht(w4, x, j.eps, lane, y);
+    if (j.fwht) {
+      for (int row = qb * kPrepWarps + warp; row < p.q_jobs; row += nqb * kPrepWarps) {
+        float x[4], y[4];
+        load_row4(j.q, j.q_bf16, (size_t)row, lane, x);
+        if (!warp_all_finite(x) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
+        prologue_fwht(w4, x, j.eps, lane, y);  // lane holds q~[4 lane + e]
         const float4 y4 = make_float4(y[0], y[1], y[2], y[3]);
         reinterpret_cast<float4*>(j.q_rot + (size_t)row * kD)[lane] = y4;
         if (j.q_rot_out) reinterpret_cast<float4*>(j.q_rot_out + (size_t)row * kD)[lane] = y4;
-        continue;
       }
-      prologue(Ms, nbuf, x, j.eps, lane, y);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        j.q_rot[(size_t)row * kD + lane + 32 * u] = y[u];
-        if (j.q_rot_out) j.q_rot_out[(size_t)row * kD + lane + 32 * u] = y[u];
-      }
+      return;
+    }
+    switch (p.q_rows) {
+      case 8: q_rows_matrix<8>(p, Ms, nbuf, qb, nqb, warp, lane); break;
+      case 4: q_rows_matrix<4>(p, Ms, nbuf, qb, nqb, warp, lane); break;
+      case 2: q_rows_matrix<2>(p, Ms, nbuf, qb, nqb, warp, lane); break;
+      default: q_rows_matrix<1>(p, Ms, nbuf, qb, nqb, warp, lane); break;
     }
   }
 }
@@ -346,9 +509,26 @@ cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
   p.kv_jobs = jobs.k ? jobs.T * jobs.cache.num_kv_heads : 0;
   p.q_jobs = jobs.q ? jobs.nq_rows : 0;
   if (p.kv_jobs == 0 && p.q_jobs == 0) return cudaSuccess;
+  // One wave: two blocks per SM (shared memory), shared between key/value and query work in
+  // proportion to rows (a key/value job counted as 1.5 query rows: its two quantisations).
   const int cap = 2 * sm_count();
-  p.kv_blocks = std::min((p.kv_jobs + kPrepWarps - 1) / kPrepWarps, cap);
-  const int q_blocks = std::min((p.q_jobs + kPrepWarps - 1) / kPrepWarps, cap);
+  const int kv_max = (p.kv_jobs + kPrepWarps - 1) / kPrepWarps, q_max = (p.q_jobs + kPrepWarps - 1) / kPrepWarps;
+  int q_blocks;
+  if (kv_max + q_max <= cap) {
+    p.kv_blocks = kv_max;
+    q_blocks = q_max;
+  } else {
+    const double wkv = 1.5 * p.kv_jobs, wq = p.q_jobs;
+    p.kv_blocks = std::min(kv_max, std::max(p.kv_jobs ? 1 : 0, (int)(cap * wkv / (wkv + wq) + 0.5)));
+    q_blocks = std::min(q_max, std::max(p.q_jobs ? 1 : 0, cap - p.kv_blocks));
+  }
+  // (a key/value pass holds key, value and output rows: at most 4 jobs, so nothing spills)
+  p.kv_rows = jobs.fwht ? 1 : std::min(4, rows_per_pass(p.kv_jobs, (long long)p.kv_blocks * kPrepWarps));
+  p.q_rows = jobs.fwht ? 1 : rows_per_pass(p.q_jobs, (long long)q_blocks * kPrepWarps);
+  if (!jobs.fwht) {  // blocks whose warps would have no pass
+    p.kv_blocks = std::min(p.kv_blocks, (p.kv_jobs + kPrepWarps * p.kv_rows - 1) / (kPrepWarps * p.kv_rows));
+    q_blocks = std::min(q_blocks, (p.q_jobs + kPrepWarps * p.q_rows - 1) / (kPrepWarps * p.q_rows));
+  }
   int dev = 0;
   cudaGetDevice(&dev);
   {
