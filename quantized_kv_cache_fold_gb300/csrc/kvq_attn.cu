@@ -853,7 +853,7 @@ constexpr int kTcMinRows = 16;
 constexpr int kTcWarps = 16;  // warp 15 only completes the last warpgroup (setmaxnreg is per warpgroup)
 // registers per thread of the converters (warps 0-3), the softmax warps (4-11) and the producer /
 // issuer warpgroup (12-15), set by setmaxnreg from the launch's 128
-constexpr int kTcRegConv = 104, kTcRegSoftmax = 168, kTcRegAux = 64;
+constexpr int kTcRegConv = 96, kTcRegSoftmax = 168, kTcRegAux = 64;
 static_assert(128 * kTcRegConv + 256 * kTcRegSoftmax + 128 * kTcRegAux <= kTcWarps * 32 * 128,
               "register shares above the launch's allocation");
 constexpr int kTcThreads = kTcWarps * 32;
@@ -863,8 +863,8 @@ constexpr int kTcHalf = kTcMaxRows * 128;  // bytes of one 64-dim half of Q'
 constexpr int kTcBars = 32;                // mbarriers of the kernel (see its list)
 
 struct TcLayout {  // offsets from the 1024-byte aligned start of dynamic shared memory
-  size_t stages, qt, pt, meta, bars, valid, flags, taddr, rowc, rowst, ovrow, red, rowm, rcx, rcy, ralpha, rdelta, pre,
-      total;
+  size_t stages, qt, pt, meta, bars, valid, flags, taddr, uinfo, rowc, rowst, ovrow, red, rowm, rcx, rcy, ralpha, rdelta,
+      pre, total;
   __host__ __device__ explicit TcLayout(int B) {
     stages = 0;
     qt = kTcStages * (size_t)kStage4;  // 69632 = 68 * 1024
@@ -874,7 +874,8 @@ struct TcLayout {  // offsets from the 1024-byte aligned start of dynamic shared
     valid = bars + 8 * kTcBars;
     flags = valid + 4 * kTcStages;
     taddr = flags + 16;
-    rowc = align_up(taddr + 16, 16);
+    uinfo = align_up(taddr + 16, 16);
+    rowc = uinfo + 3 * 16;
     rowst = rowc + 16 * kTcMaxRows;
     ovrow = rowst + 4 * kTcMaxRows;
     red = ovrow + 4 * kTcMaxRows;
@@ -961,6 +962,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   float* ovrow = reinterpret_cast<float*>(smem + L.ovrow);
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* rowm = reinterpret_cast<float*>(smem + L.rowm);
+  // descriptor of unit u in slot u % 3, written by converter warp 0 before its cready(u) arrival:
+  // (sequence | head << 16, local page of its first page, pages | first << 2 | last << 3 |
+  // final << 4, CTA page index after it). The slot is rewritten only after PV(u) completed.
+  int4* uinfo = reinterpret_cast<int4*>(smem + L.uinfo);
   float* rcx = reinterpret_cast<float*>(smem + L.rcx);        // rowc x and y by row, for 16-byte loads
   float* rcy = reinterpret_cast<float*>(smem + L.rcy);
   float* ralpha = reinterpret_cast<float*>(smem + L.ralpha);  // a base move: factor on a row's sums and O
@@ -1030,21 +1035,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   // written before cready(u), which the softmax warps waited for before they arrived on pready(u).
   {  // warps 13 and 14
     if (lane == 0 && active) {
-      TcUnits Uu(p, pre, p0, p1);
       bool ok = true;
       int b3 = 0;       // unit % 3
       uint32_t ph3 = 0;  // (unit / 3) & 1
+      int segi = -1;    // segment of the unit
       if (warp == 13) {
         const uint32_t idesc = umma_idesc_f16(NM, false, false);
         const uint64_t dq = umma_sdesc(smem_addr(smem + L.qt), 16, 1024);
         int pb3 = 0;       // (unit - 2) % 3, from unit 2 on
         uint32_t pph3 = 0;  // ((unit - 2) / 3) & 1
-        for (int v = 0; Uu.next(); ++v) {
+        for (int v = 0;; ++v) {
           const int b = v & 1;
           ok = mbar_wait_bounded(&cready[b3], ph3);
+          if (!ok) break;
+          const int uz = uinfo[b3].z;
+          if (uz & 4) ++segi;
           // S[b] was read before P of unit v - 2 was written
-          ok = ok && (v < 2 || mbar_wait_bounded(&pready[pb3], pph3));
-          ok = ok && (!Uu.first || mbar_wait_bounded(qready, (uint32_t)Uu.segi & 1u));
+          ok = v < 2 || mbar_wait_bounded(&pready[pb3], pph3);
+          ok = ok && (!(uz & 4) || mbar_wait_bounded(qready, (uint32_t)segi & 1u));
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tmem + kColS + 64 * b, a0 = tmem + kColAK + 64 * b;
@@ -1054,29 +1062,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
           umma_commit(&sfull[b]);
           if (++b3 == 3) { b3 = 0; ph3 ^= 1u; }
           if (v >= 2 && ++pb3 == 3) { pb3 = 0; pph3 ^= 1u; }
+          if (uz & 16) break;  // the CTA's last unit
         }
       } else {
         const uint32_t idesc = umma_idesc_f16(NM, false, true);
         const uint64_t dp = umma_sdesc(smem_addr(smem + L.pt), 16384, 1024);
-        while (Uu.next()) {
+        for (;;) {
           ok = mbar_wait_bounded(&pready[b3], ph3);
-          ok = ok && (!Uu.first || Uu.segi == 0 || mbar_wait_bounded(ofree, (uint32_t)(Uu.segi - 1) & 1u));
+          if (!ok) break;
+          const int uz = uinfo[b3].z;  // P(u) written implies cready(u) was seen
+          if (uz & 4) ++segi;
+          ok = !(uz & 4) || segi == 0 || mbar_wait_bounded(ofree, (uint32_t)(segi - 1) & 1u);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a0 = tmem + kColAV + 64 * b3;
           const uint64_t d0 = dp + (uint64_t)(b3 * (16384 >> 4));
-          const uint32_t acc0 = Uu.first ? 0u : 1u;
+          const uint32_t acc0 = (uz & 4) ? 0u : 1u;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // k-steps of 16 tokens: 2048 bytes of P each
             umma_f16_ts(tmem + kColO, a0 + 8 * kk, d0 + (uint64_t)(kk * (2048 >> 4)), idesc, kk > 0 ? 1u : acc0);
-          if (Uu.npg == 2) {
+          if ((uz & 3) == 2) {
 #pragma unroll
             for (int kk = 4; kk < 8; ++kk)
               umma_f16_ts(tmem + kColO, a0 + 8 * kk, d0 + (uint64_t)(kk * (2048 >> 4)), idesc, 1u);
           }
           umma_commit(&vfree[b3]);
-          if (Uu.last) umma_commit(ofull);
+          if (uz & 8) umma_commit(ofull);
           if (++b3 == 3) { b3 = 0; ph3 ^= 1u; }
+          if (uz & 16) break;  // the CTA's last unit
         }
       }
       if (!ok) {
@@ -1135,15 +1148,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
         const int s = jj ? s1 : s0;
         const uint8_t* st = stages + (size_t)s * kStage4;
         const int sw = k_chunk_swz(slot);
-        uint4 kc[4];  // all four 16-byte chunks loaded before any is converted
-#pragma unroll
-        for (int c = 0; c < 4; ++c) kc[c] = *reinterpret_cast<const uint4*>(st + slot * kRec4 + 16 * (c ^ sw));
+        const uint8_t* rec = st + slot * kRec4;
         const bool vld = valid[s] != 0;
         const uint32_t mk = reinterpret_cast<const uint32_t*>(st + 2 * kPage * kRec4)[slot];
         const uint32_t mv = reinterpret_cast<const uint32_t*>(st + 2 * kPage * kRec4)[kPage + slot];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // chunk c (words 4c..4c+3) -> columns 16c .. 16c + 15
-          const uint32_t wd[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
+        // chunk c (words 4c..4c+3) -> columns 16c .. 16c + 15; a rolled loop (the kernel's code
+        // competes for the instruction cache), each chunk's load issued one chunk ahead
+        uint4 kc = *reinterpret_cast<const uint4*>(rec + 16 * sw);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const uint4 kn = *reinterpret_cast<const uint4*>(rec + 16 * (((c + 1) & 3) ^ sw));
+          const uint32_t wd[4] = {kc.x, kc.y, kc.z, kc.w};
           uint32_t w16[16];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -1153,6 +1168,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
             for (int j = 0; j < 4; ++j) w16[4 * i + j] = h4[j];
           }
           tmem_st16u(tmem + lane_base + kColAK + 64 * bk + 16 * c, w16);
+          kc = kn;
         }
         if (vld) {
           const float sv = h2f_lo(mv);
@@ -1203,6 +1219,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
           tmem_st_16x256b_x4(col + ((uint32_t)(32 * q + 16) << 16), rb);
         }
       }
+      if (q == 0 && lane == 0)
+        uinfo[bv] = make_int4(Uc.b | (Uc.h << 16), Uc.lp(),
+                              npg | (Uc.first ? 4 : 0) | (Uc.last ? 8 : 0) | (Uc.k >= p1 ? 16 : 0), (int)(Uc.k - p0));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -1238,7 +1257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   // constants: (sum q~ * scale, -base (0 while the base is -inf; -inf on padding rows, whose
   // scores then are -inf), threshold of the lazy base (+inf on padding rows), last visible
   // position of the row's query).
-  auto load_segment = [&](int bq, int hq) {
+  auto load_segment = [&](int bq, int hq) -> int {
     bool bad = false;
     const int cb = eff_ctx(p, bq, bad, 0);
     for (int e = gt; e < H * 16; e += kGrp) {
@@ -1271,26 +1290,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
       }
     }
     fence_proxy_async_shared();
+    return cb;
   };
 
-  TcUnits U(p, pre, p0, p1);
-  bool more = active && U.next();
+  // units come from the descriptors in uinfo; the next segment's Q' is loaded at a segment end
+  bool more = active;
   bool err = false;
-  if (more) load_segment(U.b, U.h);
+  int ctx_next = 0;  // effective context length of the next segment
+  if (more) {
+    int b0, h0, lpf, npf;
+    decode_page(pre, p.B, p.Hkv, p0, b0, h0, lpf, npf);
+    ctx_next = load_segment(b0, h0);
+  }
   err = named_barrier_or(kGrpBar, kGrp, false);
   if (more && gt == 0) mbar_arrive(qready);
-  int ctxb = 0;
+  int ctxb = 0, segi = -1;
   // smallest lazy-base threshold over the half's rows (-inf until every row has a base)
   float thr_grp = -INFINITY;
   for (int v = 0; more && !err; ++v) {
     const int b = v & 1, bv = v % 3;
-    if (U.first) {
-      bool bad = false;
-      ctxb = eff_ctx(p, U.b, bad, 0);
-    }
     // waits are made warp-uniform: the tensor-memory loads after them are warp-collective
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sfull[b], (uint32_t)(v >> 1) & 1u) &&
                                           mbar_wait_bounded(&cready[bv], (uint32_t)(v / 3) & 1u));
+    const int4 ui = uinfo[bv];
+    const int ulp = ui.y, unpg = ui.z & 3;
+    const bool ufirst = (ui.z & 4) != 0, ulast = (ui.z & 8) != 0, ufinal = (ui.z & 16) != 0;
+    if (ufirst) {
+      ctxb = ctx_next;
+      ++segi;
+    }
     float d[H];
     if (ok) {
       tc_fence_after();
@@ -1309,7 +1337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
     // ---- scores of this token relative to each row's base; branch-free over the rows (padding
     // rows carry a -inf base); the causal limits apply only on a unit that reaches past the context
     const bool tvalid = ok && mt.z >= 0.0f;
-    const bool unit_mask = (U.lp() + U.npg) * kPage - 1 > ctxb;
+    const bool unit_mask = (ulp + unpg) * kPage - 1 > ctxb;
     float mx = -INFINITY;
     if (!tvalid) {
 #pragma unroll
@@ -1331,7 +1359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
         mx = fmax3(mx, d[4 * c + 2], d[4 * c + 3]);
       }
     } else {
-      const float fpos = (float)((U.lp() + jj) * kPage + slot);
+      const float fpos = (float)((ulp + jj) * kPage + slot);
 #pragma unroll
       for (int i = 0; i < H; ++i) {
         const float4 c = rowc[r0 + i];
@@ -1347,9 +1375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
       // ---- rare: move the base of the rows whose maximum passed it (row maxima over the 128 tokens)
 #pragma unroll
       for (int i = 0; i < H; ++i) {
-        float m1 = d[i];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        const float m1 = warp_max_all(d[i]);
         if (lane == 0) rowm[q * kTcMaxRows + r0 + i] = m1;
       }
       named_barrier(kGrpBar, kGrp);
@@ -1389,7 +1415,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
         for (int i = 0; i < H; ++i) d[i] += rdelta[r0 + i];
         // O (this thread's lane, the half's rows) -- not on a segment's first unit: O starts from
         // zero there. PV(v - 1) must have completed.
-        if (!U.first) {
+        if (!ufirst) {
           const bool okp = __all_sync(0xffffffffu, mbar_wait_bounded(&vfree[(v - 1) % 3], (uint32_t)((v - 1) / 3) & 1u));
           if (okp) {
             tc_fence_after();
@@ -1440,9 +1466,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
     __syncwarp();
     mbar_arrive_if(&pready[bv], lane == 0);
 
-    if (__builtin_expect(U.last, 0)) {
+    if (__builtin_expect(ulast, 0)) {
       // ---- segment end: token sums per row, the next segment's Q', then O -> CTA partial
-      const int seg = U.b * p.Hkv + U.h, segi = U.segi;
+      const int seg = (ui.x & 0xFFFF) * p.Hkv + (ui.x >> 16);
 #pragma unroll
       for (int i = 0; i < H; ++i) {
         float lt = (i & 1) ? f2hi(l2[i / 2]) : f2lo(l2[i / 2]);
@@ -1473,9 +1499,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
         ovrow[r] = ot;
       }
       named_barrier(kGrpBar, kGrp);
-      TcUnits Un = U;
-      const bool nmore = Un.next();
-      if (nmore) load_segment(Un.b, Un.h);
+      const bool nmore = !ufinal;
+      if (nmore) {
+        int nb, nh, nlp, nnp;
+        decode_page(pre, p.B, p.Hkv, p0 + ui.w, nb, nh, nlp, nnp);
+        ctx_next = load_segment(nb, nh);
+      }
       named_barrier(kGrpBar, kGrp);
       if (nmore && gt == 0) mbar_arrive(qready);
       thr_grp = -INFINITY;
@@ -1504,7 +1533,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
       err = named_barrier_or(kGrpBar, kGrp, !ok);
       if (!err && nmore && gt == 0) mbar_arrive(ofree);
     }
-    more = U.next();
+    more = !ufinal;
   }
   if (err && gt == 0) {
     set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);

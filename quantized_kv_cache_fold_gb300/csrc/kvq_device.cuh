@@ -303,6 +303,12 @@ __device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// Maximum of v over the 32 lanes of the warp (every lane active), in one instruction.
+__device__ __forceinline__ float warp_max_all(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
