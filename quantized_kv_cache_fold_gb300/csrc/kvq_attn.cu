@@ -1260,6 +1260,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   auto load_segment = [&](int bq, int hq) -> int {
     bool bad = false;
     const int cb = eff_ctx(p, bq, bad, 0);
+#pragma unroll 1
     for (int e = gt; e < H * 16; e += kGrp) {
       const int r = r0 + (e >> 4), w = e & 15;
       float part = 0.0f;
@@ -1307,166 +1308,174 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   int ctxb = 0, segi = -1;
   // smallest lazy-base threshold over the half's rows (-inf until every row has a base)
   float thr_grp = -INFINITY;
-  for (int v = 0; more && !err; ++v) {
-    const int b = v & 1, bv = v % 3;
-    // waits are made warp-uniform: the tensor-memory loads after them are warp-collective
-    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sfull[b], (uint32_t)(v >> 1) & 1u) &&
-                                          mbar_wait_bounded(&cready[bv], (uint32_t)(v / 3) & 1u));
-    const int4 ui = uinfo[bv];
-    const int ulp = ui.y, unpg = ui.z & 3;
-    const bool ufirst = (ui.z & 4) != 0, ulast = (ui.z & 8) != 0, ufinal = (ui.z & 16) != 0;
-    if (ufirst) {
-      ctxb = ctx_next;
-      ++segi;
-    }
-    float d[H];
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < H / 4; ++c) {
-        float t4[4];
-        tmem_ld4(tmem + lane_base + kColS + 64 * b + r0 + 4 * c, t4);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d[4 * c + i] = t4[i];
+  // segments; within one, its units (the hot loop), then the segment end after it
+  int v = 0;
+  while (more && !err) {
+    int4 ui;  // the unit's descriptor; after the unit loop, the segment's last unit's
+    for (;;) {
+      const int b = v & 1, bv = v % 3;
+      // waits are made warp-uniform: the tensor-memory loads after them are warp-collective
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sfull[b], (uint32_t)(v >> 1) & 1u) &&
+                                            mbar_wait_bounded(&cready[bv], (uint32_t)(v / 3) & 1u));
+      ui = uinfo[bv];
+      const int ulp = ui.y, unpg = ui.z & 3;
+      const bool ufirst = (ui.z & 4) != 0, ulast = (ui.z & 8) != 0;
+      if (ufirst) {
+        ctxb = ctx_next;
+        ++segi;
       }
-      tmem_wait_ld();
-    }
-    tc_fence_before();
-    const float4 mt = tmeta[bv * 128 + kl];  // (k scale * score scale * 2^24, k offset, v scale, v term)
+      float d[H];
+      if (ok) {
+        tc_fence_after();
+  #pragma unroll
+        for (int c = 0; c < H / 4; ++c) {
+          float t4[4];
+          tmem_ld4(tmem + lane_base + kColS + 64 * b + r0 + 4 * c, t4);
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) d[4 * c + i] = t4[i];
+        }
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      const float4 mt = tmeta[bv * 128 + kl];  // (k scale * score scale * 2^24, k offset, v scale, v term)
 
-    // ---- scores of this token relative to each row's base; branch-free over the rows (padding
-    // rows carry a -inf base); the causal limits apply only on a unit that reaches past the context
-    const bool tvalid = ok && mt.z >= 0.0f;
-    const bool unit_mask = (ulp + unpg) * kPage - 1 > ctxb;
-    float mx = -INFINITY;
-    if (!tvalid) {
-#pragma unroll
-      for (int i = 0; i < H; ++i) d[i] = -INFINITY;
-    } else if (!unit_mask) {
-      // d mt.x + (mt.y c.x + c.y), four rows at a time in fp32 pairs
-      const uint64_t mtx2 = f2(mt.x, mt.x), mty2 = f2(mt.y, mt.y);
-#pragma unroll
-      for (int c = 0; c < H / 4; ++c) {
-        const float4 cx = reinterpret_cast<const float4*>(rcx + r0)[c];
-        const float4 cy = reinterpret_cast<const float4*>(rcy + r0)[c];
-        const uint64_t s01 = fma_f2(f2(d[4 * c], d[4 * c + 1]), mtx2, fma_f2(mty2, f2(cx.x, cx.y), f2(cy.x, cy.y)));
-        const uint64_t s23 = fma_f2(f2(d[4 * c + 2], d[4 * c + 3]), mtx2, fma_f2(mty2, f2(cx.z, cx.w), f2(cy.z, cy.w)));
-        d[4 * c] = f2lo(s01);
-        d[4 * c + 1] = f2hi(s01);
-        d[4 * c + 2] = f2lo(s23);
-        d[4 * c + 3] = f2hi(s23);
-        mx = fmax3(mx, d[4 * c], d[4 * c + 1]);
-        mx = fmax3(mx, d[4 * c + 2], d[4 * c + 3]);
-      }
-    } else {
-      const float fpos = (float)((ulp + jj) * kPage + slot);
-#pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float4 c = rowc[r0 + i];
-        const float sc = fmaf(d[i], mt.x, fmaf(mt.y, c.x, c.y));
-        d[i] = fpos <= c.w ? sc : -INFINITY;
-        mx = fmaxf(mx, d[i]);
-      }
-    }
-    const bool need = mx > (mt.z >= 255.0f ? fminf(thr_grp, 0.0f) : thr_grp);  // large V scale: any excess
-    if (__builtin_expect(named_barrier_or(kGrpBar, kGrp, need || !ok), 0)) {
-      err = named_barrier_or(kGrpBar, kGrp, !ok);
-      if (err) break;
-      // ---- rare: move the base of the rows whose maximum passed it (row maxima over the 128 tokens)
-#pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float m1 = warp_max_all(d[i]);
-        if (lane == 0) rowm[q * kTcMaxRows + r0 + i] = m1;
-      }
-      named_barrier(kGrpBar, kGrp);
-      // one thread per row: the new base (published), the factor alpha on the row's sums and O
-      // and the shift of this unit's scores to the new base (1 and 0 where the base stays)
-      bool changed = false;
-      if (gt < H) {
-        const int r = r0 + gt;
-        float alpha = 1.0f, delta = 0.0f;
-        if (r < R) {
-          const float mt4 = fmaxf(fmaxf(rowm[r], rowm[kTcMaxRows + r]), fmaxf(rowm[2 * kTcMaxRows + r], rowm[3 * kTcMaxRows + r]));
-          const float4 c = rowc[r];
-          const float mold = rowst[r], muse = -c.y;
-          const float mnew = fmaxf(mold, muse + mt4);
-          if (mnew != mold) {
-            const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
-            alpha = fast_exp2(mold - mu2);
-            delta = muse - mu2;
-            changed = true;
-            const float nb = mnew == -INFINITY ? 0.0f : -mnew;
-            rowst[r] = mnew;
-            rowc[r] = make_float4(c.x, nb, mnew == -INFINITY ? -INFINITY : 8.0f, c.w);
-            rcy[r] = nb;
-          }
+      // ---- scores of this token relative to each row's base; branch-free over the rows (padding
+      // rows carry a -inf base); the causal limits apply only on a unit that reaches past the context
+      const bool tvalid = ok && mt.z >= 0.0f;
+      const bool unit_mask = (ulp + unpg) * kPage - 1 > ctxb;
+      float mx = -INFINITY;
+      if (!tvalid) {
+  #pragma unroll
+        for (int i = 0; i < H; ++i) d[i] = -INFINITY;
+      } else if (!unit_mask) {
+        // d mt.x + (mt.y c.x + c.y), four rows at a time in fp32 pairs
+        const uint64_t mtx2 = f2(mt.x, mt.x), mty2 = f2(mt.y, mt.y);
+  #pragma unroll
+        for (int c = 0; c < H / 4; ++c) {
+          const float4 cx = reinterpret_cast<const float4*>(rcx + r0)[c];
+          const float4 cy = reinterpret_cast<const float4*>(rcy + r0)[c];
+          const uint64_t s01 = fma_f2(f2(d[4 * c], d[4 * c + 1]), mtx2, fma_f2(mty2, f2(cx.x, cx.y), f2(cy.x, cy.y)));
+          const uint64_t s23 = fma_f2(f2(d[4 * c + 2], d[4 * c + 3]), mtx2, fma_f2(mty2, f2(cx.z, cx.w), f2(cy.z, cy.w)));
+          d[4 * c] = f2lo(s01);
+          d[4 * c + 1] = f2hi(s01);
+          d[4 * c + 2] = f2lo(s23);
+          d[4 * c + 3] = f2hi(s23);
+          mx = fmax3(mx, d[4 * c], d[4 * c + 1]);
+          mx = fmax3(mx, d[4 * c + 2], d[4 * c + 3]);
         }
-        ralpha[r] = alpha;
-        rdelta[r] = delta;
-      }
-      if (named_barrier_or(kGrpBar, kGrp, changed)) {
-#pragma unroll
-        for (int i = 0; i < H / 2; ++i) {
-          const uint64_t a2 = f2(ralpha[r0 + 2 * i], ralpha[r0 + 2 * i + 1]);
-          l2[i] = mul_f2(l2[i], a2);
-          ov2[i] = mul_f2(ov2[i], a2);
+      } else {
+        const float fpos = (float)((ulp + jj) * kPage + slot);
+  #pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float4 c = rowc[r0 + i];
+          const float sc = fmaf(d[i], mt.x, fmaf(mt.y, c.x, c.y));
+          d[i] = fpos <= c.w ? sc : -INFINITY;
+          mx = fmaxf(mx, d[i]);
         }
-#pragma unroll
-        for (int i = 0; i < H; ++i) d[i] += rdelta[r0 + i];
-        // O (this thread's lane, the half's rows) -- not on a segment's first unit: O starts from
-        // zero there. PV(v - 1) must have completed.
-        if (!ufirst) {
-          const bool okp = __all_sync(0xffffffffu, mbar_wait_bounded(&vfree[(v - 1) % 3], (uint32_t)((v - 1) / 3) & 1u));
-          if (okp) {
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < H / 4; ++c) {
-              float t4[4];
-              tmem_ld4(tmem + lane_base + kColO + r0 + 4 * c, t4);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 4; ++i) t4[i] *= ralpha[r0 + 4 * c + i];
-              tmem_st4(tmem + lane_base + kColO + r0 + 4 * c, t4);
+      }
+      const bool need = mx > (mt.z >= 255.0f ? fminf(thr_grp, 0.0f) : thr_grp);  // large V scale: any excess
+      if (__builtin_expect(named_barrier_or(kGrpBar, kGrp, need || !ok), 0)) {
+        err = named_barrier_or(kGrpBar, kGrp, !ok);
+        if (err) break;
+        // ---- rare: move the base of the rows whose maximum passed it (row maxima over the 128 tokens)
+  #pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float m1 = warp_max_all(d[i]);
+          if (lane == 0) rowm[q * kTcMaxRows + r0 + i] = m1;
+        }
+        named_barrier(kGrpBar, kGrp);
+        // one thread per row: the new base (published), the factor alpha on the row's sums and O
+        // and the shift of this unit's scores to the new base (1 and 0 where the base stays)
+        bool changed = false;
+        if (gt < H) {
+          const int r = r0 + gt;
+          float alpha = 1.0f, delta = 0.0f;
+          if (r < R) {
+            const float mt4 = fmaxf(fmaxf(rowm[r], rowm[kTcMaxRows + r]), fmaxf(rowm[2 * kTcMaxRows + r], rowm[3 * kTcMaxRows + r]));
+            const float4 c = rowc[r];
+            const float mold = rowst[r], muse = -c.y;
+            const float mnew = fmaxf(mold, muse + mt4);
+            if (mnew != mold) {
+              const float mu2 = mnew == -INFINITY ? 0.0f : mnew;
+              alpha = fast_exp2(mold - mu2);
+              delta = muse - mu2;
+              changed = true;
+              const float nb = mnew == -INFINITY ? 0.0f : -mnew;
+              rowst[r] = mnew;
+              rowc[r] = make_float4(c.x, nb, mnew == -INFINITY ? -INFINITY : 8.0f, c.w);
+              rcy[r] = nb;
             }
-            tmem_wait_st();
           }
-          tc_fence_before();
-          err = named_barrier_or(kGrpBar, kGrp, !okp);
-          if (err) break;
+          ralpha[r] = alpha;
+          rdelta[r] = delta;
         }
+        if (named_barrier_or(kGrpBar, kGrp, changed)) {
+  #pragma unroll
+          for (int i = 0; i < H / 2; ++i) {
+            const uint64_t a2 = f2(ralpha[r0 + 2 * i], ralpha[r0 + 2 * i + 1]);
+            l2[i] = mul_f2(l2[i], a2);
+            ov2[i] = mul_f2(ov2[i], a2);
+          }
+  #pragma unroll
+          for (int i = 0; i < H; ++i) d[i] += rdelta[r0 + i];
+          // O (this thread's lane, the half's rows) -- not on a segment's first unit: O starts from
+          // zero there. PV(v - 1) must have completed.
+          if (!ufirst) {
+            const bool okp = __all_sync(0xffffffffu, mbar_wait_bounded(&vfree[(v - 1) % 3], (uint32_t)((v - 1) / 3) & 1u));
+            if (okp) {
+              tc_fence_after();
+  #pragma unroll
+              for (int c = 0; c < H / 4; ++c) {
+                float t4[4];
+                tmem_ld4(tmem + lane_base + kColO + r0 + 4 * c, t4);
+                tmem_wait_ld();
+  #pragma unroll
+                for (int i = 0; i < 4; ++i) t4[i] *= ralpha[r0 + 4 * c + i];
+                tmem_st4(tmem + lane_base + kColO + r0 + 4 * c, t4);
+              }
+              tmem_wait_st();
+            }
+            tc_fence_before();
+            err = named_barrier_or(kGrpBar, kGrp, !okp);
+            if (err) break;
+          }
+        }
+        thr_grp = INFINITY;
+  #pragma unroll
+        for (int i = 0; i < H; ++i)
+          if (r0 + i < R) thr_grp = fminf(thr_grp, rowc[r0 + i].z);
       }
-      thr_grp = INFINITY;
-#pragma unroll
-      for (int i = 0; i < H; ++i)
-        if (r0 + i < R) thr_grp = fminf(thr_grp, rowc[r0 + i].z);
-    }
 
-    // ---- P s_V in f16 (row kl of P[v % 3], MN-major: query row r at byte 2 (r & 7) of chunk r >> 3)
-    uint32_t pk[H / 2];
-    const uint64_t mtz2 = f2(mt.z, mt.z), mtw2 = f2(mt.w, mt.w);
-#pragma unroll
-    for (int i = 0; i < H / 2; ++i) {
-      const uint64_t pp = f2(fast_exp2(d[2 * i]), fast_exp2(d[2 * i + 1]));
-      l2[i] = add_f2(l2[i], pp);
-      ov2[i] = fma_f2(pp, mtw2, ov2[i]);
-      const uint64_t ps = mul_f2(pp, mtz2);
-      pk[i] = pack_f16x2_sat(f2lo(ps), f2hi(ps));
+      // ---- P s_V in f16 (row kl of P[v % 3], MN-major: query row r at byte 2 (r & 7) of chunk r >> 3)
+      uint32_t pk[H / 2];
+      const uint64_t mtz2 = f2(mt.z, mt.z), mtw2 = f2(mt.w, mt.w);
+  #pragma unroll
+      for (int i = 0; i < H / 2; ++i) {
+        const uint64_t pp = f2(fast_exp2(d[2 * i]), fast_exp2(d[2 * i + 1]));
+        l2[i] = add_f2(l2[i], pp);
+        ov2[i] = fma_f2(pp, mtw2, ov2[i]);
+        const uint64_t ps = mul_f2(pp, mtz2);
+        pk[i] = pack_f16x2_sat(f2lo(ps), f2hi(ps));
+      }
+      // P[v % 3] was read by PV(v - 3), complete since the converters waited for it before
+      // writing this unit's codes (cready above)
+      {
+        uint8_t* prow = smem + L.pt + bv * 16384 + kl * 128;
+  #pragma unroll
+        for (int m = 0; m < H / 4; ++m) {  // rows r0 + 4m .. + 3 (8 bytes)
+          const int r = r0 + 4 * m;
+          *reinterpret_cast<uint2*>(prow + 16 * ((r >> 3) ^ (kl & 7)) + 2 * (r & 7)) = make_uint2(pk[2 * m], pk[2 * m + 1]);
+        }
+        fence_proxy_async_shared();
+      }
+      __syncwarp();
+      mbar_arrive_if(&pready[bv], lane == 0);
+      ++v;
+      if (ulast) break;
     }
-    // P[v % 3] was read by PV(v - 3), complete since the converters waited for it before
-    // writing this unit's codes (cready above)
+    if (err) break;
+
     {
-      uint8_t* prow = smem + L.pt + bv * 16384 + kl * 128;
-#pragma unroll
-      for (int m = 0; m < H / 4; ++m) {  // rows r0 + 4m .. + 3 (8 bytes)
-        const int r = r0 + 4 * m;
-        *reinterpret_cast<uint2*>(prow + 16 * ((r >> 3) ^ (kl & 7)) + 2 * (r & 7)) = make_uint2(pk[2 * m], pk[2 * m + 1]);
-      }
-      fence_proxy_async_shared();
-    }
-    __syncwarp();
-    mbar_arrive_if(&pready[bv], lane == 0);
-
-    if (__builtin_expect(ulast, 0)) {
       // ---- segment end: token sums per row, the next segment's Q', then O -> CTA partial
       const int seg = (ui.x & 0xFFFF) * p.Hkv + (ui.x >> 16);
 #pragma unroll
@@ -1499,7 +1508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
         ovrow[r] = ot;
       }
       named_barrier(kGrpBar, kGrp);
-      const bool nmore = !ufinal;
+      const bool nmore = (ui.z & 16) == 0;
       if (nmore) {
         int nb, nh, nlp, nnp;
         decode_page(pre, p.B, p.Hkv, p0 + ui.w, nb, nh, nlp, nnp);
@@ -1509,7 +1518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
       if (nmore && gt == 0) mbar_arrive(qready);
       thr_grp = -INFINITY;
       // O of the finished segment: lane kl holds dim 32q + 4g + 2e + h for kl = 32q + 16e + 8h + g
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)segi & 1u));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)segi & 1u));
       if (ok) {
         tc_fence_after();
         float o[H];
@@ -1533,7 +1542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
       err = named_barrier_or(kGrpBar, kGrp, !ok);
       if (!err && nmore && gt == 0) mbar_arrive(ofree);
     }
-    more = !ufinal;
+    more = (ui.z & 16) == 0;
   }
   if (err && gt == 0) {
     set_err(p.dev_err, KVQ_DEVERR_TIMEOUT);
