@@ -1552,15 +1552,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   named_barrier(kFinBar, kFinThreads);
 }
 
-// Query rows per combine block: the page prefix is built once for them and the partial loads of
-// all of them are in flight together.
-constexpr int kCombRows = 4;
+// Query rows per combine work item (1 or 4): with 4 the page prefix is built once for them and the
+// partial loads of all of them are in flight together; calls with few (segment, row) pairs keep
+// one row per item so that more blocks share the merge.
+constexpr int kCombRowsMax = 4;
 
 // Work items (segment, group of up to kCombRows query rows), spread over a grid of a few blocks
 // per SM: each block builds the page prefix once (before the wait, so while the attention grid
 // finishes), then merges each item's CTA partials row by row and normalises. Thread d owns
 // output dim d.
-template <int FMT>
+template <int FMT, int kCombRows>
 __global__ void __launch_bounds__(128, 4) combine_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
   volatile int* flags = cpre + p.B + 1;
@@ -1648,10 +1649,21 @@ __global__ void __launch_bounds__(128, 4) combine_kernel(const AttnParams p) {
   }
 }
 
-// Combine grid: the work items, at most 4 blocks per SM (one wave at 128 registers a thread).
-unsigned combine_grid(const AttnParams& p, int sm) {
-  const long long items = (long long)p.B * p.Hkv * ((p.R + kCombRows - 1) / kCombRows);
-  return (unsigned)std::max<long long>(1, std::min<long long>(items, 4LL * sm));
+// Rows per combine item: 4 once one row per item would need more than one wave of blocks.
+int combine_rows(const AttnParams& p, int sm) {
+  return (long long)p.B * p.Hkv * p.R > 4LL * sm ? kCombRowsMax : 1;
+}
+
+// Combine launch: the work items over at most 4 blocks per SM (one wave at 128 registers a thread).
+template <int FMT>
+cudaError_t launch_combine(cudaLaunchConfig_t& cfg, const AttnParams& p, int sm) {
+  const int cr = combine_rows(p, sm);
+  const long long items = (long long)p.B * p.Hkv * ((p.R + cr - 1) / cr);
+  cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>(items, 4LL * sm)), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
+  return cr == 1 ? cudaLaunchKernelEx(&cfg, combine_kernel<FMT, 1>, p)
+                 : cudaLaunchKernelEx(&cfg, combine_kernel<FMT, kCombRowsMax>, p);
 }
 
 struct DevCache {
@@ -1712,10 +1724,7 @@ cudaError_t launch_attn_t(AttnParams& p, size_t smem, int threads, long long p_m
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_kernel<FMT, NT>, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(combine_grid(p, sm), 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
+  return launch_combine<FMT>(cfg, p, sm);
 }
 
 // int4 with more than 8 query rows per KV head: the tcgen05 kernel (NR = rows rounded up to 8),
@@ -1762,10 +1771,7 @@ cudaError_t launch_tc_t(AttnParams& p, long long p_max, cudaStream_t stream) {
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<NR>, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(combine_grid(p, sm), 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<0>, p);
+  return launch_combine<0>(cfg, p, sm);
 }
 
 }  // namespace

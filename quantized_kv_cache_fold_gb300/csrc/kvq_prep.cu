@@ -25,14 +25,19 @@ namespace {
 
 constexpr int kPrepWarps = 8;
 constexpr int kPrepThreads = kPrepWarps * 32;
-// Row stride of the matrix in shared memory: 16-byte rows, and a 16-byte load of 8 lanes' rows
-// (j, j + 1, ..., word offsets 132 j) covers the 32 banks once.
-constexpr int kMStride = 132;
+// Row stride of the matrix in shared memory, per launch: 132 when passes hold several rows (16-byte
+// rows; a 16-byte load of 8 lanes' rows, word offsets 132 j, covers the 32 banks once), 129 when
+// every pass is one row (4-byte loads, lanes' rows on distinct banks; fewer wavefronts per load
+// than 16-byte loads of one row, the faster form for decode's few rows).
+constexpr int kMStride = 132;  // the larger: shared-memory size
 // Rows per warp and pass of the matrix prologue (1, 2, 4 or 8, from the call's row counts):
 // each matrix entry read from shared memory serves all of them, and row pairs share one
 // fma.rn.f32x2. One row per pass is bound by the matrix reads.
 constexpr int kMaxRows = 8;
-constexpr int kPrepSmem = (128 * kMStride + kPrepWarps * 128 * kMaxRows) * 4;
+constexpr int kPrepSmem = (128 * kMStride + kPrepWarps * 128 * kMaxRows) * 4;  // the most a launch asks for
+// Shared memory of a launch: the matrix rows and each warp's normalised rows, no more (a prep
+// grid starts while the previous grid's blocks still hold shared memory on the SMs).
+inline int prep_smem(int mstride, int rows) { return (128 * mstride + kPrepWarps * 128 * rows) * 4; }
 
 // Smallest of 1, 2, 4, 8 that covers `rows` rows per warp in one pass (8 at most).
 inline int rows_per_pass(long long rows, long long warps) {
@@ -47,6 +52,8 @@ struct PrepParams {
   int q_jobs;
   int kv_rows;  // key/value jobs per warp and pass (matrix prologue)
   int q_rows;   // query rows per warp and pass (matrix prologue)
+  int mstride;  // row stride of the matrix in shared memory (132, or 129 when both are 1)
+  int nrows;    // rows of each warp's normalised-row buffer: max(kv_rows, q_rows)
 };
 
 // 1 / sqrt(mean(x^2) + eps) of the 128-vector spread over the warp (lane l holds
@@ -91,10 +98,10 @@ __device__ __forceinline__ void prologue_fwht(const float4 w, const float (&x)[4
 // fma chain over k = 0..127 in order, acc = fma(M[l + 32u][k], n[k], acc) from 0, with
 // n = fp32(x / sqrt(mean(x^2) + eps)) (norm_inv's order). Rows 2p and 2p + 1 run in the two
 // halves of one fma.rn.f32x2, which rounds each half as fma.rn.f32: the chains are unchanged.
-// Ms: shared [128][kMStride], Ms[j kMStride + k] = M[j][k]; nbuf: shared float[R][128] of this
+// Ms: shared [128][ms], Ms[j ms + k] = M[j][k] (ms = 129 or 132); nbuf: shared float[R][128] of this
 // warp (R = 1: n; R even: pair p at float 256 p, element k of rows 2p, 2p + 1 side by side).
 template <int R>
-__device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, float* nbuf, const float (&x)[R][4],
+__device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, int ms, float* nbuf, const float (&x)[R][4],
                                               int nr, float eps, int lane, float (&y)[R][4]) {
   float nx[R][4];
 #pragma unroll
@@ -118,19 +125,31 @@ __device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, floa
     }
   }
   __syncwarp();
-  const float* m0 = Ms + lane * kMStride;
+  const float* m0 = Ms + lane * ms;
   if constexpr (R == 1) {
     float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (ms != kMStride) {  // 4-byte loads (ms = 129)
 #pragma unroll 2
-    for (int k = 0; k < kD; k += 4) {
-      const float4 n4 = reinterpret_cast<const float4*>(nbuf)[k >> 2];
+      for (int k = 0; k < kD; k += 4) {
+        const float4 n4 = reinterpret_cast<const float4*>(nbuf)[k >> 2];
+        const float nv[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 m = *reinterpret_cast<const float4*>(m0 + 32 * c * kMStride + k);
-        a[c] = __fmaf_rn(m.x, n4.x, a[c]);
-        a[c] = __fmaf_rn(m.y, n4.y, a[c]);
-        a[c] = __fmaf_rn(m.z, n4.z, a[c]);
-        a[c] = __fmaf_rn(m.w, n4.w, a[c]);
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) a[c] = __fmaf_rn(m0[32 * c * ms + k + u], nv[u], a[c]);
+      }
+    } else {  // 16-byte loads (ms = 132)
+#pragma unroll 2
+      for (int k = 0; k < kD; k += 4) {
+        const float4 n4 = reinterpret_cast<const float4*>(nbuf)[k >> 2];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 m = *reinterpret_cast<const float4*>(m0 + 32 * c * kMStride + k);
+          a[c] = __fmaf_rn(m.x, n4.x, a[c]);
+          a[c] = __fmaf_rn(m.y, n4.y, a[c]);
+          a[c] = __fmaf_rn(m.z, n4.z, a[c]);
+          a[c] = __fmaf_rn(m.w, n4.w, a[c]);
+        }
       }
     }
 #pragma unroll
@@ -143,7 +162,7 @@ __device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, floa
     for (int k = 0; k < kD; k += 4) {
       float4 m[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) m[c] = *reinterpret_cast<const float4*>(m0 + 32 * c * kMStride + k);
+      for (int c = 0; c < 4; ++c) m[c] = *reinterpret_cast<const float4*>(m0 + 32 * c * ms + k);
 #pragma unroll
       for (int pr = 0; pr < R / 2; ++pr) {
         const float4 n01 = reinterpret_cast<const float4*>(nbuf + pr * 256)[k >> 1];      // k, k + 1
@@ -308,7 +327,7 @@ __device__ __forceinline__ void kv_rows_matrix(const PrepParams& p, const float*
       kf[r] = warp_all_finite(x[r]);
       vf[r] = warp_all_finite(xv[r]);
     }
-    prologue_rows<R>(Ms, nbuf, x, nr, j.eps, lane, y);
+    prologue_rows<R>(Ms, p.mstride, nbuf, x, nr, j.eps, lane, y);
     Quant4 qk[R], qv[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -341,7 +360,7 @@ __device__ __forceinline__ void q_rows_matrix(const PrepParams& p, const float* 
 #pragma unroll
     for (int r = 0; r < R; ++r)
       if (r < nr && !warp_all_finite(x[r]) && lane == 0) set_err(j.dev_err, KVQ_DEVERR_NONFINITE);
-    prologue_rows<R>(Ms, nbuf, x, nr, j.eps, lane, y);  // lane holds y[r][lane + 32u]
+    prologue_rows<R>(Ms, p.mstride, nbuf, x, nr, j.eps, lane, y);  // lane holds y[r][lane + 32u]
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (r < nr) {
@@ -356,11 +375,16 @@ __device__ __forceinline__ void q_rows_matrix(const PrepParams& p, const float* 
   }
 }
 
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
+// R: query rows per warp and pass (1, 2, 4 or 8); key/value passes take min(R, 4) jobs. One
+// instantiation per R keeps each launch's code to its own path (the decode launch, R = 1, is a
+// short latency-bound grid).
+template <int R>
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrepParams p) {
+  constexpr int RKV = R < 4 ? R : 4;
   extern __shared__ __align__(16) float smem_f[];
   float* Ms = smem_f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* nbuf = smem_f + 128 * kMStride + warp * 128 * kMaxRows;
+  float* nbuf = smem_f + 128 * p.mstride + warp * 128 * p.nrows;
   const PrepJobs& j = p.j;
   const bool kv_role = (int)blockIdx.x < p.kv_blocks;
   const float* M = kv_role ? j.Mk : j.Mq;
@@ -390,15 +414,24 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   // the FWHT prologue needs only this lane's four multipliers; the matrix prologue stages M
   const float4 w4 = j.fwht ? reinterpret_cast<const float4*>(M)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   if (!j.fwht) {
-    // 16 independent 16-byte loads per thread, then the 16-byte shared stores (padded rows)
+    // 16 independent 16-byte loads per thread, then the shared stores into padded rows
     constexpr int kPer = kD * kD / 4 / kPrepThreads;
     float4 v[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) v[u] = reinterpret_cast<const float4*>(M)[threadIdx.x + u * kPrepThreads];
+    const int ms = p.mstride;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int e = 4 * (threadIdx.x + u * kPrepThreads);
-      *reinterpret_cast<float4*>(Ms + (e >> 7) * kMStride + (e & 127)) = v[u];
+      float* d = Ms + (e >> 7) * ms + (e & 127);
+      if (ms == kMStride) {
+        *reinterpret_cast<float4*>(d) = v[u];
+      } else {
+        d[0] = v[u].x;
+        d[1] = v[u].y;
+        d[2] = v[u].z;
+        d[3] = v[u].w;
+      }
     }
   }
   __syncthreads();
@@ -421,11 +454,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       }
       return;
     }
-    switch (p.kv_rows) {
-      case 4: kv_rows_matrix<4>(p, Ms, nbuf, warp, lane); break;
-      case 2: kv_rows_matrix<2>(p, Ms, nbuf, warp, lane); break;
-      default: kv_rows_matrix<1>(p, Ms, nbuf, warp, lane); break;
-    }
+    kv_rows_matrix<RKV>(p, Ms, nbuf, warp, lane);
   } else {
     const int qb = blockIdx.x - p.kv_blocks, nqb = gridDim.x - p.kv_blocks;
     if (j.fwht) {
@@ -440,12 +469,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
       }
       return;
     }
-    switch (p.q_rows) {
-      case 8: q_rows_matrix<8>(p, Ms, nbuf, qb, nqb, warp, lane); break;
-      case 4: q_rows_matrix<4>(p, Ms, nbuf, qb, nqb, warp, lane); break;
-      case 2: q_rows_matrix<2>(p, Ms, nbuf, qb, nqb, warp, lane); break;
-      default: q_rows_matrix<1>(p, Ms, nbuf, qb, nqb, warp, lane); break;
-    }
+    q_rows_matrix<R>(p, Ms, nbuf, qb, nqb, warp, lane);
   }
 }
 
@@ -486,7 +510,7 @@ __global__ void fp8_append_kernel(const Fp8AppendJob j) {
 
 std::mutex g_prep_mu;  // guards the per-device caches below
 int g_sm_count[64] = {0};
-bool g_prep_attr[64] = {false};
+bool g_prep_attr[64][4] = {{false}};  // per device and instantiation (R = 1, 2, 4, 8)
 
 int sm_count() {
   int dev = 0;
@@ -522,34 +546,45 @@ cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
     p.kv_blocks = std::min(kv_max, std::max(p.kv_jobs ? 1 : 0, (int)(cap * wkv / (wkv + wq) + 0.5)));
     q_blocks = std::min(q_max, std::max(p.q_jobs ? 1 : 0, cap - p.kv_blocks));
   }
-  // (a key/value pass holds key, value and output rows: at most 4 jobs, so nothing spills)
-  p.kv_rows = jobs.fwht ? 1 : std::min(4, rows_per_pass(p.kv_jobs, (long long)p.kv_blocks * kPrepWarps));
-  p.q_rows = jobs.fwht ? 1 : rows_per_pass(p.q_jobs, (long long)q_blocks * kPrepWarps);
+  // rows per pass: enough for one pass per warp; the kernel takes R = the larger of the two
+  // roles' needs for query passes and min(R, 4) for key/value passes (a key/value pass holds key,
+  // value and output rows: at most 4 jobs, so nothing spills)
+  const int R = jobs.fwht ? 1
+                          : std::max(rows_per_pass(p.q_jobs, (long long)q_blocks * kPrepWarps),
+                                     std::min(4, rows_per_pass(p.kv_jobs, (long long)p.kv_blocks * kPrepWarps)));
+  p.q_rows = R;
+  p.kv_rows = std::min(R, 4);
+  p.mstride = p.kv_rows == 1 && p.q_rows == 1 ? 129 : kMStride;
+  p.nrows = std::max(p.kv_rows, p.q_rows);
   if (!jobs.fwht) {  // blocks whose warps would have no pass
     p.kv_blocks = std::min(p.kv_blocks, (p.kv_jobs + kPrepWarps * p.kv_rows - 1) / (kPrepWarps * p.kv_rows));
     q_blocks = std::min(q_blocks, (p.q_jobs + kPrepWarps * p.q_rows - 1) / (kPrepWarps * p.q_rows));
   }
+  const void* kern = R == 8 ? (const void*)prep_kernel<8> : R == 4 ? (const void*)prep_kernel<4>
+                   : R == 2 ? (const void*)prep_kernel<2> : (const void*)prep_kernel<1>;
+  const int ri = R == 8 ? 3 : R == 4 ? 2 : R == 2 ? 1 : 0;
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(g_prep_mu);
-    if (dev < 0 || dev >= 64 || !g_prep_attr[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+    if (dev < 0 || dev >= 64 || !g_prep_attr[dev][ri]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) g_prep_attr[dev] = true;
+      if (dev >= 0 && dev < 64) g_prep_attr[dev][ri] = true;
     }
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(p.kv_blocks + q_blocks), 1, 1);
   cfg.blockDim = dim3(kPrepThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPrepSmem;
+  cfg.dynamicSmemBytes = (size_t)prep_smem(p.mstride, p.nrows);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prep_kernel, p);
+  void* args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 cudaError_t launch_fp8_append(const Fp8AppendJob& job, cudaStream_t stream) {
