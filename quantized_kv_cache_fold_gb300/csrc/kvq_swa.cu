@@ -261,6 +261,22 @@ __device__ __forceinline__ void load_unit(uint8_t* st, const uint8_t* seg, int u
   bulk_g2s(st + kHalf, blk + kPage * kRec8, kHalf, bar, pol);
 }
 
+// Whether unit u holds a window position: a slot at most span back from slot_last (its slot
+// nearest behind slot_last is d slots back, 0 if it holds slot_last).
+__device__ __forceinline__ bool unit_in_window(int u, int slot_last, int span, int cap) {
+  const int first = u * kUnit, last = first + kUnit - 1;
+  const int d = (slot_last >= first && slot_last <= last) ? 0 : (slot_last - last + cap) % cap;
+  return d <= span;
+}
+
+// Position word read without ordering against other grids (relaxed): a hint for prefetches
+// issued before the grid wait; what the kernel uses is read again after it.
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 template <int NT>
 __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -295,13 +311,28 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     }
     fence_barrier_init();
     fence_proxy_async_shared();
-    if (tg == 0)  // the units copied first (all of a cluster plan's; a long stream's head)
+    // the units copied first (all of a cluster plan's); a one-CTA plan (many sequences) copies
+    // units that hold window positions once the position is known, so it prefetches the first of
+    // those as the position hint places them
+    if (tg == 0 && p.cs > 1) {
       for (int i = 0; i < min(nu, 2 * p.nst); ++i) {
         const int u = stream + i * nstream;
         const uint8_t* blk = seg + (size_t)(u >> 1) * kBlk + (u & 1) * kHalf;
         prefetch_l2_bulk(blk, kHalf);
         prefetch_l2_bulk(blk + kPage * kRec8, kHalf);
       }
+    } else if (tg == 0) {
+      const int ch = max(0, ld_relaxed_s32(p.pos0 + b));
+      const int pl = ch + p.S - 1, sl = pl % p.cap, sp = pl - max(0, ch - p.window + 1);
+      for (int i = 0, n = 0; i < nu && n < 2 * p.nst; ++i) {
+        const int u = stream + i * nstream;
+        if (!unit_in_window(u, sl, sp, p.cap)) continue;
+        const uint8_t* blk = seg + (size_t)(u >> 1) * kBlk + (u & 1) * kHalf;
+        prefetch_l2_bulk(blk, kHalf);
+        prefetch_l2_bulk(blk + kPage * kRec8, kHalf);
+        ++n;
+      }
+    }
     if (warp == 0 && rank == 0) {
       prefetch_l2(p.pos0 + b);
       for (int r = 0; r < p.S; ++r)  // the G query rows of this KV head are contiguous
@@ -318,8 +349,9 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
   griddep_wait();
   griddep_launch_dependents();  // after the wait: at most one grid runs ahead
 
-  // ---- this warp's first copies (L2 hits when the prefetch had time to land)
-  if (lane == 0) {
+  // ---- this warp's first copies (L2 hits when the prefetch had time to land); a one-CTA plan
+  // copies once the position is known (just below)
+  if (p.cs > 1 && lane == 0) {
     const uint64_t pol = policy_evict_first();
     for (int i = 0; i < min(p.nst, nu); ++i)
       load_unit(wst + (size_t)i * kStg, seg, stream + i * nstream, &wfull[i], pol);
@@ -338,6 +370,36 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     load_row4(p.v_new, p.bf16, row0, lane, xnew[1]);
   }
 
+  int c0 = c0raw;
+  if (c0 < 0) {
+    if (rank == 0 && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
+    c0 = 0;
+  }
+  const int p_last = c0 + p.S - 1;  // newest position after the append
+  const int slot_last = p_last % p.cap;
+
+  const int span = p_last - max(0, c0 - p.window + 1);
+  int issued = p.cs > 1 ? min(p.nst, nu) : 0;  // units issued so far (warp-uniform)
+  int next_i = issued;          // the stream's next unit index to consider for a refill
+  int su0 = stream, su1 = stream + nstream;  // unit held by stage 0 / 1 (nst <= 2)
+  int done = 0;                 // units consumed
+  // the stream's next unit that holds a window position
+  auto next_window_unit = [&]() {
+    for (; next_i < nu; ++next_i)
+      if (unit_in_window(stream + next_i * nstream, slot_last, span, p.cap)) break;
+  };
+  if (p.cs == 1) {  // the first copies, now that the window is known
+    for (int s = 0; s < p.nst; ++s) {
+      next_window_unit();
+      if (next_i >= nu) break;
+      const int un = stream + next_i * nstream;
+      if (lane == 0) load_unit(wst + (size_t)s * kStg, seg, un, &wfull[s], policy_evict_first());
+      if (s == 0) su0 = un;
+      else su1 = un;
+      ++next_i;
+      ++issued;
+    }
+  }
   // ---- query fragments (B operand, 8 rows per tile)
   uint32_t qf[NT][8][2];
 #pragma unroll
@@ -382,14 +444,6 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       qf[nt][ks][1] = pack_f16x2(qv[4 * ks + 2], qv[4 * ks + 3]);
     }
   }
-
-  int c0 = c0raw;
-  if (c0 < 0) {
-    if (rank == 0 && threadIdx.x == 0) set_err(p.dev_err, KVQ_DEVERR_POS);
-    c0 = 0;
-  }
-  const int p_last = c0 + p.S - 1;  // newest position after the append
-  const int slot_last = p_last % p.cap;
 
   // ---- per-row window limits
   int lim_lo[NT][2], lim_hi[NT][2];
@@ -452,16 +506,12 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
       for (int c = 0; c < 4; ++c) acc[nt][i][c] = 0.0f;
   }
 
-  // Units are consumed in the order they were issued. The first min(nst, nu) are the stream's
-  // first units, copied before the position was known; each refill takes the stream's next unit
-  // that holds a position of the rows' windows [max(0, c0 - window + 1), p_last] and skips units
-  // wholly outside them (the ring's slots beyond the window, and slots not yet written). A unit
-  // holding an appended row is never skipped.
-  const int span = p_last - max(0, c0 - p.window + 1);
-  int issued = min(p.nst, nu);  // units issued so far (warp-uniform)
-  int next_i = issued;          // the stream's next unit index to consider for a refill
-  int su0 = stream, su1 = stream + nstream;  // unit held by stage 0 / 1 (nst <= 2)
-  int done = 0;                 // units consumed
+  // Units are consumed in the order they were issued. A cluster plan's first min(nst, nu) are the
+  // stream's first units, copied before the position was known; a one-CTA plan's first ones, and
+  // every refill, are the stream's next units that hold a position of the rows' windows
+  // [max(0, c0 - window + 1), p_last]: units wholly outside them (the ring's slots beyond the
+  // window, and slots not yet written) are skipped. A unit holding an appended row is never
+  // skipped.
   for (int k = 0; k < issued; ++k) {
     const int s = k % p.nst;
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&wfull[s], (uint32_t)(k / p.nst) & 1u));
@@ -487,14 +537,8 @@ __global__ void __launch_bounds__(256, 1) swa_cluster_kernel(const SwaParams p) 
     attend_unit<NT>(st, u, p_last, slot_last, p.cap, p.score_scale, qf, lim_lo, lim_hi, m, l, acc, lane);
     done = k + 1;
     __syncwarp();
-    // refill this stage with the stream's next unit that holds a window position: the unit's
-    // slot nearest behind slot_last is d slots back (0 if it holds slot_last)
-    for (; next_i < nu; ++next_i) {
-      const int un = stream + next_i * nstream;
-      const int first = un * kUnit, last = first + kUnit - 1;
-      const int d = (slot_last >= first && slot_last <= last) ? 0 : (slot_last - last + p.cap) % p.cap;
-      if (d <= span) break;
-    }
+    // refill this stage with the stream's next unit that holds a window position
+    next_window_unit();
     if (next_i < nu) {
       const int un = stream + next_i * nstream;
       if (lane == 0) {
