@@ -225,10 +225,10 @@ class Stack256k:
 # is that ratio times its own algorithmic bytes (traffic grows with the pages read). The
 # counters belong to the kernel sources whose hash is recorded; after any change to them the
 # traffic is reported as null until a new capture.
-ATTN_CAPTURE = {"dram_read": 906262272, "dram_write": 3356160, "algorithmic": 905157248,
+ATTN_CAPTURE = {"dram_read": 906232576, "dram_write": 3410176, "algorithmic": 905157248,
                 "sources": ["quantized_kv_cache_fold_gb300/csrc/kvq_attn.cu",
                             "quantized_kv_cache_fold_gb300/csrc/kvq_device.cuh"],
-                "sources_sha256_16": "0d18d717a0b11eae"}
+                "sources_sha256_16": "b115995efdb2a651"}
 
 
 def attn_traffic(call_bytes):
