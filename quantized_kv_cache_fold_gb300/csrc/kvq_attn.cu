@@ -1552,118 +1552,177 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   named_barrier(kFinBar, kFinThreads);
 }
 
-// Query rows per combine work item (1 or 4): with 4 the page prefix is built once for them and the
-// partial loads of all of them are in flight together; calls with few (segment, row) pairs keep
-// one row per item so that more blocks share the merge.
-constexpr int kCombRowsMax = 4;
+// Two forms of the merge of a segment's CTA partials with log-sum-exp weights, then the
+// normalisation. Both build the page prefix once per block before waiting (so while the
+// attention grid finishes): the previous grid is the same call's attention kernel, which
+// triggers this launch only after its own wait, so every grid before it has completed, and it
+// writes nothing but the partials and the error word; the context lengths (read at L2, see
+// eff_ctx) are taken before waiting.
+//
+// combine_rows_kernel, for calls with many (segment, query row) items: one warp per item, lane
+// l owns output dims 2l, 2l + 1, 64 + 2l and 64 + 2l + 1 (two 8-byte loads of each partial
+// row), chunks of kCombChunkWarp partials in flight together, at most 64 registers a thread
+// so that one wave holds 4 blocks per SM.
+// combine_kernel, for calls with few items (long segments, so many partials each): one block
+// of 128 threads per item, thread d owns dim d, chunks of kCombChunkBlock partials.
+// Each chunk is merged against its own maximum, then folded into the item's total.
+constexpr int kCombWarps = 8;
+constexpr int kCombChunkWarp = 4;
+constexpr int kCombChunkBlock = 8;
 
-// Work items (segment, group of up to kCombRows query rows), spread over a grid of a few blocks
-// per SM: each block builds the page prefix once (before the wait, so while the attention grid
-// finishes), then merges each item's CTA partials row by row and normalises. Thread d owns
-// output dim d.
-template <int FMT, int kCombRows>
-__global__ void __launch_bounds__(128, 4) combine_kernel(const AttnParams p) {
+template <int FMT>
+__global__ void __launch_bounds__(kCombWarps * 32, 4) combine_rows_kernel(const AttnParams p) {
   extern __shared__ __align__(16) int cpre[];
   volatile int* flags = cpre + p.B + 1;
-  // The previous grid is the same call's attention kernel. It triggers this launch only after
-  // its own wait, so every grid before it has completed, and it writes nothing but the partials
-  // and the error word: the context lengths (read at L2, see eff_ctx) are taken before waiting.
   build_prefix(p, FMT, cpre, flags);
   griddep_wait();
   griddep_launch_dependents();
   __syncthreads();
-  const int R = p.R, ngr = (R + kCombRows - 1) / kCombRows;
-  const int n_items = p.B * p.Hkv * ngr;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-  const int seg = item / ngr, rg = item - seg * ngr;
-  const int r0 = rg * kCombRows, nr = min(kCombRows, R - r0);
-  const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+  const int lane = threadIdx.x & 31;
+  const int R = p.R;
   const long long P = (long long)p.Hkv * cpre[p.B];
   const int n_eff = (int)min((long long)p.n_cta, P);
-  const int np = cpre[b + 1] - cpre[b];
-  const long long first_pg = (long long)p.Hkv * cpre[b] + (long long)h * np;
-  const int c0 = (int)cta_of(first_pg, P, n_eff), c1 = (int)cta_of(first_pg + np - 1, P, n_eff);
-  const int d = threadIdx.x;
-  // per row: chunks of up to 8 partials, every load of a chunk (of all the block's rows) issued
-  // before any is used; a chunk is merged with log-sum-exp weights against its own maximum,
-  // then folded into the row's total
-  float M[kCombRows], lsum[kCombRows], a[kCombRows];
+  const int n_items = p.B * p.Hkv * R;
+  for (int item = blockIdx.x * kCombWarps + (threadIdx.x >> 5); item < n_items; item += gridDim.x * kCombWarps) {
+    const int seg = item / R, row = item - seg * R;
+    const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+    const int np = cpre[b + 1] - cpre[b];
+    const long long first_pg = (long long)p.Hkv * cpre[b] + (long long)h * np;
+    const int c0 = (int)cta_of(first_pg, P, n_eff), c1 = (int)cta_of(first_pg + np - 1, P, n_eff);
+    float M = -INFINITY, lsum = 0.0f;
+    float2 alo = make_float2(0.0f, 0.0f), ahi = make_float2(0.0f, 0.0f);
+    for (int cb = c0; cb <= c1; cb += kCombChunkWarp) {
+      float mv[kCombChunkWarp], lv[kCombChunkWarp];
+      float2 xl[kCombChunkWarp], xh[kCombChunkWarp];
 #pragma unroll
-  for (int i = 0; i < kCombRows; ++i) {
-    M[i] = -INFINITY;
-    lsum[i] = 0.0f;
-    a[i] = 0.0f;
-  }
-  for (int cb = c0; cb <= c1; cb += 8) {
-    float mv[kCombRows][8], lv[kCombRows][8], av[kCombRows][8];
-#pragma unroll
-    for (int i = 0; i < kCombRows; ++i) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (i < nr && cb + k <= c1) {
-          const float* src = p.partials + ((size_t)(cb + k + seg) * R + r0 + i) * kPartialStride;
-          mv[i][k] = src[0];
-          lv[i][k] = src[1];
-          av[i][k] = src[2 + d];
+      for (int k = 0; k < kCombChunkWarp; ++k) {
+        if (cb + k <= c1) {
+          const float* src = p.partials + ((size_t)(cb + k + seg) * R + row) * kPartialStride;
+          mv[k] = src[0];
+          lv[k] = src[1];
+          xl[k] = *reinterpret_cast<const float2*>(src + 2 + 2 * lane);
+          xh[k] = *reinterpret_cast<const float2*>(src + 66 + 2 * lane);
         } else {
-          mv[i][k] = -INFINITY;
-          lv[i][k] = 0.0f;
-          av[i][k] = 0.0f;
+          mv[k] = -INFINITY;
+          lv[k] = 0.0f;
+          xl[k] = xh[k] = make_float2(0.0f, 0.0f);
         }
       }
+      float Mc = mv[0];
+#pragma unroll
+      for (int k = 1; k < kCombChunkWarp; ++k) Mc = fmaxf(Mc, mv[k]);
+      if (Mc == -INFINITY) continue;  // nothing visible in this chunk
+      float lc = 0.0f;
+      float2 cl = make_float2(0.0f, 0.0f), ch = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < kCombChunkWarp; ++k) {
+        const float w = fast_exp2(mv[k] - Mc);
+        lc += w * lv[k];
+        cl.x += w * xl[k].x;
+        cl.y += w * xl[k].y;
+        ch.x += w * xh[k].x;
+        ch.y += w * xh[k].y;
+      }
+      if (M == -INFINITY) {
+        M = Mc;
+        lsum = lc;
+        alo = cl;
+        ahi = ch;
+      } else {
+        const float Mn = fmaxf(M, Mc);
+        const float so = fast_exp2(M - Mn), sc = fast_exp2(Mc - Mn);
+        lsum = lsum * so + lc * sc;
+        alo.x = alo.x * so + cl.x * sc;
+        alo.y = alo.y * so + cl.y * sc;
+        ahi.x = ahi.x * so + ch.x * sc;
+        ahi.y = ahi.y * so + ch.y * sc;
+        M = Mn;
+      }
     }
+    const int r = row / p.G, gi = row - (row / p.G) * p.G;
+    float* dst = p.out + (((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD;
+    reinterpret_cast<float2*>(dst)[lane] = make_float2(alo.x / lsum, alo.y / lsum);
+    reinterpret_cast<float2*>(dst + 64)[lane] = make_float2(ahi.x / lsum, ahi.y / lsum);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(128, 4) combine_kernel(const AttnParams p) {
+  extern __shared__ __align__(16) int cpre[];
+  volatile int* flags = cpre + p.B + 1;
+  build_prefix(p, FMT, cpre, flags);
+  griddep_wait();
+  griddep_launch_dependents();
+  __syncthreads();
+  const int R = p.R;
+  const int n_items = p.B * p.Hkv * R;
+  const long long P = (long long)p.Hkv * cpre[p.B];
+  const int n_eff = (int)min((long long)p.n_cta, P);
+  const int d = threadIdx.x;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int seg = item / R, row = item - seg * R;
+    const int b = seg / p.Hkv, h = seg - (seg / p.Hkv) * p.Hkv;
+    const int np = cpre[b + 1] - cpre[b];
+    const long long first_pg = (long long)p.Hkv * cpre[b] + (long long)h * np;
+    const int c0 = (int)cta_of(first_pg, P, n_eff), c1 = (int)cta_of(first_pg + np - 1, P, n_eff);
+    float M = -INFINITY, lsum = 0.0f, a = 0.0f;
+    for (int cb = c0; cb <= c1; cb += kCombChunkBlock) {
+      float mv[kCombChunkBlock], lv[kCombChunkBlock], av[kCombChunkBlock];
 #pragma unroll
-    for (int i = 0; i < kCombRows; ++i) {
-      float Mc = mv[i][0];
+      for (int k = 0; k < kCombChunkBlock; ++k) {
+        if (cb + k <= c1) {
+          const float* src = p.partials + ((size_t)(cb + k + seg) * R + row) * kPartialStride;
+          mv[k] = src[0];
+          lv[k] = src[1];
+          av[k] = src[2 + d];
+        } else {
+          mv[k] = -INFINITY;
+          lv[k] = 0.0f;
+          av[k] = 0.0f;
+        }
+      }
+      float Mc = mv[0];
 #pragma unroll
-      for (int k = 1; k < 8; ++k) Mc = fmaxf(Mc, mv[i][k]);
+      for (int k = 1; k < kCombChunkBlock; ++k) Mc = fmaxf(Mc, mv[k]);
       if (Mc == -INFINITY) continue;  // nothing visible in this chunk
       float lc = 0.0f, ac = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float w = fast_exp2(mv[i][k] - Mc);
-        lc += w * lv[i][k];
-        ac += w * av[i][k];
+      for (int k = 0; k < kCombChunkBlock; ++k) {
+        const float w = fast_exp2(mv[k] - Mc);
+        lc += w * lv[k];
+        ac += w * av[k];
       }
-      if (M[i] == -INFINITY) {
-        M[i] = Mc;
-        lsum[i] = lc;
-        a[i] = ac;
+      if (M == -INFINITY) {
+        M = Mc;
+        lsum = lc;
+        a = ac;
       } else {
-        const float Mn = fmaxf(M[i], Mc);
-        const float so = fast_exp2(M[i] - Mn), sc = fast_exp2(Mc - Mn);
-        lsum[i] = lsum[i] * so + lc * sc;
-        a[i] = a[i] * so + ac * sc;
-        M[i] = Mn;
+        const float Mn = fmaxf(M, Mc);
+        const float so = fast_exp2(M - Mn), sc = fast_exp2(Mc - Mn);
+        lsum = lsum * so + lc * sc;
+        a = a * so + ac * sc;
+        M = Mn;
       }
     }
-  }
-#pragma unroll
-  for (int i = 0; i < kCombRows; ++i) {
-    if (i < nr) {
-      const int row = r0 + i;
-      const int r = row / p.G, gi = row - (row / p.G) * p.G;
-      p.out[(((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + d] = a[i] / lsum[i];
-    }
-  }
+    const int r = row / p.G, gi = row - (row / p.G) * p.G;
+    p.out[(((size_t)b * p.S + r) * p.Hq + h * p.G + gi) * kD + d] = a / lsum;
   }
 }
 
-// Rows per combine item: 4 once one row per item would need more than one wave of blocks.
-int combine_rows(const AttnParams& p, int sm) {
-  return (long long)p.B * p.Hkv * p.R > 4LL * sm ? kCombRowsMax : 1;
-}
-
-// Combine launch: the work items over at most 4 blocks per SM (one wave at 128 registers a thread).
+// Combine launch: a block per item while the items fit in one wave of 4 blocks per SM, else a
+// warp per item over at most one wave.
 template <int FMT>
 cudaError_t launch_combine(cudaLaunchConfig_t& cfg, const AttnParams& p, int sm) {
-  const int cr = combine_rows(p, sm);
-  const long long items = (long long)p.B * p.Hkv * ((p.R + cr - 1) / cr);
-  cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>(items, 4LL * sm)), 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  const long long items = (long long)p.B * p.Hkv * p.R;
   cfg.dynamicSmemBytes = (p.B + 1 + 4) * sizeof(int);
-  return cr == 1 ? cudaLaunchKernelEx(&cfg, combine_kernel<FMT, 1>, p)
-                 : cudaLaunchKernelEx(&cfg, combine_kernel<FMT, kCombRowsMax>, p);
+  if (items <= 4LL * sm) {
+    cfg.gridDim = dim3((unsigned)std::max<long long>(1, items), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<FMT>, p);
+  }
+  cfg.gridDim = dim3((unsigned)std::min<long long>((items + kCombWarps - 1) / kCombWarps, 4LL * sm), 1, 1);
+  cfg.blockDim = dim3(kCombWarps * 32, 1, 1);
+  return cudaLaunchKernelEx(&cfg, combine_rows_kernel<FMT>, p);
 }
 
 struct DevCache {

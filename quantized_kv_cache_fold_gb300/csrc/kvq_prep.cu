@@ -30,20 +30,14 @@ constexpr int kPrepThreads = kPrepWarps * 32;
 // every pass is one row (4-byte loads, lanes' rows on distinct banks; fewer wavefronts per load
 // than 16-byte loads of one row, the faster form for decode's few rows).
 constexpr int kMStride = 132;  // the larger: shared-memory size
-// Rows per warp and pass of the matrix prologue (1, 2, 4 or 8, from the call's row counts):
-// each matrix entry read from shared memory serves all of them, and row pairs share one
-// fma.rn.f32x2. One row per pass is bound by the matrix reads.
+// Rows per warp and pass of the matrix prologue (1 to 8, from the call's row counts, see
+// launch_prep): each matrix entry read from shared memory serves all of them, and row pairs
+// share one fma.rn.f32x2. One row per pass is bound by the matrix reads.
 constexpr int kMaxRows = 8;
 constexpr int kPrepSmem = (128 * kMStride + kPrepWarps * 128 * kMaxRows) * 4;  // the most a launch asks for
 // Shared memory of a launch: the matrix rows and each warp's normalised rows, no more (a prep
 // grid starts while the previous grid's blocks still hold shared memory on the SMs).
 inline int prep_smem(int mstride, int rows) { return (128 * mstride + kPrepWarps * 128 * rows) * 4; }
-
-// Smallest of 1, 2, 4, 8 that covers `rows` rows per warp in one pass (8 at most).
-inline int rows_per_pass(long long rows, long long warps) {
-  const long long per = (rows + warps - 1) / std::max(1LL, warps);
-  return per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
-}
 
 struct PrepParams {
   PrepJobs j;
@@ -97,9 +91,11 @@ __device__ __forceinline__ void prologue_fwht(const float4 w, const float (&x)[4
 // Lane l holds x[r][4l..4l+3] and returns y[r][u] = row r's output l + 32u, u = 0..3, each the
 // fma chain over k = 0..127 in order, acc = fma(M[l + 32u][k], n[k], acc) from 0, with
 // n = fp32(x / sqrt(mean(x^2) + eps)) (norm_inv's order). Rows 2p and 2p + 1 run in the two
-// halves of one fma.rn.f32x2, which rounds each half as fma.rn.f32: the chains are unchanged.
+// halves of one fma.rn.f32x2, which rounds each half as fma.rn.f32: the chains are unchanged;
+// the last row of an odd R > 1 runs as a plain fma.rn.f32 chain in the same order.
 // Ms: shared [128][ms], Ms[j ms + k] = M[j][k] (ms = 129 or 132); nbuf: shared float[R][128] of this
-// warp (R = 1: n; R even: pair p at float 256 p, element k of rows 2p, 2p + 1 side by side).
+// warp (R = 1: n; R > 1: pair p at float 256 p, element k of rows 2p, 2p + 1 side by side, then
+// the odd row's n at float 256 (R / 2)).
 template <int R>
 __device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, int ms, float* nbuf, const float (&x)[R][4],
                                               int nr, float eps, int lane, float (&y)[R][4]) {
@@ -123,6 +119,9 @@ __device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, int 
       d[0] = make_float4(nx[2 * pr][0], nx[2 * pr + 1][0], nx[2 * pr][1], nx[2 * pr + 1][1]);
       d[1] = make_float4(nx[2 * pr][2], nx[2 * pr + 1][2], nx[2 * pr][3], nx[2 * pr + 1][3]);
     }
+    if constexpr ((R & 1) != 0)
+      reinterpret_cast<float4*>(nbuf + (R / 2) * 256)[lane] =
+          make_float4(nx[R - 1][0], nx[R - 1][1], nx[R - 1][2], nx[R - 1][3]);
   }
   __syncwarp();
   const float* m0 = Ms + lane * ms;
@@ -155,14 +154,27 @@ __device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, int 
 #pragma unroll
     for (int c = 0; c < 4; ++c) y[0][c] = a[c];
   } else {
+    constexpr int RO = R & 1;  // the odd row's plain chain
     uint64_t a2[R / 2][4];
+    float a1[RO + 1][4];
 #pragma unroll
     for (int pr = 0; pr < R / 2; ++pr) a2[pr][0] = a2[pr][1] = a2[pr][2] = a2[pr][3] = 0ull;
+    a1[0][0] = a1[0][1] = a1[0][2] = a1[0][3] = 0.0f;
 #pragma unroll 2
     for (int k = 0; k < kD; k += 4) {
       float4 m[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) m[c] = *reinterpret_cast<const float4*>(m0 + 32 * c * ms + k);
+      if constexpr (RO != 0) {
+        const float4 n4 = reinterpret_cast<const float4*>(nbuf + (R / 2) * 256)[k >> 2];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          a1[0][c] = __fmaf_rn(m[c].x, n4.x, a1[0][c]);
+          a1[0][c] = __fmaf_rn(m[c].y, n4.y, a1[0][c]);
+          a1[0][c] = __fmaf_rn(m[c].z, n4.z, a1[0][c]);
+          a1[0][c] = __fmaf_rn(m[c].w, n4.w, a1[0][c]);
+        }
+      }
 #pragma unroll
       for (int pr = 0; pr < R / 2; ++pr) {
         const float4 n01 = reinterpret_cast<const float4*>(nbuf + pr * 256)[k >> 1];      // k, k + 1
@@ -184,6 +196,9 @@ __device__ __forceinline__ void prologue_rows(const float* __restrict__ Ms, int 
         y[2 * pr][c] = f2lo(a2[pr][c]);
         y[2 * pr + 1][c] = f2hi(a2[pr][c]);
       }
+    if constexpr (RO != 0)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[R - 1][c] = a1[0][c];
   }
   __syncwarp();
 }
@@ -375,12 +390,13 @@ __device__ __forceinline__ void q_rows_matrix(const PrepParams& p, const float* 
   }
 }
 
-// R: query rows per warp and pass (1, 2, 4 or 8); key/value passes take min(R, 4) jobs. One
-// instantiation per R keeps each launch's code to its own path (the decode launch, R = 1, is a
-// short latency-bound grid).
-template <int R>
+// RQ: query rows per warp and pass, RKV: key/value jobs per warp and pass (at most 4: a pass holds
+// key, value and output rows), with the matrix prologue; one of each with the FWHT one. One
+// instantiation per shape keeps each launch's code to its own path (the decode launch, 1 and 1,
+// is a short latency-bound grid).
+template <int RQ, int RKV>
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrepParams p) {
-  constexpr int RKV = R < 4 ? R : 4;
+  static_assert(RQ >= 1 && RQ <= kMaxRows && RKV >= 1 && RKV <= 4, "prep pass shapes");
   extern __shared__ __align__(16) float smem_f[];
   float* Ms = smem_f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -469,7 +485,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrepParams 
       }
       return;
     }
-    q_rows_matrix<R>(p, Ms, nbuf, qb, nqb, warp, lane);
+    q_rows_matrix<RQ>(p, Ms, nbuf, qb, nqb, warp, lane);
   }
 }
 
@@ -510,7 +526,20 @@ __global__ void fp8_append_kernel(const Fp8AppendJob j) {
 
 std::mutex g_prep_mu;  // guards the per-device caches below
 int g_sm_count[64] = {0};
-bool g_prep_attr[64][4] = {{false}};  // per device and instantiation (R = 1, 2, 4, 8)
+// Pass shapes (query rows, key/value jobs per warp and pass) of the matrix prologue's
+// instantiations; the FWHT prologue takes the first.
+struct PrepShape {
+  int rq, rkv;
+  const void* kern;
+};
+const PrepShape kPrepShapes[] = {
+    {1, 1, (const void*)prep_kernel<1, 1>}, {2, 1, (const void*)prep_kernel<2, 1>},
+    {2, 2, (const void*)prep_kernel<2, 2>}, {3, 2, (const void*)prep_kernel<3, 2>},
+    {4, 2, (const void*)prep_kernel<4, 2>}, {4, 3, (const void*)prep_kernel<4, 3>},
+    {6, 4, (const void*)prep_kernel<6, 4>}, {8, 4, (const void*)prep_kernel<8, 4>},
+};
+constexpr int kNumPrepShapes = (int)(sizeof(kPrepShapes) / sizeof(kPrepShapes[0]));
+bool g_prep_attr[64][kNumPrepShapes] = {{false}};  // per device and instantiation
 
 int sm_count() {
   int dev = 0;
@@ -527,50 +556,89 @@ int sm_count() {
 
 }  // namespace
 
+// Work of a key/value job against a query row in the matrix prologue: the same matrix product,
+// plus two quantisations (the key's and the value's).
+constexpr double kKvWeight = 1.5;
+
+// Largest work (query rows, key/value jobs weighted kKvWeight) that one SM receives from a grid
+// of kvb key/value blocks then qb query blocks, dealt round robin over sm SMs (block i shares
+// an SM with block i + sm), each warp taking rkv jobs or rq rows; the matrix product makes the
+// kernel bound by the SM's FMA throughput once several passes share it.
+double prep_sm_load(long long kv_jobs, long long q_jobs, int kvb, int qb, int rkv, int rq, int sm) {
+  auto block_load = [&](long long i) -> double {
+    if (i < kvb) return kKvWeight * (double)std::min<long long>(kPrepWarps * rkv, kv_jobs - i * kPrepWarps * rkv);
+    i -= kvb;
+    return (double)std::min<long long>(kPrepWarps * rq, q_jobs - i * kPrepWarps * rq);
+  };
+  const long long n = (long long)kvb + qb;
+  double worst = 0.0;
+  for (long long s = 0; s < std::min<long long>(n, sm); ++s)
+    worst = std::max(worst, block_load(s) + (s + sm < n ? block_load(s + sm) : 0.0));
+  return worst;
+}
+
 cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
   PrepParams p;
   p.j = jobs;
   p.kv_jobs = jobs.k ? jobs.T * jobs.cache.num_kv_heads : 0;
   p.q_jobs = jobs.q ? jobs.nq_rows : 0;
   if (p.kv_jobs == 0 && p.q_jobs == 0) return cudaSuccess;
-  // One wave: two blocks per SM (shared memory), shared between key/value and query work in
-  // proportion to rows (a key/value job counted as 1.5 query rows: its two quantisations).
-  const int cap = 2 * sm_count();
-  const int kv_max = (p.kv_jobs + kPrepWarps - 1) / kPrepWarps, q_max = (p.q_jobs + kPrepWarps - 1) / kPrepWarps;
-  int q_blocks;
-  if (kv_max + q_max <= cap) {
-    p.kv_blocks = kv_max;
-    q_blocks = q_max;
+  const int sm = sm_count();
+  const int cap = 2 * sm;  // one wave: two blocks per SM (shared memory)
+  int shape = 0, q_blocks = 0;
+  if (jobs.fwht) {
+    // one row per warp and pass; blocks shared between the roles in proportion to work
+    const int kv_max = (p.kv_jobs + kPrepWarps - 1) / kPrepWarps, q_max = (p.q_jobs + kPrepWarps - 1) / kPrepWarps;
+    if (kv_max + q_max <= cap) {
+      p.kv_blocks = kv_max;
+      q_blocks = q_max;
+    } else {
+      const double wkv = kKvWeight * p.kv_jobs, wq = p.q_jobs;
+      p.kv_blocks = std::min(kv_max, std::max(p.kv_jobs ? 1 : 0, (int)(cap * wkv / (wkv + wq) + 0.5)));
+      q_blocks = std::min(q_max, std::max(p.q_jobs ? 1 : 0, cap - p.kv_blocks));
+    }
   } else {
-    const double wkv = 1.5 * p.kv_jobs, wq = p.q_jobs;
-    p.kv_blocks = std::min(kv_max, std::max(p.kv_jobs ? 1 : 0, (int)(cap * wkv / (wkv + wq) + 0.5)));
-    q_blocks = std::min(q_max, std::max(p.q_jobs ? 1 : 0, cap - p.kv_blocks));
+    // the pass shape whose grid (one pass per warp) fits one wave with the least work on any SM,
+    // then the fewest rows per pass (a pass's latency grows with its rows); calls too large for
+    // one wave take the largest shape, several passes per warp, blocks shared in proportion to work
+    double best = 0.0;
+    shape = -1;
+    for (int i = 0; i < kNumPrepShapes; ++i) {
+      const int rq = kPrepShapes[i].rq, rkv = kPrepShapes[i].rkv;
+      const int kvb = (p.kv_jobs + kPrepWarps * rkv - 1) / (kPrepWarps * rkv);
+      const int qb = (p.q_jobs + kPrepWarps * rq - 1) / (kPrepWarps * rq);
+      if (kvb + qb > cap) continue;
+      const double load = prep_sm_load(p.kv_jobs, p.q_jobs, kvb, qb, rkv, rq, sm);
+      if (shape < 0 || load < best) {
+        best = load;
+        shape = i;
+        p.kv_blocks = kvb;
+        q_blocks = qb;
+      }
+    }
+    if (shape < 0) {
+      shape = kNumPrepShapes - 1;
+      const int rq = kPrepShapes[shape].rq, rkv = kPrepShapes[shape].rkv;
+      const int kv_max = (p.kv_jobs + kPrepWarps * rkv - 1) / (kPrepWarps * rkv);
+      const int q_max = (p.q_jobs + kPrepWarps * rq - 1) / (kPrepWarps * rq);
+      const double wkv = kKvWeight * p.kv_jobs, wq = p.q_jobs;
+      p.kv_blocks = std::min(kv_max, std::max(p.kv_jobs ? 1 : 0, (int)(cap * wkv / (wkv + wq) + 0.5)));
+      q_blocks = std::min(q_max, std::max(p.q_jobs ? 1 : 0, cap - p.kv_blocks));
+    }
   }
-  // rows per pass: enough for one pass per warp; the kernel takes R = the larger of the two
-  // roles' needs for query passes and min(R, 4) for key/value passes (a key/value pass holds key,
-  // value and output rows: at most 4 jobs, so nothing spills)
-  const int R = jobs.fwht ? 1
-                          : std::max(rows_per_pass(p.q_jobs, (long long)q_blocks * kPrepWarps),
-                                     std::min(4, rows_per_pass(p.kv_jobs, (long long)p.kv_blocks * kPrepWarps)));
-  p.q_rows = R;
-  p.kv_rows = std::min(R, 4);
+  p.q_rows = kPrepShapes[shape].rq;
+  p.kv_rows = kPrepShapes[shape].rkv;
   p.mstride = p.kv_rows == 1 && p.q_rows == 1 ? 129 : kMStride;
   p.nrows = std::max(p.kv_rows, p.q_rows);
-  if (!jobs.fwht) {  // blocks whose warps would have no pass
-    p.kv_blocks = std::min(p.kv_blocks, (p.kv_jobs + kPrepWarps * p.kv_rows - 1) / (kPrepWarps * p.kv_rows));
-    q_blocks = std::min(q_blocks, (p.q_jobs + kPrepWarps * p.q_rows - 1) / (kPrepWarps * p.q_rows));
-  }
-  const void* kern = R == 8 ? (const void*)prep_kernel<8> : R == 4 ? (const void*)prep_kernel<4>
-                   : R == 2 ? (const void*)prep_kernel<2> : (const void*)prep_kernel<1>;
-  const int ri = R == 8 ? 3 : R == 4 ? 2 : R == 2 ? 1 : 0;
+  const void* kern = kPrepShapes[shape].kern;
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(g_prep_mu);
-    if (dev < 0 || dev >= 64 || !g_prep_attr[dev][ri]) {
+    if (dev < 0 || dev >= 64 || !g_prep_attr[dev][shape]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) g_prep_attr[dev][ri] = true;
+      if (dev >= 0 && dev < 64) g_prep_attr[dev][shape] = true;
     }
   }
   cudaLaunchConfig_t cfg{};
