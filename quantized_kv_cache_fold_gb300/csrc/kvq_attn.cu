@@ -317,9 +317,11 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   const int nwc = p.ntg * p.nkg;
   const int nst = p.nstages;
 
-  // launched with programmatic serialisation: nothing is read before the previous grid is done
-  griddep_wait();
-  griddep_launch_dependents();
+  // Launched with programmatic serialisation: the setup runs while the previous grid (the call's
+  // prologue/append kernel, or the window append) finishes. It reads only context lengths (the
+  // page prefix): no kernel of the call writes them, and the grids before the previous one
+  // completed before this grid could launch. Everything after the setup waits for the previous
+  // grid.
   build_prefix(p, FMT, pre, flags);
   if (threadIdx.x < nst) {
     mbar_init(&full[threadIdx.x], 1);
@@ -327,6 +329,8 @@ __global__ void __maxnreg__(NT == 1 ? (FMT == 0 ? KVQ_INT4_MAXREG : 184) : 255)
   }
   fence_barrier_init();
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
   const long long P = (long long)p.Hkv * pre[p.B];
@@ -975,8 +979,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   constexpr uint32_t kFinBar = 1;
   constexpr int kGrp = 128, kFinThreads = 14 * 32;
 
-  griddep_wait();
-  griddep_launch_dependents();
+  // The setup (page prefix from the context lengths, barriers, Q' padding, tensor memory) runs
+  // while the previous grid, the call's prologue/append kernel, finishes; see attn_kernel. Every
+  // grid before it has completed, so no earlier kernel of the stream still holds tensor memory.
   build_prefix(p, 0, pre, flags);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -1005,6 +1010,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnParams
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *taddr_s;
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (blockIdx.x == 0 && threadIdx.x == 0 && flags[1]) set_err(p.dev_err, KVQ_DEVERR_POS);
   const long long P = (long long)p.Hkv * pre[p.B];
