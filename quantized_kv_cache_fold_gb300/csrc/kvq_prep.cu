@@ -536,7 +536,8 @@ const PrepShape kPrepShapes[] = {
     {1, 1, (const void*)prep_kernel<1, 1>}, {2, 1, (const void*)prep_kernel<2, 1>},
     {2, 2, (const void*)prep_kernel<2, 2>}, {3, 2, (const void*)prep_kernel<3, 2>},
     {4, 2, (const void*)prep_kernel<4, 2>}, {4, 3, (const void*)prep_kernel<4, 3>},
-    {6, 4, (const void*)prep_kernel<6, 4>}, {8, 4, (const void*)prep_kernel<8, 4>},
+    {6, 3, (const void*)prep_kernel<6, 3>}, {6, 4, (const void*)prep_kernel<6, 4>},
+    {8, 4, (const void*)prep_kernel<8, 4>},
 };
 constexpr int kNumPrepShapes = (int)(sizeof(kPrepShapes) / sizeof(kPrepShapes[0]));
 bool g_prep_attr[64][kNumPrepShapes] = {{false}};  // per device and instantiation
@@ -554,11 +555,11 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
-}  // namespace
-
 // Work of a key/value job against a query row in the matrix prologue: the same matrix product,
-// plus two quantisations (the key's and the value's).
-constexpr double kKvWeight = 1.5;
+// plus two quantisations (the key's and the value's), the row loads and the slot look-up;
+// measured per block on 64 x 16,384 tokens at S = 8 (4 jobs per warp 14.5 us, 6 query rows per
+// warp 11.3 us): about 2.
+constexpr double kKvWeight = 2.0;
 
 // Largest work (query rows, key/value jobs weighted kKvWeight) that one SM receives from a grid
 // of kvb key/value blocks then qb query blocks, dealt round robin over sm SMs (block i shares
@@ -576,6 +577,8 @@ double prep_sm_load(long long kv_jobs, long long q_jobs, int kvb, int qb, int rk
     worst = std::max(worst, block_load(s) + (s + sm < n ? block_load(s + sm) : 0.0));
   return worst;
 }
+
+}  // namespace
 
 cudaError_t launch_prep(const PrepJobs& jobs, cudaStream_t stream) {
   PrepParams p;

@@ -5,10 +5,10 @@ rotated and quantised to 4-bit codes, values quantised unrotated, and queries ca
 rotation with both QK-norm gains folded in. The prep launch deals these rows to warps in passes
 of 1 to 8 query rows and 1 to 4 key/value jobs, chosen from the call's row counts; an odd
 count runs its last row as a plain fp32 chain beside the paired ones. On a 152-SM GPU the
-cases below take the shapes (query rows, key/value jobs) (2, 1), (3, 2), (4, 3), (3, 2),
-(4, 2) and (6, 4) in one wave, and (8, 4) with several passes per warp (more rows than one
-wave holds). Every case checks the codes and q~ bit-exact and the attention within the
-oracle's tolerance, on short ragged contexts in random page order.
+cases below take the shapes (query rows, key/value jobs) (1, 1), (2, 1), (2, 2), (3, 2),
+(4, 2), (4, 3), (6, 3), (6, 4) and (8, 4) in one wave, and (8, 4) with several passes per warp
+(more rows than one wave holds). Every case checks the codes and q~ bit-exact and the
+attention within the oracle's tolerance, on short ragged contexts in random page order.
 """
 
 import numpy as np
@@ -20,7 +20,8 @@ from synth.workloads import Workload
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,S", [(64, 1), (64, 2), (64, 3), (64, 4), (64, 5), (64, 8), (128, 8)])
+@pytest.mark.parametrize("B,S", [(8, 1), (64, 1), (180, 1), (130, 2), (64, 5), (180, 2), (64, 8), (180, 3),
+                                 (190, 3), (128, 8)])
 def test_prep_pass_shapes(orc, B, S):
     ctx = np.random.default_rng(1000 + 10 * B + S).integers(0, 260, B).astype(np.int64)
     w = Workload("prep", 31 + S, B, 20, 4, S, ctx, S % 2 == 0, page_order="random")
