@@ -225,10 +225,10 @@ class Stack256k:
 # is that ratio times its own algorithmic bytes (traffic grows with the pages read). The
 # counters belong to the kernel sources whose hash is recorded; after any change to them the
 # traffic is reported as null until a new capture.
-ATTN_CAPTURE = {"dram_read": 906337792, "dram_write": 3215872, "algorithmic": 905157248,
+ATTN_CAPTURE = {"dram_read": 906257408, "dram_write": 3086080, "algorithmic": 905157248,
                 "sources": ["quantized_kv_cache_fold_gb300/csrc/kvq_attn.cu",
                             "quantized_kv_cache_fold_gb300/csrc/kvq_device.cuh"],
-                "sources_sha256_16": "ba3e02fee8c254c1"}
+                "sources_sha256_16": "06bd601516a68f61"}
 
 
 def attn_traffic(call_bytes):
